@@ -1,0 +1,502 @@
+"""Ozaki scheme II over base-13 FP4 limbs: the method's stages, written plainly.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Stage order follows the sources:
+
+1. [TME4] abstract -- each fp64 row of A (column of B) is scaled by a power of
+   two, rounded to an integer and reduced modulo each of r moduli.
+2. [AWE] abstract -- each residue splits, with carries, into base-13 digits
+   drawn from S = {0, +-1, +-2, +-3, +-4, +-6, +-8, +-12} (FP4 e2m1 values
+   times two); three limbs with weights (1, 13, 169).
+3. [AWE] abstract -- the limbs multiply pairwise: 9 FP4 GEMMs, each exact.
+4. [AWE] abstract ("also holds modulo m") and [TME4] abstract (per-output
+   reconstruction) -- recombine the 9 products modulo m, rebuild the integer
+   product by the Chinese remainder theorem, scale back to fp64.
+
+Readings where the sources are silent (each one also listed in the design
+notes): moduli are the greedy pairwise-coprime integers descending from 256;
+balanced residues lie in [-floor(m/2), ceil(m/2) - 1]; the bit budget P is the
+largest integer with 2 K 2^P < prod(m), split p_A = ceil(P/2), p_B = floor(P/2);
+the scale exponent of a row is the frexp exponent of its largest magnitude;
+rounding to integer is round-half-to-even; the two digits that have two
+representatives in S take the one of smaller magnitude; the fp64 result is the
+single correct rounding of C' 2^-(s_i + t_j).
+
+Parity pins (tests/test_oracle_pins.py): S against residues mod 13 and the
+e2m1 definition; exhaustive int8 limb round trip; greedy moduli by brute force;
+vectorised rounding against exact Fractions; CRT round trips and brute force on
+small moduli; limb GEMMs against a triple loop and closed forms; the modular
+recombination against a direct modular product; the full product against the
+exact rational product, the error bound and exactly representable cases.
+"""
+
+from fractions import Fraction
+import math
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# Constants fixed by the sources
+# ----------------------------------------------------------------------------
+
+#: FP4 (e2m1) values scaled by two -- [AWE] abstract.
+S = (0, 1, -1, 2, -2, 3, -3, 4, -4, 6, -6, 8, -8, 12, -12)
+#: Digit base and limb weights -- [AWE] abstract.
+BASE = 13
+LIMB_WEIGHTS = (1, 13, 169)
+N_LIMBS = 3
+#: Largest modulus: keeps every balanced residue inside int8 (reading).
+MODULUS_CEILING = 256
+
+
+# ----------------------------------------------------------------------------
+# Stage 0: moduli and bit budget (reading of [TME4] abstract; configs)
+# ----------------------------------------------------------------------------
+
+def moduli(r):
+    """First ``r`` greedy pairwise-coprime integers counting down from 256.
+
+    The sources name no moduli.  Reading: take each integer from 256 down
+    that is coprime to every modulus already taken.
+    """
+    if r < 1:
+        raise ValueError("r must be >= 1")
+    out = []
+    m = MODULUS_CEILING
+    while len(out) < r:
+        if m < 2:
+            raise ValueError("ran out of moduli")
+        if all(math.gcd(m, q) == 1 for q in out):
+            out.append(m)
+        m -= 1
+    return out
+
+
+def modulus_product(r):
+    """Product of the first ``r`` moduli, as a Python int."""
+    prod = 1
+    for m in moduli(r):
+        prod *= m
+    return prod
+
+
+def bit_budget(k, r):
+    """Return (P, p_A, p_B): P is the largest integer with 2 k 2^P < M.
+
+    |A'| <= 2^p_A and |B'| <= 2^p_B then give |sum_k A'B'| <= k 2^P < M/2,
+    so the product is recoverable from its residues.  Raises ValueError when
+    not even P = 0 fits.
+    """
+    if k < 1:
+        raise ValueError("k must be >= 1")
+    M = modulus_product(r)
+    if not (2 * k * 1 < M):
+        raise ValueError("modulus product too small for this k")
+    P = 0
+    while 2 * k * 2 ** (P + 1) < M:
+        P += 1
+    return P, (P + 1) // 2, P // 2
+
+
+# ----------------------------------------------------------------------------
+# Stage 1: scale, round, reduce ([TME4] abstract)
+# ----------------------------------------------------------------------------
+
+def frexp_exponent(x):
+    """e with 2^(e-1) <= |x| < 2^e (frexp exponent); None for zero."""
+    if x == 0:
+        return None
+    return math.frexp(float(x))[1]
+
+
+def row_shifts(X, p):
+    """Power-of-two shift s_i = p - e_i per row of X (0 for an all-zero row).
+
+    e_i is the frexp exponent of max_k |X_ik|, so |X_ik 2^s_i| < 2^p.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    out = np.zeros(X.shape[0], dtype=np.int64)
+    for i in range(X.shape[0]):
+        mx = float(np.max(np.abs(X[i]))) if X.shape[1] else 0.0
+        e = frexp_exponent(mx)
+        out[i] = 0 if e is None else p - e
+    return out
+
+
+def scale_round_scalar(x, s):
+    """round-half-to-even(x 2^s), computed exactly with Fractions."""
+    return round(Fraction(float(x)) * Fraction(2) ** int(s))
+
+
+def scale_round(X, shifts):
+    """Vectorised round-half-to-even(X_ik 2^s_i) as int64 (|result| <= 2^62).
+
+    Exact integer arithmetic on the significand: x = q 2^(e-53) with q the
+    53-bit integer significand from frexp, then a left shift or a rounded right
+    shift.  Pinned against :func:`scale_round_scalar`.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    s = np.asarray(shifts, dtype=np.int64).reshape(-1, 1)
+    mant, e = np.frexp(X)
+    q = (np.abs(mant) * 2.0 ** 53).astype(np.int64)  # exact, < 2^53
+    sh = e.astype(np.int64) - 53 + s
+    sh = np.broadcast_to(sh, X.shape)
+    out = np.zeros(X.shape, dtype=np.int64)
+    left = sh >= 0
+    if np.any(left):
+        if np.any(np.ldexp(q[left].astype(np.float64), sh[left]) > 2.0 ** 62):
+            raise OverflowError("scaled integer exceeds 2^62")
+        out[left] = q[left] << sh[left]
+    right = ~left
+    if np.any(right):
+        d = np.minimum(-sh[right], 62)
+        qq = q[right]
+        qd = qq >> d
+        rem = qq & ((np.int64(1) << d) - 1)
+        half = np.int64(1) << (d - 1)
+        up = (rem > half) | ((rem == half) & ((qd & 1) == 1))
+        out[right] = qd + up.astype(np.int64)
+    return np.where(X < 0, -out, out)
+
+
+def balanced_residue(x, m):
+    """Residue of integer x modulo m in [-floor(m/2), ceil(m/2) - 1]."""
+    v = int(x) % m
+    if v > (m - 1) // 2:
+        v -= m
+    return v
+
+
+def balanced_residue_array(X, m):
+    """Element-wise :func:`balanced_residue` on an int64 array."""
+    v = np.mod(np.asarray(X, dtype=np.int64), m)
+    return np.where(v > (m - 1) // 2, v - m, v)
+
+
+# ----------------------------------------------------------------------------
+# Stage 2: base-13 limbs in S and their FP4 codes ([AWE] abstract)
+# ----------------------------------------------------------------------------
+
+def digit_of_class(c):
+    """The element of S congruent to c mod 13 with the smallest magnitude.
+
+    Classes 1 and 12 have two representatives in S (1 / -12 and 12 / -1);
+    the smaller magnitude is taken (reading).
+    """
+    c %= BASE
+    best = None
+    for d in S:
+        if d % BASE == c and (best is None or abs(d) < abs(best)):
+            best = d
+    if best is None:
+        raise ValueError("S does not cover residue class %d" % c)
+    return best
+
+
+def limb_split(x):
+    """Split integer x into (d0, d1, d2), x = d0 + 13 d1 + 169 d2, d_i in S.
+
+    The two low digits are chosen by congruence (with a carry into the next
+    digit); the top digit is what remains and must itself lie in S.
+    """
+    x = int(x)
+    digits = []
+    for _ in range(N_LIMBS - 1):
+        d = digit_of_class(x)
+        digits.append(d)
+        x = (x - d) // BASE
+    if x not in S:
+        raise ValueError("top limb %d not in S" % x)
+    digits.append(x)
+    return tuple(digits)
+
+
+def limb_table_int8():
+    """(256, 3) int64 table: limbs of v for v = -128..127 (row v + 128)."""
+    return np.array([limb_split(v) for v in range(-128, 128)], dtype=np.int64)
+
+
+def limb_digits(X):
+    """Limb digits of an int array with values in [-128, 127]: shape (3, ...)."""
+    X = np.asarray(X, dtype=np.int64)
+    if X.size and (X.min() < -128 or X.max() > 127):
+        raise ValueError("limb_digits expects int8-range values")
+    tab = limb_table_int8()
+    d = tab[X + 128]  # (..., 3)
+    return np.moveaxis(d, -1, 0)
+
+
+def e2m1_value(code):
+    """Value of a 4-bit FP4 e2m1 code: sign, 2-bit exponent (bias 1), 1-bit mantissa."""
+    code = int(code) & 0xF
+    sign = -1.0 if code & 0x8 else 1.0
+    exp = (code >> 1) & 0x3
+    man = code & 0x1
+    if exp == 0:
+        mag = man * 0.5
+    else:
+        mag = 2.0 ** (exp - 1) * (1.0 + man / 2.0)
+    return sign * mag
+
+
+def e2m1_code(d):
+    """The 4-bit e2m1 code holding digit d as the FP4 value d / 2 (0 -> +0)."""
+    target = d / 2.0
+    for code in range(16):
+        if code == 0x8:
+            continue  # -0 is never produced
+        if e2m1_value(code) == target:
+            return code
+    raise ValueError("digit %r is not in S" % (d,))
+
+
+# ----------------------------------------------------------------------------
+# Stage 3: the 9 limb products ([AWE] abstract)
+# ----------------------------------------------------------------------------
+
+def limb_products(Ad, Bd):
+    """P[i][j] = Ad[i] @ Bd[j] for i, j in 0..2, exact, as int64.
+
+    Ad: (3, M, K) digits, Bd: (3, K, N) digits.  Float64 BLAS is exact here
+    because every partial sum is an integer below 2^53 (checked).
+    """
+    Ad = np.asarray(Ad, dtype=np.int64)
+    Bd = np.asarray(Bd, dtype=np.int64)
+    K = Ad.shape[2]
+    amax = int(np.abs(Ad).max()) if Ad.size else 0
+    bmax = int(np.abs(Bd).max()) if Bd.size else 0
+    if K * amax * bmax >= 2 ** 53:
+        raise OverflowError("limb product not exact in float64")
+    P = np.zeros((N_LIMBS, N_LIMBS, Ad.shape[1], Bd.shape[2]), dtype=np.int64)
+    for i in range(N_LIMBS):
+        for j in range(N_LIMBS):
+            P[i, j] = np.rint(Ad[i].astype(np.float64) @ Bd[j].astype(np.float64)).astype(np.int64)
+    return P
+
+
+def mod_recombine(P, m):
+    """c = (sum_{i,j} 13^(i+j) P_ij) mod m, in [0, m)."""
+    acc = np.zeros(P.shape[2:], dtype=np.int64)
+    for i in range(N_LIMBS):
+        for j in range(N_LIMBS):
+            w = LIMB_WEIGHTS[i] * LIMB_WEIGHTS[j]
+            acc = (acc + (w % m) * np.mod(P[i, j], m)) % m
+    return acc
+
+
+def mod_product_direct(a, b, m):
+    """(a @ b) mod m for int residue matrices, without limbs (cross-check)."""
+    a = np.asarray(a, dtype=np.int64)
+    b = np.asarray(b, dtype=np.int64)
+    prod = np.rint(a.astype(np.float64) @ b.astype(np.float64)).astype(np.int64)
+    if a.shape[1] * 128 * 128 >= 2 ** 53:
+        raise OverflowError("direct product not exact in float64")
+    return np.mod(prod, m)
+
+
+# ----------------------------------------------------------------------------
+# Stage 4: CRT and scale back ([AWE] abstract; [TME4] abstract)
+# ----------------------------------------------------------------------------
+
+def crt(residues, mods):
+    """Integer C' in (-M/2, M/2) with C' = residues[l] (mod mods[l]).
+
+    Direct form: X = sum_l c_l (M/m_l) ((M/m_l)^-1 mod m_l) mod M, then the
+    symmetric lift.  M is even (256 is the first modulus) and |C'| < M/2, so
+    X = M/2 cannot occur.
+    """
+    M = 1
+    for m in mods:
+        M *= m
+    X = 0
+    for c, m in zip(residues, mods):
+        Mi = M // m
+        X += int(c) * Mi * pow(Mi % m, -1, m)
+    X %= M
+    return X - M if X > M // 2 else X
+
+
+def crt_array(res, mods):
+    """:func:`crt` over an array of residue vectors: res shape (r, ...)."""
+    M = 1
+    for m in mods:
+        M *= m
+    X = np.zeros(res.shape[1:], dtype=object)
+    for l, m in enumerate(mods):
+        Mi = M // m
+        w = Mi * pow(Mi % m, -1, m)
+        X = X + res[l].astype(object) * w
+    X = X % M
+    return np.where(X > M // 2, X - M, X)
+
+
+def scale_back(Cp, S_shift):
+    """Single correct rounding of Cp 2^-S_shift to fp64 (+-inf on overflow)."""
+    val = Fraction(int(Cp)) / Fraction(2) ** int(S_shift)
+    try:
+        return float(val)
+    except OverflowError:
+        return math.copysign(math.inf, val)
+
+
+def scale_back_array(Cp, sA, sB):
+    """:func:`scale_back` over a matrix: entry (i, j) uses sA[i] + sB[j]."""
+    out = np.empty(Cp.shape, dtype=np.float64)
+    for i in range(Cp.shape[0]):
+        for j in range(Cp.shape[1]):
+            out[i, j] = scale_back(Cp[i, j], int(sA[i]) + int(sB[j]))
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Pipelines
+# ----------------------------------------------------------------------------
+
+def deconstruct(X, p, r):
+    """Stage 1 + 2 for the rows of X: shifts, integers, residues, limb digits.
+
+    Returns dict(shift=(rows,), xint=(rows, k), res=(r, rows, k),
+    digits=(r, 3, rows, k)).
+    """
+    s = row_shifts(X, p)
+    xi = scale_round(X, s)
+    mods = moduli(r)
+    res = np.stack([balanced_residue_array(xi, m) for m in mods]) if r else None
+    digits = np.stack([limb_digits(res[l]) for l in range(r)])
+    return dict(shift=s, xint=xi, res=res, digits=digits)
+
+
+def dgemm_block(A, B, r, rows=None, cols=None, stages=False):
+    """Emulated C[rows][:, cols] = A @ B by the four stages.
+
+    ``rows`` / ``cols`` select a sub-block (default: all).  Row and column
+    exponents always see the full row / column.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    cols = np.arange(N) if cols is None else np.asarray(cols)
+    mods = moduli(r)
+    _, pA, pB = bit_budget(K, r)
+    da = deconstruct(A[rows], pA, r)
+    db = deconstruct(B[:, cols].T, pB, r)  # columns of B as rows
+    res = np.zeros((r, len(rows), len(cols)), dtype=np.int64)
+    for l, m in enumerate(mods):
+        Ad = da["digits"][l]                       # (3, rows, K)
+        Bd = np.swapaxes(db["digits"][l], 1, 2)    # (3, K, cols)
+        res[l] = mod_recombine(limb_products(Ad, Bd), m)
+    Cp = crt_array(res, mods)
+    C = scale_back_array(Cp, da["shift"], db["shift"])
+    if stages:
+        return C, dict(mods=mods, pA=pA, pB=pB, a=da, b=db, res=res, Cp=Cp)
+    return C
+
+
+def dgemm(A, B, r, stages=False):
+    """Emulated fp64 C = A @ B with r moduli (whole matrix)."""
+    return dgemm_block(A, B, r, stages=stages)
+
+
+def igemm_s8(A, B):
+    """Exact int32 C = A @ B of int8 matrices by 9 base-13 limb products."""
+    A = np.asarray(A, dtype=np.int64)
+    B = np.asarray(B, dtype=np.int64)
+    Ad = limb_digits(A)
+    Bd = limb_digits(B)
+    P = limb_products(Ad, Bd)
+    C = np.zeros(P.shape[2:], dtype=np.int64)
+    for i in range(N_LIMBS):
+        for j in range(N_LIMBS):
+            C += LIMB_WEIGHTS[i] * LIMB_WEIGHTS[j] * P[i, j]
+    if C.size and (C.max() > 2 ** 31 - 1 or C.min() < -2 ** 31):
+        raise OverflowError("int32 overflow")
+    return C.astype(np.int32)
+
+
+def igemm_s8_direct(A, B):
+    """A @ B of int8 matrices in one exact float64 product (no limbs)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    if A.shape[1] * 128 * 128 >= 2 ** 53:
+        raise OverflowError("not exact in float64")
+    return np.rint(A @ B).astype(np.int64)
+
+
+# ----------------------------------------------------------------------------
+# The exact product and the error bound
+# ----------------------------------------------------------------------------
+
+def exact_dot_fraction(a, b):
+    """Exact sum_k a_k b_k as a Fraction (slow; tiny inputs)."""
+    return sum((Fraction(float(x)) * Fraction(float(y)) for x, y in zip(a, b)), Fraction(0))
+
+
+_SPLITTER = 134217729.0  # 2^27 + 1
+
+
+def two_product(a, b):
+    """Error-free product a*b = p + e (Dekker / Veltkamp), element-wise.
+
+    Exact when no intermediate overflows or underflows (|a|, |b| well inside
+    the normal range, |a b| above 2^-969).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    p = a * b
+    ca = _SPLITTER * a
+    ah = ca - (ca - a)
+    al = a - ah
+    cb = _SPLITTER * b
+    bh = cb - (cb - b)
+    bl = b - bh
+    e = ((ah * bh - p) + ah * bl + al * bh) + al * bl
+    return p, e
+
+
+def exact_residual(A, B, C, rows=None, cols=None):
+    """RN(sum_k A_ik B_kj - C_ij) for the selected entries (fsum of two-products)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    rows = np.arange(A.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(B.shape[1]) if cols is None else np.asarray(cols)
+    out = np.zeros((len(rows), len(cols)), dtype=np.float64)
+    for ii, i in enumerate(rows):
+        p, e = two_product(A[i][:, None], B[:, cols])  # (K, cols)
+        for jj in range(len(cols)):
+            out[ii, jj] = math.fsum(p[:, jj].tolist() + e[:, jj].tolist() + [-float(C[ii, jj])])
+    return out
+
+
+def abs_product_sum(A, B, rows=None, cols=None):
+    """(|A| |B|)_ij for the selected entries, correctly rounded (fsum)."""
+    A = np.abs(np.asarray(A, dtype=np.float64))
+    B = np.abs(np.asarray(B, dtype=np.float64))
+    rows = np.arange(A.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(B.shape[1]) if cols is None else np.asarray(cols)
+    out = np.zeros((len(rows), len(cols)), dtype=np.float64)
+    for ii, i in enumerate(rows):
+        p, e = two_product(A[i][:, None], B[:, cols])
+        for jj in range(len(cols)):
+            out[ii, jj] = math.fsum(p[:, jj].tolist() + e[:, jj].tolist())
+    return out
+
+
+def error_bound_ratio(A, B, C, rows=None, cols=None):
+    """Max over entries of |C - C_exact| / (2 K 2^-53 (|A||B|)_ij).
+
+    The target bound is ratio <= 1.  Entries whose (|A||B|)_ij is 0 must be
+    exact; they count as ratio 0 when exact and inf otherwise.
+    """
+    K = np.asarray(A).shape[1]
+    res = np.abs(exact_residual(A, B, C, rows, cols))
+    absum = abs_product_sum(A, B, rows, cols)
+    bound = 2.0 * K * 2.0 ** -53 * absum
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, res / np.where(bound > 0, bound, 1.0),
+                         np.where(res == 0, 0.0, np.inf))
+    return float(ratio.max()) if ratio.size else 0.0
