@@ -337,7 +337,7 @@ def scale_back(Cp, S_shift):
     try:
         return float(val)
     except OverflowError:
-        return math.copysign(math.inf, val)
+        return math.inf if val > 0 else -math.inf
 
 
 def scale_back_array(Cp, sA, sB):

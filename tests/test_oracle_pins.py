@@ -419,3 +419,13 @@ def test_oi_star_is_the_crossing_point():
         else:
             hi = mid
     assert abs(lo - oracle.oi_star(c_q, r, P_fp64, P_int)) / lo < 1e-9
+
+
+def test_scale_back_overflow_rounds_to_signed_inf():
+    # Round to nearest: a value at or beyond the largest finite double plus
+    # half an ulp becomes +-inf, with the sign of the exact value.
+    big = 2 ** 1100
+    assert oracle.scale_back(big, 0) == math.inf
+    assert oracle.scale_back(-big, 0) == -math.inf
+    assert oracle.scale_back(3, -1100) == math.inf
+    assert oracle.scale_back(3, 1100) == 0.0
