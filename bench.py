@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark: emulated DGEMM TFLOP/s (2MNK/t) and % of FP4 roofline on one GB300.
+
+One step = one pass of the whole hot path over one synthetic problem held in
+HBM: deconstruction of A's rows and B's columns (scale, round, residues, FP4
+limb planes), the FP4 limb GEMM with modular recombination, and the CRT +
+scale back to fp64.  The default workload is M = N = K = 8192 with entries
+u 2^e (u ~ U(-1, 1), e uniform in [-10, 10]) and r = 13 moduli.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on bounded samples
+
+Under torchrun every rank runs its own replica (the problems are independent:
+weak scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_pair  # noqa: E402
+
+METRIC = "emulated DGEMM TFLOP/s (2MNK/t) and % of FP4 roofline at 1 GB300"
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CPU_SAMPLE = 128        # sampled rows and columns of C per oracle step
+CPU_MIN_SECONDS = 10.0  # bounded CPU baseline: repeat the sample at least this long
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ozemu", choices=["ozemu", "reference"])
+    ap.add_argument("--workload", default="dgemm_8192_wide", choices=sorted(WORKLOADS))
+    ap.add_argument("--r", type=int, default=None, help="override the number of moduli")
+    ap.add_argument("--m", type=int, default=None, help="override M (same distribution and seed)")
+    ap.add_argument("--n", type=int, default=None, help="override N")
+    ap.add_argument("--k", type=int, default=None, help="override K")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-native", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def max_over_ranks(x, dist, device):
+    """Max of a float across all ranks (plain value when not distributed)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world_size, flop_per_step, steps, elapsed_ms):
+    """Units all ranks processed over the slowest rank's time, in TFLOP/s."""
+    return world_size * flop_per_step * steps / (elapsed_ms / 1e3) / 1e12
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+CPU_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle
+from workloads import WORKLOADS, make_pair, sample_indices
+spec = dict(WORKLOADS[{name!r}]); spec.update({shape!r})
+A, B = make_pair(spec["m"], spec["n"], spec["k"], spec["seed"], spec["dist"])
+r = {r}
+n_rows = min({ns}, spec["m"]); n_cols = min({ns}, spec["n"])
+steps, total, t0 = 0, 0.0, time.time()
+while True:
+    rows = sample_indices(spec["m"], n_rows, seed=100 + steps)
+    cols = sample_indices(spec["n"], n_cols, seed=200 + steps)
+    t = time.time()
+    oracle.dgemm_block(A, B, r, rows=rows, cols=cols)
+    total += time.time() - t
+    steps += 1
+    if (({max_steps} and steps >= {max_steps}) or (not {max_steps} and total >= {min_s})):
+        break
+print(json.dumps(dict(seconds=total, steps=steps, rows=n_rows, cols=n_cols, k=spec["k"])))
+"""
+
+
+def cpu_oracle(name, r, min_seconds, max_steps=0, sample=CPU_SAMPLE, shape=None):
+    """Times the oracle on bounded samples in a single-threaded subprocess."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = CPU_SNIPPET.format(root=ROOT, name=name, r=r, ns=sample, max_steps=max_steps, min_s=min_seconds,
+                              shape=dict(shape or {}))
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    d = json.loads(out.stdout.strip().splitlines()[-1])
+    flops = 2.0 * d["rows"] * d["cols"] * d["k"] * d["steps"]
+    d["tflops"] = flops / d["seconds"] / 1e12
+    return d
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def kernel_traffic():
+    """DRAM bytes per launch of the limb GEMM from the committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "limb_gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for fn in ("gemm_fp4.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "ozaki_ii_fp64_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    if d.get("source_sha256") != h.hexdigest():
+        return None
+    return d
+
+
+def workload_name(args, spec):
+    base = WORKLOADS[args.workload]
+    if all(spec[x] == base[x] for x in ("m", "n", "k")):
+        return args.workload
+    return "%s@%dx%dx%d" % (args.workload, spec["m"], spec["n"], spec["k"])
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import ozaki_ii_fp64_gb300 as oz
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    oz.load()
+
+    spec = dict(WORKLOADS[args.workload])
+    for key in ("m", "n", "k"):
+        if getattr(args, key):
+            spec[key] = getattr(args, key)
+    A_h, B_h = make_pair(spec["m"], spec["n"], spec["k"], spec["seed"], spec["dist"])
+    if spec["kind"] != "dgemm":
+        raise SystemExit("bench.py times the emulated DGEMM workloads")
+    m, n, k = spec["m"], spec["n"], spec["k"]
+    r = args.r or spec["r"]
+    pA, pB = oz.ozemu_bit_budget(k, r)
+    A = torch.from_numpy(A_h).to(dev)
+    B = torch.from_numpy(B_h).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # Preallocated stage buffers: nothing is allocated in the timed region.
+    ap = torch.empty(oz.ozemu_plane_bytes(m, k, r), dtype=torch.uint8, device=dev)
+    bp = torch.empty(oz.ozemu_plane_bytes(n, k, r), dtype=torch.uint8, device=dev)
+    sa = torch.empty(m, dtype=torch.int32, device=dev)
+    sb = torch.empty(n, dtype=torch.int32, device=dev)
+    res = torch.empty(oz.ozemu_residue_bytes(m, n, r), dtype=torch.uint8, device=dev)
+    C = torch.empty((m, n), dtype=torch.float64, device=dev)
+    launches_per_step = 5  # split rows, transpose, split rows of B^T, limb GEMM, CRT
+
+    def check(st, what):
+        if st != 0:
+            raise oz.OzemuError(st, what)
+
+    def step(ev0=None, ev1=None):
+        check(oz.ozemu_split_rows_f64(m, k, A.data_ptr(), k, pA, r, ap.data_ptr(), sa.data_ptr(), sh), "split A")
+        check(oz.ozemu_split_cols_f64(k, n, B.data_ptr(), n, pB, r, bp.data_ptr(), sb.data_ptr(), sh), "split B")
+        if ev0 is not None:
+            ev0.record(stream)
+        check(oz.ozemu_residue_gemm(m, n, k, r, ap.data_ptr(), bp.data_ptr(), res.data_ptr(), sh), "limb gemm")
+        if ev1 is not None:
+            ev1.record(stream)
+        check(oz.ozemu_crt_f64(m, n, r, res.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), n, sh), "crt")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if oz.ozemu_get_status(sh) != 0:
+        raise SystemExit("device status not OK after warm-up")
+
+    # Per-stage durations (one untimed pass, for the report only).
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    evs[0].record(stream)
+    check(oz.ozemu_split_rows_f64(m, k, A.data_ptr(), k, pA, r, ap.data_ptr(), sa.data_ptr(), sh), "split A")
+    evs[1].record(stream)
+    check(oz.ozemu_split_cols_f64(k, n, B.data_ptr(), n, pB, r, bp.data_ptr(), sb.data_ptr(), sh), "split B")
+    evs[2].record(stream)
+    check(oz.ozemu_residue_gemm(m, n, k, r, ap.data_ptr(), bp.data_ptr(), res.data_ptr(), sh), "limb gemm")
+    evs[3].record(stream)
+    check(oz.ozemu_crt_f64(m, n, r, res.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), n, sh), "crt")
+    evs[4].record(stream)
+    torch.cuda.synchronize(dev)
+    stage_ms = {"split_A": evs[0].elapsed_time(evs[1]), "split_B": evs[1].elapsed_time(evs[2]),
+                "limb_gemm": evs[2].elapsed_time(evs[3]), "crt": evs[3].elapsed_time(evs[4])}
+
+    # Timed region.
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(g0[i], g1[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    gemm_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
+    status = oz.ozemu_get_status(sh)
+    if status != 0:
+        raise SystemExit("device status %d after the timed region" % status)
+    elapsed_ms = max_over_ranks(elapsed_ms, dist if ws > 1 else None, dev)
+
+    ms_per_step = elapsed_ms / args.steps
+    flop = 2.0 * m * n * k
+    value = whole_job_tflops(ws, flop, args.steps, elapsed_ms)
+
+    pk, pk_kind = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16  # TFLOP/s, burst
+    fp4_flop = 9.0 * r * flop
+    achieved = fp4_flop / (gemm_ms / 1e3) / 1e12
+    tr = kernel_traffic()
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp4_peak, 4),
+                "traffic": (round(tr["bytes_per_launch"] * (m * n * k) / tr["mnk"]) if tr else None),
+                "kernel": "limb_gemm_kernel<128,residue>",
+                "peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (pk_kind, FP4_OVER_BF16),
+                "algorithmic": "9 r 2MNK FP4 flop per launch"}
+    # Whole-step roofline: the slower of the FP4 term and the algorithmic bytes at HBM peak.
+    # K1 reads 8 B and writes 1.5 r B per input element, K2 reads the planes
+    # once (1.5 r B per input element) and writes r B per output, K3 reads
+    # r B and writes 8 B per output.
+    bytes_alg = (m * k + k * n) * (8 + 3.0 * r) + m * n * (2.0 * r + 8)
+    t_roof = max(fp4_flop / (fp4_peak * 1e12), bytes_alg / (pk["hbm_gbs"] * 1e9))
+    pct_roof = 100.0 * t_roof / (ms_per_step / 1e3)
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(args, spec), "m": m, "n": n, "k": k, "r": r, "dist": spec["dist"],
+                       "seed": spec["seed"], "l2": "inputs larger than L2 (%d MiB per operand), no flush"
+                                                    % (m * k * 8 >> 20)},
+            "pct_fp4_roofline": round(pct_roof, 2), "roofline": roofline,
+            "stage_ms": {kk: round(v, 3) for kk, v in stage_ms.items()},
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk}
+
+    # End to end through the C ABI with host buffers: H2D of A and B from
+    # pinned memory, ozemu_dgemm, D2H of C, every step.
+    if not args.no_e2e:
+        A_pin = torch.from_numpy(A_h).pin_memory()
+        B_pin = torch.from_numpy(B_h).pin_memory()
+        C_pin = torch.empty((m, n), dtype=torch.float64).pin_memory()
+        A2 = torch.empty_like(A)
+        B2 = torch.empty_like(B)
+        C2 = torch.empty_like(C)
+
+        def e2e_step():
+            A2.copy_(A_pin, non_blocking=True)
+            B2.copy_(B_pin, non_blocking=True)
+            check(oz.ozemu_dgemm(m, n, k, A2.data_ptr(), k, B2.data_ptr(), n, C2.data_ptr(), n, r, sh), "dgemm")
+            C_pin.copy_(C2, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e_steps = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1) / e_steps
+        if oz.ozemu_get_status(sh) != 0:
+            raise SystemExit("device status not OK after e2e")
+        # the result must be the device-timed path's result
+        if not torch.equal(C_pin, C.cpu()):
+            raise SystemExit("e2e result differs from the staged result")
+        line["e2e"] = {"value": round(ws * flop / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": int(A_h.nbytes + B_h.nbytes), "d2h_bytes_per_step": int(m * n * 8),
+                       "ms_per_step": round(e_ms, 3), "steps": e_steps}
+
+    if not args.no_native:
+        # Context: native fp64 GEMM (cuBLAS DGEMM via torch.matmul) on the same GPU.
+        torch.matmul(A[:1024], B)
+        torch.cuda.synchronize(dev)
+        n0 = torch.cuda.Event(enable_timing=True)
+        n1 = torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        torch.matmul(A, B)
+        n1.record(stream)
+        torch.cuda.synchronize(dev)
+        nat_ms = n0.elapsed_time(n1)
+        line["native_dgemm"] = {"tflops": round(flop / (nat_ms / 1e3) / 1e12, 3), "ms": round(nat_ms, 3),
+                                "speedup_of_emulation": round(nat_ms / ms_per_step, 2)}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_oracle(args.workload, r, CPU_MIN_SECONDS, shape={"m": m, "n": n, "k": k})
+        line["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                "sample": "%d steps of a %dx%d block of C at full K=%d (oracle, 1 thread), %.1f s"
+                                          % (cb["steps"], cb["rows"], cb["cols"], cb["k"], cb["seconds"])}
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    spec = dict(WORKLOADS[args.workload])
+    for key in ("m", "n", "k"):
+        if getattr(args, key):
+            spec[key] = getattr(args, key)
+    shape = {"m": spec["m"], "n": spec["n"], "k": spec["k"]}
+    r = args.r or spec.get("r", 13)
+    # warm-up steps are bounded samples too; each step is one sample block.
+    if args.warmup:
+        cpu_oracle(args.workload, r, 0, max_steps=args.warmup, sample=32, shape=shape)
+    cb = cpu_oracle(args.workload, r, 0, max_steps=args.steps, sample=32, shape=shape)
+    value = cb["tflops"]
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * cb["seconds"] / cb["steps"], 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_name(args, spec), "m": spec["m"], "n": spec["n"], "k": spec["k"], "r": r,
+                       "dist": spec["dist"], "seed": spec["seed"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step a %dx%d block of C at full K=%d (oracle, 1 thread)"
+                                       % (cb["rows"], cb["cols"], cb["k"])},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

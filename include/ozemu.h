@@ -1,0 +1,179 @@
+/*
+ * ozemu -- Ozaki scheme II FP64 emulation on GB300 (sm_103a) FP4 tensor cores.
+ *
+ * C ABI of libozemu.so.  Plain pointers and sizes only.  Unless a comment
+ * says "host", every pointer argument is a DEVICE pointer owned by the
+ * caller, and every call only enqueues work on `stream` and returns without
+ * synchronising (ozemu_get_status is the one call that synchronises).
+ *
+ * Sources the operations follow (cited by page title and section):
+ *   [TME4] "The Missing Fourth Term for the Emulation Tensor Memory
+ *          Equilibrium (TME) Model: The Residue Deconstruction Cost"
+ *          (arXiv 2610.10924), abstract -- Ozaki scheme II: each fp64 row/column
+ *          is scaled by a power of two, rounded to an integer and reduced
+ *          modulo each of r moduli; per-output reconstruction.
+ *   [AWE]  arXiv 2609.24519 (Adaptive Weight Encoding for FP4 tensor cores),
+ *          English abstract -- digits in S = {0,+-1,+-2,+-3,+-4,+-6,+-8,+-12}
+ *          (FP4 e2m1 values times two), base-13 limbs with weights
+ *          (1, 13, 169), 9 exact FP4 GEMMs per INT8 x INT8 product, the same
+ *          formulation modulo m.
+ *
+ * Conventions
+ *   - Matrices are row-major.  A is m x k (leading dimension lda >= k),
+ *     B is k x n (ldb >= n), C is m x n (ldc >= n).  C = A B, no alpha/beta.
+ *   - Moduli: the greedy pairwise-coprime integers counting down from 256
+ *     (256, 255, 253, 251, 247, 241, ...); r of them, 1 <= r <= ozemu_max_moduli().
+ *   - Bit budget for inner dimension k: P is the largest integer with
+ *     2 k 2^P < m_1 m_2 ... m_r; p_A = ceil(P/2), p_B = floor(P/2).
+ *   - Row shift s_i = p - e_i, where e_i is the frexp exponent of the row's
+ *     largest magnitude (2^(e_i-1) <= max < 2^e_i); 0 for an all-zero row.
+ *     Integers are round-half-to-even(x 2^s).
+ *   - Residues are balanced: in [-floor(m/2), ceil(m/2) - 1] (int8 range).
+ *   - Limb split of a residue x: x = d0 + 13 d1 + 169 d2 with d_i in S; the
+ *     low digits are the smallest-magnitude member of S in x's class mod 13.
+ *
+ * Limb-plane layout (written by the split calls, read by the GEMM calls)
+ *   rows_p = round_up(rows, 128), k_p = round_up(k, 128), row_bytes = k_p/2.
+ *   Plane (l, j) for modulus l (0-based) and limb j in {0,1,2} starts at byte
+ *   ((l*3 + j) * rows_p) * row_bytes; row i of it at + i*row_bytes.  Element
+ *   k of a row is the 4-bit FP4 e2m1 code of d/2 in byte k/2, low nibble for
+ *   even k.  Padding rows and columns hold digit 0 (code 0).  INT8 planes are
+ *   the same with a single "modulus" (3 planes).
+ *   Total bytes: ozemu_plane_bytes(rows, k, r).
+ *
+ * Residue layout (written by ozemu_residue_gemm, read by ozemu_crt_f64)
+ *   uint8 [r][m][ldr], ldr = round_up(n, 16): residue of C' modulo m_l in
+ *   [0, m_l) at byte (l*m + i)*ldr + j.  Total bytes: ozemu_residue_bytes.
+ *
+ * Errors: calls return an ozemu_status.  Argument checks happen on the host
+ * before anything is enqueued.  Device-side conditions (non-finite input,
+ * a pipeline wait that hit its time limit) set a per-device flag that
+ * ozemu_get_status reports and clears.
+ */
+#ifndef OZEMU_H
+#define OZEMU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OZEMU_OK = 0,
+  OZEMU_ERR_INVALID_ARG = -1, /* bad size, pointer, leading dim, r or p      */
+  OZEMU_ERR_K_OVERFLOW = -2,  /* int32 result could overflow (k > 131071)   */
+  OZEMU_ERR_ALLOC = -3,       /* workspace allocation failed                */
+  OZEMU_ERR_CUDA = -4,        /* a CUDA call or launch failed               */
+  OZEMU_ERR_NONFINITE = -5,   /* an input held Inf or NaN (output unspecified) */
+  OZEMU_ERR_TIMEOUT = -6,     /* a kernel pipeline wait hit its time limit  */
+  OZEMU_ERR_UNSUPPORTED = -7  /* current device is not sm_103 (GB300)       */
+} ozemu_status;
+
+/* ------------------------------------------------------------------------ */
+/* Full products                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Exact C32 = A B for int8 A (m x k, row-major, lda = k) and int8 B (k x n,
+ * row-major, ldb = n); C32 int32 m x n row-major (ldc = n).  Each operand is
+ * split into 3 base-13 limbs and the product takes 9 FP4 GEMMs, recombined
+ * with weights 13^(i+j) ([AWE] abstract).  k > 131071 -> OZEMU_ERR_K_OVERFLOW.
+ * m, n or k = 0 is a no-op (k = 0 zeroes C32).  Uses the cached workspace. */
+int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B,
+                   int32_t* C32, cudaStream_t stream);
+
+/* Emulated fp64 C = A B with r moduli: deconstruction of A's rows and B's
+ * columns ([TME4] abstract), 9 FP4 limb GEMMs per modulus with modular
+ * recombination ([AWE] abstract), CRT and one correct rounding per entry of
+ * C' 2^-(s_i + t_j).  Requires 2k < m_1...m_r (else OZEMU_ERR_INVALID_ARG).
+ * m, n or k = 0 is a no-op (k = 0 zeroes C).  Inf/NaN in A or B sets the
+ * non-finite flag; C is then unspecified.  Uses the cached workspace. */
+int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
+                int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Host-side queries (no device work)                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Largest supported r (16: keeps p_A, p_B <= 62 for every k >= 1). host. */
+int ozemu_max_moduli(void);
+
+/* Writes the first r moduli to out[0..r-1] (host pointer). host. */
+int ozemu_moduli(int r, int32_t* out);
+
+/* Bit budget for inner dimension k and r moduli: *p_a = ceil(P/2),
+ * *p_b = floor(P/2) (host pointers).  OZEMU_ERR_INVALID_ARG if 2k >= M. host. */
+int ozemu_bit_budget(int k, int r, int* p_a, int* p_b);
+
+/* Bytes of the limb planes of `rows` rows of length k with r moduli
+ * (r = 1 for INT8 planes); 0 on bad arguments.  host. */
+size_t ozemu_plane_bytes(int rows, int k, int r);
+
+/* Bytes of the residue output of an m x n product with r moduli. host. */
+size_t ozemu_residue_bytes(int m, int n, int r);
+
+/* ------------------------------------------------------------------------ */
+/* Stages (stored limb planes / residues can be reused across products)     */
+/* ------------------------------------------------------------------------ */
+
+/* Deconstruct the rows of X (rows x k, row-major, ldx >= k) with budget p
+ * (0 <= p <= 62, from ozemu_bit_budget) and r moduli: writes shifts[rows]
+ * (int32, s_i) and the limb planes (ozemu_plane_bytes(rows, k, r) bytes).
+ * [TME4] abstract (scale, round, reduce); [AWE] abstract (limbs in S). */
+int ozemu_split_rows_f64(int rows, int k, const double* X, int ldx, int p, int r,
+                         uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+
+/* Same for the columns of X (k x cols, row-major, ldx >= cols): column j
+ * becomes plane row j.  Uses the cached workspace for a transposed copy. */
+int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r,
+                         uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+
+/* INT8 limb planes of the rows of X (rows x k, ldx >= k): 3 planes. */
+int ozemu_split_rows_s8(int rows, int k, const int8_t* X, int ldx,
+                        uint8_t* planes, cudaStream_t stream);
+
+/* INT8 limb planes of the columns of X (k x cols, ldx >= cols). Workspace. */
+int ozemu_split_cols_s8(int k, int cols, const int8_t* X, int ldx,
+                        uint8_t* planes, cudaStream_t stream);
+
+/* Residues of C' = A'B' modulo each of r moduli, from limb planes of A's rows
+ * (m rows) and B's columns (n rows), inner dimension k: 9 FP4 GEMMs per
+ * modulus, recombined modulo m_l ([AWE] abstract: the formulation holds
+ * modulo m).  Output in the residue layout above. */
+int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes,
+                       const uint8_t* b_planes, uint8_t* residues, cudaStream_t stream);
+
+/* Exact int32 C32 = sum_{i,j} 13^(i+j) A_i B_j from INT8 limb planes
+ * ([AWE] abstract); C32 m x n row-major with leading dimension ldc >= n.
+ * k > 131071 -> OZEMU_ERR_K_OVERFLOW. */
+int ozemu_limb_gemm_s32(int m, int n, int k, const uint8_t* a_planes,
+                        const uint8_t* b_planes, int32_t* C32, int ldc,
+                        cudaStream_t stream);
+
+/* Per-output reconstruction ([TME4] abstract): C' in (-M/2, M/2) from its r
+ * residues by mixed-radix CRT, then C[i*ldc + j] = RN(C' 2^-(sA[i] + sB[j])),
+ * one correct rounding (subnormal and overflow included). */
+int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a,
+                  const int32_t* shifts_b, double* C, int ldc, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and workspace                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then returns and clears the current device's flags:
+ * OZEMU_ERR_NONFINITE, OZEMU_ERR_TIMEOUT, OZEMU_ERR_CUDA (a sticky CUDA error)
+ * or OZEMU_OK. */
+int ozemu_get_status(cudaStream_t stream);
+
+/* Frees the workspace cached for the current device (synchronises it).
+ * Calls after this re-allocate on demand. */
+void ozemu_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OZEMU_H */

@@ -1,0 +1,483 @@
+// C ABI of libozemu.so: argument checks, per-call constants, the cached
+// per-device workspace and status flags, and the staging of the kernels.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ozemu.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ozemu {
+namespace {
+
+typedef unsigned __int128 u128;
+
+// ------------------------------------------------------------------ moduli
+// Greedy pairwise-coprime integers counting down from 256.
+struct ModuliTable {
+  uint32_t m[kMaxModuli];
+  ModuliTable() {
+    int n = 0;
+    for (uint32_t c = 256; n < kMaxModuli && c >= 2; --c) {
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        uint32_t a = c, b = m[j];
+        while (b) {
+          uint32_t t = a % b;
+          a = b;
+          b = t;
+        }
+        ok = (a == 1);
+      }
+      if (ok) m[n++] = c;
+    }
+  }
+};
+const ModuliTable& moduli() {
+  static const ModuliTable t;
+  return t;
+}
+
+u128 modulus_product(int r) {
+  u128 p = 1;
+  for (int l = 0; l < r; ++l) p *= moduli().m[l];
+  return p;
+}
+
+// Largest P with 2 k 2^P < M; -1 if none.
+int budget_P(long long k, int r) {
+  const u128 M = modulus_product(r);
+  const u128 two_k = static_cast<u128>(2) * static_cast<u128>(k);
+  if (!(two_k < M)) return -1;
+  int P = 0;
+  while (P < 126 && (two_k << (P + 1)) < M) ++P;
+  return P;
+}
+
+uint32_t pow_mod(uint64_t base, uint64_t e, uint32_t m) {
+  uint64_t r = 1 % m;
+  base %= m;
+  while (e) {
+    if (e & 1) r = r * base % m;
+    base = base * base % m;
+    e >>= 1;
+  }
+  return static_cast<uint32_t>(r);
+}
+
+uint32_t inv_mod(uint32_t a, uint32_t m) {  // a coprime to m
+  long long t = 0, nt = 1, rr = m, nr = a % m;
+  while (nr) {
+    long long q = rr / nr, x = t - q * nt;
+    t = nt;
+    nt = x;
+    x = rr - q * nr;
+    rr = nr;
+    nr = x;
+  }
+  return static_cast<uint32_t>(t < 0 ? t + m : t);
+}
+
+SplitModuli split_moduli(int r) {
+  SplitModuli s;
+  std::memset(&s, 0, sizeof(s));
+  s.r = r;
+  for (int l = 0; l < r; ++l) {
+    const uint32_t m = moduli().m[l];
+    s.m[l] = m;
+    s.c21x4[l] = 4u * pow_mod(2, 21, m);
+    s.c42x4[l] = 4u * pow_mod(2, 42, m);
+    s.magic4[l] = static_cast<uint32_t>((1ull << 32) / (4ull * m));
+    s.off[l] = pow_mod(2, 62, m);
+  }
+  return s;
+}
+
+EpiModuli epi_moduli(int r) {
+  EpiModuli e;
+  std::memset(&e, 0, sizeof(e));
+  for (int l = 0; l < r; ++l) {
+    const uint32_t m = moduli().m[l];
+    e.m[l] = static_cast<float>(m);
+    e.inv_m[l] = 1.0f / static_cast<float>(m);
+    e.w169[l] = static_cast<float>(169u % m);
+  }
+  return e;
+}
+
+CrtModuli crt_moduli(int r) {
+  CrtModuli c;
+  std::memset(&c, 0, sizeof(c));
+  c.r = r;
+  u128 pref = 1;
+  for (int l = 0; l < r; ++l) {
+    const uint32_t m = moduli().m[l];
+    c.m[l] = m;
+    c.magic[l] = static_cast<uint32_t>((1ull << 32) / m);
+    const uint32_t inv = inv_mod(static_cast<uint32_t>(pref % m), m);
+    c.inv[l] = inv;
+    u128 pj = 1;
+    for (int j = 0; j < l; ++j) {
+      c.g[l][j] = static_cast<uint32_t>((static_cast<uint64_t>(pj % m) * inv) % m);
+      pj *= moduli().m[j];
+    }
+    for (int w = 0; w < 4; ++w) c.prefix[l][w] = static_cast<uint32_t>(pref >> (32 * w));
+    pref *= m;
+  }
+  return c;
+}
+
+// ----------------------------------------------------------- device state
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  uint32_t* flags = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int kchunk_blocks() {
+  static int kc = [] {
+    int v = 8192;
+    if (const char* s = std::getenv("OZEMU_KCHUNK")) {
+      int x = std::atoi(s);
+      if (x >= 128 && x <= 8192 && x % 128 == 0) v = x;
+    }
+    return v / 128;
+  }();
+  return kc;
+}
+
+// Current device's state, created on first use.  Returns OZEMU_OK or an error.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OZEMU_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.checked = true;
+  }
+  if (!d.supported) return OZEMU_ERR_UNSUPPORTED;
+  if (!d.flags) {
+    if (cudaMalloc(&d.flags, 256) != cudaSuccess) return OZEMU_ERR_ALLOC;
+    if (cudaMemset(d.flags, 0, 256) != cudaSuccess) return OZEMU_ERR_CUDA;
+  }
+  *out = &d;
+  return OZEMU_OK;
+}
+
+// Workspace of at least `bytes` on the current device (grows; synchronises
+// the device when it has to replace a smaller buffer).
+int workspace(DeviceState* d, size_t bytes, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (bytes > d->ws_bytes) {
+    if (d->ws) {
+      cudaDeviceSynchronize();
+      cudaFree(d->ws);
+      d->ws = nullptr;
+      d->ws_bytes = 0;
+    }
+    size_t want = bytes + bytes / 8;
+    if (cudaMalloc(&d->ws, want) != cudaSuccess) {
+      cudaGetLastError();
+      return OZEMU_ERR_ALLOC;
+    }
+    d->ws_bytes = want;
+  }
+  *out = static_cast<uint8_t*>(d->ws);
+  return OZEMU_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t plane_bytes(long long rows, long long k, int r) {
+  return static_cast<size_t>(3LL * r * round_up(static_cast<int>(rows), kRowAlign)) *
+         static_cast<size_t>(round_up(static_cast<int>(k), kKAlign) / 2);
+}
+
+bool rows_ok(int rows, int r) {  // plane-row coordinates fit in int
+  return 3LL * r * round_up(rows, kRowAlign) < (1LL << 31);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? OZEMU_OK : OZEMU_ERR_CUDA; }
+
+// ---------------------------------------------------------------- stages
+int split_rows_f64(int rows, int k, const double* X, long long ldx, int p, int r, uint8_t* planes,
+                   int32_t* shifts, DeviceState* d, cudaStream_t st) {
+  return cuda_status(launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r), planes, shifts, d->flags, st));
+}
+
+int split_cols_f64(int k, int cols, const double* X, long long ldx, int p, int r, uint8_t* planes,
+                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st) {
+  if (k > 0) {
+    cudaError_t e = launch_transpose_f64(X, ldx, k, cols, scratch, k, st);
+    if (e != cudaSuccess) return OZEMU_ERR_CUDA;
+  }
+  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st);
+}
+
+int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* bp, uint8_t* res, DeviceState* d,
+                 cudaStream_t st) {
+  LimbGemmCall c;
+  c.residue_mode = true;
+  c.m = m;
+  c.n = n;
+  c.k = k;
+  c.r = r;
+  c.a_planes = ap;
+  c.b_planes = bp;
+  c.res_out = res;
+  c.ldr = round_up(n, 16);
+  c.c32 = nullptr;
+  c.ldc = 0;
+  c.kc_blocks = kchunk_blocks();
+  c.em = epi_moduli(r);
+  c.flags = d->flags;
+  return cuda_status(launch_limb_gemm(c, st));
+}
+
+int limb_gemm_s32(int m, int n, int k, const uint8_t* ap, const uint8_t* bp, int32_t* C, long long ldc,
+                  DeviceState* d, cudaStream_t st) {
+  LimbGemmCall c;
+  c.residue_mode = false;
+  c.m = m;
+  c.n = n;
+  c.k = k;
+  c.r = 1;
+  c.a_planes = ap;
+  c.b_planes = bp;
+  c.res_out = nullptr;
+  c.ldr = 0;
+  c.c32 = C;
+  c.ldc = ldc;
+  c.kc_blocks = kchunk_blocks();
+  c.em = epi_moduli(1);
+  c.flags = d->flags;
+  return cuda_status(launch_limb_gemm(c, st));
+}
+
+constexpr int kMaxKInt32 = 131071;
+
+}  // namespace
+}  // namespace ozemu
+
+using namespace ozemu;
+
+extern "C" {
+
+int ozemu_max_moduli(void) { return kMaxModuli; }
+
+int ozemu_moduli(int r, int32_t* out) {
+  if (r < 1 || r > kMaxModuli || !out) return OZEMU_ERR_INVALID_ARG;
+  for (int l = 0; l < r; ++l) out[l] = static_cast<int32_t>(moduli().m[l]);
+  return OZEMU_OK;
+}
+
+int ozemu_bit_budget(int k, int r, int* p_a, int* p_b) {
+  if (k < 1 || r < 1 || r > kMaxModuli || !p_a || !p_b) return OZEMU_ERR_INVALID_ARG;
+  const int P = budget_P(k, r);
+  if (P < 0) return OZEMU_ERR_INVALID_ARG;
+  *p_a = (P + 1) / 2;
+  *p_b = P / 2;
+  return OZEMU_OK;
+}
+
+size_t ozemu_plane_bytes(int rows, int k, int r) {
+  if (rows < 0 || k < 0 || r < 1 || r > kMaxModuli) return 0;
+  return plane_bytes(rows, k, r);
+}
+
+size_t ozemu_residue_bytes(int m, int n, int r) {
+  if (m < 0 || n < 0 || r < 1 || r > kMaxModuli) return 0;
+  return static_cast<size_t>(r) * static_cast<size_t>(m) * static_cast<size_t>(round_up(n, 16));
+}
+
+int ozemu_split_rows_f64(int rows, int k, const double* X, int ldx, int p, int r, uint8_t* planes,
+                         int32_t* shifts, cudaStream_t stream) {
+  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+    return OZEMU_ERR_INVALID_ARG;
+  if (rows == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !shifts || !aligned16(planes) || !rows_ok(rows, r)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  return split_rows_f64(rows, k, X, ldx, p, r, planes, shifts, d, stream);
+}
+
+int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
+                         int32_t* shifts, cudaStream_t stream) {
+  if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+    return OZEMU_ERR_INVALID_ARG;
+  if (cols == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !shifts || !aligned16(planes) || !rows_ok(cols, r)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ws = nullptr;
+  s = workspace(d, align256(static_cast<size_t>(k > 0 ? k : 1) * cols * sizeof(double)), &ws);
+  if (s != OZEMU_OK) return s;
+  return split_cols_f64(k, cols, X, ldx, p, r, planes, shifts, reinterpret_cast<double*>(ws), d, stream);
+}
+
+int ozemu_split_rows_s8(int rows, int k, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream) {
+  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (rows == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !aligned16(planes) || !rows_ok(rows, 1)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_split_rows_s8(X, ldx, rows, k, planes, stream));
+}
+
+int ozemu_split_cols_s8(int k, int cols, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream) {
+  if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (cols == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !aligned16(planes) || !rows_ok(cols, 1)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ws = nullptr;
+  s = workspace(d, align256(static_cast<size_t>(k > 0 ? k : 1) * cols), &ws);
+  if (s != OZEMU_OK) return s;
+  int8_t* t = reinterpret_cast<int8_t*>(ws);
+  if (k > 0 && launch_transpose_s8(X, ldx, k, cols, t, k, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  return cuda_status(launch_split_rows_s8(t, k > 0 ? k : 1, cols, k, planes, stream));
+}
+
+int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
+                       uint8_t* residues, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!residues || !aligned16(residues) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  if (k > 0 && (!a_planes || !b_planes || !aligned16(a_planes) || !aligned16(b_planes)))
+    return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0)
+    return cuda_status(cudaMemsetAsync(residues, 0, ozemu_residue_bytes(m, n, r), stream));
+  return residue_gemm(m, n, k, r, a_planes, b_planes, residues, d, stream);
+}
+
+int ozemu_limb_gemm_s32(int m, int n, int k, const uint8_t* a_planes, const uint8_t* b_planes, int32_t* C32,
+                        int ldc, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (k > kMaxKInt32) return OZEMU_ERR_K_OVERFLOW;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C32 || !rows_ok(m, 1) || !rows_ok(n, 1)) return OZEMU_ERR_INVALID_ARG;
+  if (k > 0 && (!a_planes || !b_planes || !aligned16(a_planes) || !aligned16(b_planes)))
+    return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(launch_zero_s32(C32, m, n, ldc, stream));
+  return limb_gemm_s32(m, n, k, a_planes, b_planes, C32, ldc, d, stream);
+}
+
+int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a, const int32_t* shifts_b,
+                  double* C, int ldc, cudaStream_t stream) {
+  if (m < 0 || n < 0 || r < 1 || r > kMaxModuli || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!residues || !aligned16(residues) || !shifts_a || !shifts_b || !C) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(
+      launch_crt_f64(m, n, residues, round_up(n, 16), shifts_a, shifts_b, C, ldc, crt_moduli(r), stream));
+}
+
+int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B, int32_t* C32, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0) return OZEMU_ERR_INVALID_ARG;
+  if (k > kMaxKInt32) return OZEMU_ERR_K_OVERFLOW;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C32 || (k > 0 && (!A || !B)) || !rows_ok(m, 1) || !rows_ok(n, 1)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(launch_zero_s32(C32, m, n, n, stream));
+  const size_t pa = align256(plane_bytes(m, k, 1)), pb = align256(plane_bytes(n, k, 1));
+  const size_t bt = align256(static_cast<size_t>(k) * n);
+  uint8_t* ws = nullptr;
+  s = workspace(d, pa + pb + bt, &ws);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ap = ws;
+  uint8_t* bp = ws + pa;
+  int8_t* btr = reinterpret_cast<int8_t*>(ws + pa + pb);
+  if (launch_split_rows_s8(A, k, m, k, ap, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (launch_transpose_s8(B, n, k, n, btr, k, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (launch_split_rows_s8(btr, k, n, k, bp, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  return limb_gemm_s32(m, n, k, ap, bp, C32, n, d, stream);
+}
+
+int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                int r, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (k > 0 && ozemu_bit_budget(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
+  const size_t pa = align256(plane_bytes(m, k, r)), pb = align256(plane_bytes(n, k, r));
+  const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
+  const size_t rb = align256(ozemu_residue_bytes(m, n, r));
+  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  uint8_t* ws = nullptr;
+  s = workspace(d, pa + pb + sa + sb + rb + bt, &ws);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ap = ws;
+  uint8_t* bp = ap + pa;
+  int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
+  int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
+  uint8_t* res = bp + pb + sa + sb;
+  double* btr = reinterpret_cast<double*>(res + rb);
+  s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, d, stream);
+  if (s != OZEMU_OK) return s;
+  s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, d, stream);
+  if (s != OZEMU_OK) return s;
+  s = residue_gemm(m, n, k, r, ap, bp, res, d, stream);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), stream));
+}
+
+int ozemu_get_status(cudaStream_t stream) {
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  uint32_t f = 0;
+  if (cudaMemcpy(&f, d->flags, sizeof(f), cudaMemcpyDeviceToHost) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (cudaMemset(d->flags, 0, sizeof(f)) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (f & kFlagTimeout) return OZEMU_ERR_TIMEOUT;
+  if (f & kFlagNonFinite) return OZEMU_ERR_NONFINITE;
+  return OZEMU_OK;
+}
+
+void ozemu_release(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (d.ws) {
+    cudaDeviceSynchronize();
+    cudaFree(d.ws);
+    d.ws = nullptr;
+    d.ws_bytes = 0;
+  }
+}
+
+}  // extern "C"

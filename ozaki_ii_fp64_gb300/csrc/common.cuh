@@ -1,0 +1,209 @@
+// Shared device helpers for the ozemu kernels (sm_103a only).
+//
+// Inline PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor), tcgen05
+// (TMEM alloc / MMA / ld / st / commit) and the per-call constant blocks that
+// the host passes to the kernels by value.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ozemu {
+
+constexpr int kMaxModuli = 16;
+constexpr int kRowAlign = 128;   // plane rows padded to this (GEMM tile M)
+constexpr int kKAlign = 128;     // plane k padded to this (GEMM stage K)
+
+// Device flag bits (per-device word, reported by ozemu_get_status).
+constexpr uint32_t kFlagNonFinite = 1u;
+constexpr uint32_t kFlagTimeout = 2u;
+
+// Time limit of one pipeline wait before the kernel gives up (ns).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Per-modulus constants for the deconstruction kernel.  With the integer
+// offset u = x + 2^62 split in 21-bit chunks u = a2 2^42 + a1 2^21 + a0,
+// v = a2 (2^42 mod m) + a1 (2^21 mod m) + a0 < 2^30, and 4v < 2^32.
+struct SplitModuli {
+  int r;
+  uint32_t m[kMaxModuli];
+  uint32_t c21x4[kMaxModuli];   // 4 (2^21 mod m)
+  uint32_t c42x4[kMaxModuli];   // 4 (2^42 mod m)
+  uint32_t magic4[kMaxModuli];  // floor(2^32 / (4 m))
+  uint32_t off[kMaxModuli];     // 2^62 mod m
+};
+
+// Per-modulus constants for the GEMM epilogue.
+struct EpiModuli {
+  float m[kMaxModuli];
+  float inv_m[kMaxModuli];      // 1/m rounded to fp32
+  float w169[kMaxModuli];       // 169 mod m
+};
+
+// Mixed-radix CRT constants.
+struct CrtModuli {
+  int r;
+  uint32_t m[kMaxModuli];
+  uint32_t magic[kMaxModuli];             // floor(2^32 / m)
+  uint32_t inv[kMaxModuli];               // (m_0 ... m_{l-1})^-1 mod m_l
+  uint32_t g[kMaxModuli][kMaxModuli];     // g[l][j] = (m_0...m_{j-1}) inv_l mod m_l, j < l
+  uint32_t prefix[kMaxModuli][4];         // m_0 ... m_{l-1} as 128-bit little-endian words
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, at most kWaitLimitNs.
+// On time-out sets the device timeout flag and the CTA's abort word and
+// returns false.  Also returns false early once another role of this CTA, or
+// any CTA on the device, has timed out (the flag word is device-wide).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_word,
+                                          uint32_t* flags) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort_word || (*reinterpret_cast<volatile uint32_t*>(flags) & kFlagTimeout)) {
+        *abort_word = 1;
+        return false;
+      }
+      uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        atomicOr(flags, kFlagTimeout);
+        *abort_word = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// ----------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Block-scaled FP4 MMA, NVFP4 form: A, B e2m1 from shared-memory
+// descriptors, one UE4M3 scale per 16 K-elements read from TMEM.
+__device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 16 columns of 32-bit words: register i holds column i of the
+// calling thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile whose rows are
+// 64 bytes (128 FP4 elements) written by TMA with 64-byte swizzling: 8-row
+// core groups 512 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;          // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;                 // version
+  d |= static_cast<uint64_t>(4u) << 61;                 // 64-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::mxf4nvf4, A and B e2m1, K-major, UE4M3
+// scales, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_fp4(int n) {
+  return (1u << 7)                                // A format: e2m1
+         | (1u << 10)                             // B format: e2m1
+         | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8
+         | (0u << 23)                             // scale type UE4M3
+         | (static_cast<uint32_t>(128 >> 4) << 24);  // M / 16
+}
+
+}  // namespace ozemu

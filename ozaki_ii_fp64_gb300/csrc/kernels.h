@@ -1,0 +1,49 @@
+// Host-side launchers of the ozemu kernels (internal to libozemu.so).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ozemu {
+
+inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Deconstruction of the rows of X into limb planes (split.cu).
+cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
+                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream);
+cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k, uint8_t* planes,
+                                 cudaStream_t stream);
+cudaError_t launch_transpose_f64(const double* in, long long ldin, int rows, int cols, double* out,
+                                 long long ldout, cudaStream_t stream);
+cudaError_t launch_transpose_s8(const int8_t* in, long long ldin, int rows, int cols, int8_t* out, long long ldout,
+                                cudaStream_t stream);
+
+// FP4 limb GEMM (gemm_fp4.cu).  Residue mode writes uint8 [r][m][ldr]
+// residues; int mode (r = 1) writes int32 C32 with leading dimension ldc.
+// kc_blocks: 128-wide K blocks per exactly accumulated chunk.
+struct LimbGemmCall {
+  bool residue_mode;
+  int m, n, k, r;
+  const uint8_t* a_planes;
+  const uint8_t* b_planes;
+  uint8_t* res_out;
+  long long ldr;
+  int32_t* c32;
+  long long ldc;
+  int kc_blocks;
+  EpiModuli em;
+  uint32_t* flags;
+};
+cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream);
+
+// CRT and scale back (crt.cu).
+cudaError_t launch_crt_f64(int m, int n, const uint8_t* residues, long long ldr, const int32_t* sa,
+                           const int32_t* sb, double* C, long long ldc, const CrtModuli& cm, cudaStream_t stream);
+
+// Fill helpers.
+cudaError_t launch_zero_f64(double* C, int m, int n, long long ldc, cudaStream_t stream);
+cudaError_t launch_zero_s32(int32_t* C, int m, int n, long long ldc, cudaStream_t stream);
+
+}  // namespace ozemu

@@ -1,0 +1,125 @@
+"""C ABI checks that need no GPU: the library builds, loads, exports every
+function include/ozemu.h declares, and its host-side queries and argument
+checks behave as documented (checks run before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def oz():
+    import ozaki_ii_fp64_gb300 as oz
+    oz.load()
+    return oz
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(ozemu_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("ozemu_igemm_s8", "ozemu_dgemm", "ozemu_get_status", "ozemu_max_moduli", "ozemu_release"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(oz):
+    lib = oz.load()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_mirrors_every_declared_symbol(oz):
+    missing = [n for n in declared_functions() if not callable(getattr(oz, n, None))]
+    assert not missing, missing
+
+
+def test_moduli_match_oracle(oz):
+    assert oz.ozemu_max_moduli() == 16
+    assert oz.ozemu_moduli(16) == oracle.moduli(16)
+
+
+@pytest.mark.parametrize("k", [1, 2, 255, 256, 4096, 8192, 16384, 65536, 131071])
+@pytest.mark.parametrize("r", [3, 8, 11, 12, 13, 16])
+def test_bit_budget_matches_oracle(oz, k, r):
+    try:
+        _, pa, pb = oracle.bit_budget(k, r)
+    except ValueError:
+        with pytest.raises(oz.OzemuError):
+            oz.ozemu_bit_budget(k, r)
+        return
+    assert oz.ozemu_bit_budget(k, r) == (pa, pb)
+
+
+def test_layout_sizes(oz):
+    assert oz.ozemu_plane_bytes(1, 1, 1) == 3 * 128 * 64
+    assert oz.ozemu_plane_bytes(129, 300, 13) == 3 * 13 * 256 * 192
+    assert oz.ozemu_residue_bytes(5, 17, 2) == 2 * 5 * 32
+    assert oz.ozemu_plane_bytes(-1, 1, 1) == 0
+    assert oz.ozemu_residue_bytes(1, 1, 17) == 0
+
+
+NULL = None
+FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
+
+
+@pytest.mark.parametrize("call", [
+    lambda oz: oz.ozemu_dgemm(-1, 1, 1, FAKE, 1, FAKE, 1, FAKE, 1, 13, NULL),
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, FAKE, 3, FAKE, 4, FAKE, 4, 13, NULL),      # lda < k
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, FAKE, 4, FAKE, 3, FAKE, 4, 13, NULL),      # ldb < n
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 3, 13, NULL),      # ldc < n
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, NULL),       # r < 1
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 17, NULL),      # r > 16
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, NULL, 4, FAKE, 4, FAKE, 4, 13, NULL),      # null A
+    lambda oz: oz.ozemu_dgemm(4, 4, 4, FAKE, 4, FAKE, 4, NULL, 4, 13, NULL),      # null C
+    lambda oz: oz.ozemu_dgemm(4, 4, 200, FAKE, 200, FAKE, 4, FAKE, 4, 1, NULL),   # 2k >= 256
+    lambda oz: oz.ozemu_igemm_s8(-1, 2, 2, FAKE, FAKE, FAKE, NULL),
+    lambda oz: oz.ozemu_igemm_s8(2, 2, 2, NULL, FAKE, FAKE, NULL),
+    lambda oz: oz.ozemu_split_rows_f64(4, 4, FAKE, 4, 63, 13, FAKE, FAKE, NULL),  # p > 62
+    lambda oz: oz.ozemu_split_rows_f64(4, 4, FAKE, 4, 40, 13, FAKE + 8, FAKE, NULL),  # unaligned planes
+    lambda oz: oz.ozemu_split_cols_f64(4, 4, FAKE, 3, 40, 13, FAKE, FAKE, NULL),  # ldx < cols
+    lambda oz: oz.ozemu_split_rows_s8(4, 4, FAKE, 3, FAKE, NULL),
+    lambda oz: oz.ozemu_split_cols_s8(4, 4, NULL, 4, FAKE, NULL),
+    lambda oz: oz.ozemu_residue_gemm(4, 4, 4, 0, FAKE, FAKE, FAKE, NULL),
+    lambda oz: oz.ozemu_residue_gemm(4, 4, 4, 13, FAKE, FAKE, FAKE + 4, NULL),    # unaligned residues
+    lambda oz: oz.ozemu_limb_gemm_s32(4, 4, 4, FAKE, FAKE, FAKE, 3, NULL),        # ldc < n
+    lambda oz: oz.ozemu_crt_f64(4, 4, 13, FAKE, FAKE, NULL, FAKE, 4, NULL),
+])
+def test_invalid_arguments_rejected_on_host(oz, call):
+    assert call(oz) == oz.OZEMU_ERR_INVALID_ARG
+
+
+def test_k_overflow_rejected_on_host(oz):
+    assert oz.ozemu_igemm_s8(4, 4, 131072, FAKE, FAKE, FAKE, NULL) == oz.OZEMU_ERR_K_OVERFLOW
+    assert oz.ozemu_limb_gemm_s32(4, 4, 131072, FAKE, FAKE, FAKE, 4, NULL) == oz.OZEMU_ERR_K_OVERFLOW
+
+
+def test_empty_problems_are_noops(oz):
+    assert oz.ozemu_dgemm(0, 5, 5, NULL, 5, NULL, 5, NULL, 5, 13, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_dgemm(5, 0, 5, NULL, 5, NULL, 1, NULL, 1, 13, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_igemm_s8(0, 0, 7, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_split_rows_f64(0, 9, NULL, 9, 30, 13, NULL, NULL, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_residue_gemm(0, 3, 3, 13, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
+
+
+def test_product_path_has_no_fallback():
+    # The package never imports the oracle and never computes on the host.
+    pkg = os.path.join(ROOT, "ozaki_ii_fp64_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
