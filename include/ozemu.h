@@ -70,7 +70,8 @@ typedef enum {
   OZEMU_ERR_CUDA = -4,        /* a CUDA call or launch failed               */
   OZEMU_ERR_NONFINITE = -5,   /* an input held Inf or NaN (output unspecified) */
   OZEMU_ERR_TIMEOUT = -6,     /* a kernel pipeline wait hit its time limit  */
-  OZEMU_ERR_UNSUPPORTED = -7  /* current device is not sm_103 (GB300)       */
+  OZEMU_ERR_UNSUPPORTED = -7, /* current device is not sm_103 (GB300)       */
+  OZEMU_ERR_SCRATCH_TOO_SMALL = -8 /* problem needs more than the fixed scratch */
 } ozemu_status;
 
 /* ------------------------------------------------------------------------ */
@@ -171,6 +172,39 @@ int ozemu_get_status(cudaStream_t stream);
 /* Frees the workspace cached for the current device (synchronises it).
  * Calls after this re-allocate on demand. */
 void ozemu_release(void);
+
+/* ------------------------------------------------------------------------ */
+/* Allocation-free product                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Same result as ozemu_dgemm (bit for bit), but it never allocates device
+ * memory: no cudaMalloc, cudaFree or allocating library call.  It is meant
+ * for callers that cannot allocate: a host application or framework that
+ * reserves the GPU's memory up front and hands out no more, code whose
+ * allocation calls would synchronise the device on a latency-critical path,
+ * or an environment where an allocation may fail part way through a run.
+ * The source pages have no counterpart to this call; it is a packaging of
+ * the same stages.
+ *
+ * All intermediate data (limb planes, shifts, the transposed copy of B,
+ * residues and a status word) lives in one file-scope static device array of
+ * 64 MiB, which every GPU that loads that part of the library holds until the
+ * process exits.  The problem must fit: with rows_p(x) = round_up(x, 128),
+ * k_p = round_up(k, 128) and 256-byte alignment of each part,
+ *   3 r (rows_p(m) + rows_p(n)) k_p / 2 + 4 (m + n) + r m round_up(n, 16)
+ *   + 8 k n + 256  <=  64 MiB,
+ * otherwise the call returns OZEMU_ERR_SCRATCH_TOO_SMALL before enqueueing
+ * anything (for example m = n = k = 1024 with r = 13 fits; 2048^3 does not).
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array and overwrites what the last call
+ * left there, so calls that overlap on the GPU (different streams, or several
+ * host threads) race: serialise them.  Device-side conditions (non-finite
+ * input, a pipeline wait time-out) are recorded in the array's status word,
+ * which each call clears first; ozemu_get_status does not report them.
+ * Arguments and errors otherwise as ozemu_dgemm. */
+int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const double* B,
+                        int ldb, double* C, int ldc, int r, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -21,10 +21,12 @@ OZEMU_ERR_CUDA = -4
 OZEMU_ERR_NONFINITE = -5
 OZEMU_ERR_TIMEOUT = -6
 OZEMU_ERR_UNSUPPORTED = -7
+OZEMU_ERR_SCRATCH_TOO_SMALL = -8
 
 _STATUS_NAMES = {
     0: "OZEMU_OK", -1: "OZEMU_ERR_INVALID_ARG", -2: "OZEMU_ERR_K_OVERFLOW", -3: "OZEMU_ERR_ALLOC",
     -4: "OZEMU_ERR_CUDA", -5: "OZEMU_ERR_NONFINITE", -6: "OZEMU_ERR_TIMEOUT", -7: "OZEMU_ERR_UNSUPPORTED",
+    -8: "OZEMU_ERR_SCRATCH_TOO_SMALL",
 }
 
 
@@ -57,6 +59,7 @@ _SIGNATURES = {
     "ozemu_crt_f64": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P]),
     "ozemu_get_status": (_I, [_P]),
     "ozemu_release": (None, []),
+    "ozemu_dgemm_noalloc": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
 }
 
 
@@ -158,6 +161,10 @@ def ozemu_get_status(stream):
 
 def ozemu_release():
     _call("ozemu_release")
+
+
+def ozemu_dgemm_noalloc(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
+    return _call("ozemu_dgemm_noalloc", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
 
 
 # ------------------------------------------------------- torch marshalling

@@ -269,6 +269,43 @@ int limb_gemm_s32(int m, int n, int k, const uint8_t* ap, const uint8_t* bp, int
 
 constexpr int kMaxKInt32 = 131071;
 
+// Scratch of the allocation-free entry point: one fixed static device array
+// (its device address is looked up per device, never allocated by us).
+constexpr size_t kNoAllocBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  uint8_t* base = nullptr;  // device address of g_noalloc_scratch
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the static scratch for the current device; the lookup
+// happens once per device with that device current.
+int noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OZEMU_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (!(major == 10 && minor == 3)) return OZEMU_ERR_UNSUPPORTED;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return OZEMU_ERR_CUDA;
+    }
+    d.base = static_cast<uint8_t*>(p);
+    d.ready = true;
+  }
+  *out = d.base;
+  return OZEMU_OK;
+}
+
 }  // namespace
 }  // namespace ozemu
 
@@ -465,6 +502,44 @@ int ozemu_get_status(cudaStream_t stream) {
   if (f & kFlagTimeout) return OZEMU_ERR_TIMEOUT;
   if (f & kFlagNonFinite) return OZEMU_ERR_NONFINITE;
   return OZEMU_OK;
+}
+
+int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C,
+                        int ldc, int r, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (k > 0 && ozemu_bit_budget(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
+  const size_t fl = 256;
+  const size_t pa = align256(plane_bytes(m, k, r)), pb = align256(plane_bytes(n, k, r));
+  const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
+  const size_t rb = align256(ozemu_residue_bytes(m, n, r));
+  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  if (k > 0 && fl + pa + pb + sa + sb + rb + bt > kNoAllocBytes) return OZEMU_ERR_SCRATCH_TOO_SMALL;
+  uint8_t* base = nullptr;
+  int s = noalloc_scratch(&base);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
+  // Only the status word must start at zero; every other part is fully
+  // overwritten by the stage that produces it.
+  if (cudaMemsetAsync(base, 0, fl, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  DeviceState d;
+  d.flags = reinterpret_cast<uint32_t*>(base);
+  uint8_t* ap = base + fl;
+  uint8_t* bp = ap + pa;
+  int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
+  int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
+  uint8_t* res = bp + pb + sa + sb;
+  double* btr = reinterpret_cast<double*>(res + rb);
+  s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, &d, stream);
+  if (s != OZEMU_OK) return s;
+  s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, &d, stream);
+  if (s != OZEMU_OK) return s;
+  s = residue_gemm(m, n, k, r, ap, bp, res, &d, stream);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), stream));
 }
 
 void ozemu_release(void) {
