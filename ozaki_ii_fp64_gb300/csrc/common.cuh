@@ -86,6 +86,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, at most kWaitLimitNs.
 // On time-out sets the device timeout flag and the CTA's abort word and
 // returns false.  Also returns false early once another role of this CTA, or
@@ -160,11 +171,40 @@ __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// Same MMA with the A-operand collector buffer: `fill` reads A from shared
+// memory and keeps it, `use` reads the kept A, `lastuse` reads it and frees
+// the buffer.  Consecutive products with the same A tile then read it once.
+#define OZEMU_MMA_FP4_COLLECTOR(NAME, USAGE)                                                                    \
+  __device__ __forceinline__ void NAME(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,      \
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {            \
+    asm volatile(                                                                                               \
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"                                                          \
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X.collector::a::" USAGE               \
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),                                                  \
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)                     \
+        : "memory");                                                                                            \
+  }
+OZEMU_MMA_FP4_COLLECTOR(mma_fp4_fill, "fill")
+OZEMU_MMA_FP4_COLLECTOR(mma_fp4_use, "use")
+OZEMU_MMA_FP4_COLLECTOR(mma_fp4_lastuse, "lastuse")
+#undef OZEMU_MMA_FP4_COLLECTOR
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 16 columns of 32-bit words: register i holds column i of the
+// 32 lanes x N columns of 32-bit words: register i holds column i of the
 // calling thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "

@@ -1,10 +1,13 @@
 // FP4 limb GEMM on tcgen05: the 9 exact products of [AWE] abstract.
 //
-// One CTA computes one 128 x BN output tile for one modulus l.  For every
+// A persistent grid (one CTA per SM) walks the (modulus l, 128 x BN output
+// tile) pairs.  For every
 // 128-wide K block the three A limb tiles and three B limb tiles (FP4 e2m1,
 // K-major, 64-byte rows, 64-byte swizzle) arrive by TMA into a shared-memory
 // stage; one thread issues the 9 limb products (2 MMAs of K = 64 each) into
-// two TMEM accumulators, folding the limb weights into the block scales:
+// two TMEM accumulators, grouped by A limb so that the A-operand collector
+// buffer serves the three products of each A tile from one shared-memory
+// read, and folding the limb weights into the block scales:
 //
 //   D1 = A0B0 + 13 (A0B1 + A1B0)
 //   D2 = A0B2 + A1B1 + A2B0 + 13 (A1B2 + A2B1) + 169 A2B2
@@ -19,13 +22,18 @@
 // each chunk the epilogue folds D1 + 169 D2 into a running value kept in a
 // third TMEM region and the MMAs restart the accumulators.
 //
+// The epilogue copies the accumulators to registers and releases them at
+// once, so the next chunk's (or tile's) MMAs overlap the modular arithmetic
+// and the stores; the TMA producer runs ahead across tiles through the
+// shared-memory ring.
+//
 // The epilogue reduces D1 + 169 D2 modulo m_l ([AWE] abstract: the
 // formulation holds modulo m) and stores a uint8 residue, or (INT8 product)
 // forms the exact int32 sum.
 //
-// Warp roles (192 threads): warp 0 lane 0 = TMA producer; warp 1 = TMEM
-// allocator, lane 0 = MMA issuer; warps 2..5 = epilogue (TMEM lane quarter
-// = warp % 4).  Every wait is bounded in time; on expiry the kernel flags a
+// Warp roles (320 threads): warp 0 lane 0 = TMA producer; warp 1 = TMEM
+// allocator, lane 0 = MMA issuer; warps 2..9 = epilogue (TMEM lane quarter
+// = warp % 4, half of the tile's columns each).  Every wait is bounded in time; on expiry the kernel flags a
 // time-out, drains what it issued, frees TMEM and exits.
 #include <cstdint>
 #include <cuda.h>
@@ -40,7 +48,8 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBKBytes = 64;             // 128 FP4 elements per K block
 constexpr int kATile = kBM * kBKBytes;   // 8 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each half of the columns
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColD1 = 0, kColD2 = 128, kColRun = 256, kColSf2 = 384, kColSf26 = 416;
 constexpr int kGroupM = 8;               // tile-row group for L2 reuse
@@ -51,6 +60,7 @@ struct Cfg {
   static constexpr int kStage = 3 * kATile + 3 * kBTile;
   static constexpr int kStages = (200 * 1024) / kStage > 8 ? 8 : (200 * 1024) / kStage;
   static constexpr int kSmem = 1024 + kStages * kStage + 256;
+  static constexpr int kCols = BN / 2;   // accumulator columns per epilogue thread
 };
 
 struct GemmArgs {
@@ -59,6 +69,7 @@ struct GemmArgs {
   int kb_chunk;    // K blocks per exact chunk
   int rows_a_p, rows_b_p;
   int tiles_m, tiles_n;
+  int total_tiles; // r * tiles_m * tiles_n
   EpiModuli em;
   uint8_t* res_out;
   long long ldr;
@@ -91,11 +102,36 @@ __device__ __forceinline__ float fmod_small(float x, float m, float inv_m) {
   return fmaf(-q, m, x);
 }
 
+// Tile t -> (modulus l, tile row tm, tile column tn): modulus-major, then
+// groups of kGroupM tile rows swept column by column (L2 reuse).
+__device__ __forceinline__ void tile_coords(int t, const GemmArgs& a, int& l, int& tm, int& tn) {
+  const int per_mod = a.tiles_m * a.tiles_n;
+  l = t / per_mod;
+  const int u = t % per_mod;
+  const int group = kGroupM * a.tiles_n;
+  const int first_m = (u / group) * kGroupM;
+  const int gm = min(kGroupM, a.tiles_m - first_m);
+  tm = first_m + (u % group) % gm;
+  tn = (u % group) / gm;
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CW]) {
+#pragma unroll
+  for (int c = 0; c < CW; c += 8) tmem_ld8(taddr + c, v + c);
+}
+template <int CW>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[CW]) {
+#pragma unroll
+  for (int c = 0; c < CW; c += 8) tmem_st8(taddr + c, v + c);
+}
+
 template <int BN, bool kResidue>
 __global__ void __launch_bounds__(kThreads, 1)
     limb_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs args) {
   using C = Cfg<BN>;
+  constexpr int CW = C::kCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
@@ -115,23 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (skip) return;
 
-  // Tile and modulus of this CTA (modulus-major, grouped tile raster).
-  const int per_mod = args.tiles_m * args.tiles_n;
-  const int l = blockIdx.x / per_mod;
-  const int t = blockIdx.x % per_mod;
-  const int group = kGroupM * args.tiles_n;
-  const int first_m = (t / group) * kGroupM;
-  const int gm = min(kGroupM, args.tiles_m - first_m);
-  const int tm = first_m + (t % group) % gm;
-  const int tn = (t % group) / gm;
-
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 4);
+    mbar_init(tempty, kEpiWarps);
     mbar_init(mma_done, 1);
     *abort_word = 0;
     fence_mbar_init();
@@ -149,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Constant block scales: every byte of the two regions is 2.0 (0x40) or
   // 26.0 (0x5D) in UE4M3, so any scale-factor layout reads the same value.
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t v[16];
 #pragma unroll
@@ -172,152 +198,217 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
-      const int a_row = l * 3 * args.rows_a_p + tm * kBM;
-      const int b_row = l * 3 * args.rows_b_p + tn * BN;
-      int issued = 0;
-      for (int kb = 0; kb < kb_total; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, abort_word, args.flags)) break;
-        uint8_t* st = smem + s * C::kStage;
-        mbar_arrive_expect_tx(&full[s], C::kStage);
+      int it = 0;  // K blocks issued by this CTA (across tiles)
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.total_tiles && ok; t += gridDim.x) {
+        int l, tm, tn;
+        tile_coords(t, args, l, tm, tn);
+        const int a_row = l * 3 * args.rows_a_p + tm * kBM;
+        const int b_row = l * 3 * args.rows_b_p + tn * BN;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_word, args.flags)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * C::kStage;
+          mbar_arrive_expect_tx(&full[s], C::kStage);
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
-          tma_load_2d(st + j * kATile, &tmA, &full[s], kb * kBKBytes, a_row + j * args.rows_a_p);
+          for (int j = 0; j < 3; ++j)
+            tma_load_2d(st + j * kATile, &tmA, &full[s], kb * kBKBytes, a_row + j * args.rows_a_p);
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
-          tma_load_2d(st + 3 * kATile + j * C::kBTile, &tmB, &full[s], kb * kBKBytes, b_row + j * args.rows_b_p);
-        issued = kb + 1;
+          for (int j = 0; j < 3; ++j)
+            tma_load_2d(st + 3 * kATile + j * C::kBTile, &tmB, &full[s], kb * kBKBytes, b_row + j * args.rows_b_p);
+        }
       }
-      if (*abort_word) {
+      if (!ok) {
         // Let the copies already issued land before the CTA exits.
-        for (int kb = (issued > C::kStages ? issued - C::kStages : 0); kb < issued; ++kb)
-          drain_wait(&full[kb % C::kStages], (kb / C::kStages) & 1, args.flags);
+        for (int i = (it > C::kStages ? it - C::kStages : 0); i < it; ++i)
+          drain_wait(&full[i % C::kStages], (i / C::kStages) & 1, args.flags);
       }
     }
+    __syncwarp();  // the whole warp reaches the final barrier together
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = idesc_fp4(BN);
       const uint32_t d1 = tbase + kColD1, d2 = tbase + kColD2;
       const uint32_t s2 = tbase + kColSf2, s26 = tbase + kColSf26;
+      int it = 0;  // K blocks consumed
+      int g = 0;   // accumulator chunks produced
       bool ok = true;
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        if (c > 0) {
-          if (!mbar_wait(tempty, (c - 1) & 1, abort_word, args.flags)) break;
-          tc_fence_after();
-        }
-        const int kb0 = c * args.kb_chunk;
-        const int kb1 = min(kb0 + args.kb_chunk, kb_total);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int s = kb % C::kStages;
-          const uint32_t ph = (kb / C::kStages) & 1;
-          if (!mbar_wait(&full[s], ph, abort_word, args.flags)) {
-            ok = false;
-            break;
+      // Whether stage `it` is already known to be full: tested without
+      // blocking while the previous stage's MMAs fill the (shallow) MMA
+      // queue, so that a blocking wait, which lets the queue drain, is only
+      // paid when the data is actually late.
+      bool known_full = false;
+      for (int t = blockIdx.x; t < args.total_tiles && ok; t += gridDim.x) {
+        for (int c = 0; c < n_chunks && ok; ++c, ++g) {
+          if (g > 0) {
+            // The epilogue has copied the previous chunk out of TMEM.
+            if (!mbar_wait(tempty, (g - 1) & 1, abort_word, args.flags)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * C::kStage);
+          const int kb0 = c * args.kb_chunk;
+          const int kb1 = min(kb0 + args.kb_chunk, kb_total);
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % C::kStages;
+            const uint32_t ph = (it / C::kStages) & 1;
+            if (!known_full && !mbar_wait(&full[s], ph, abort_word, args.flags)) {
+              ok = false;
+              break;
+            }
+            known_full = false;
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + s * C::kStage);
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
-            const uint64_t a1 = smem_desc_sw64(st + 1 * kATile + ks * 32);
-            const uint64_t a2 = smem_desc_sw64(st + 2 * kATile + ks * 32);
-            const uint64_t b0 = smem_desc_sw64(st + 3 * kATile + 0 * C::kBTile + ks * 32);
-            const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * C::kBTile + ks * 32);
-            const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * C::kBTile + ks * 32);
-            const uint32_t acc = (kb == kb0 && ks == 0) ? 0u : 1u;
-            mma_fp4(d1, a0, b0, idesc, s2, s2, acc);
-            mma_fp4(d1, a0, b1, idesc, s2, s26, 1u);
-            mma_fp4(d1, a1, b0, idesc, s26, s2, 1u);
-            mma_fp4(d2, a0, b2, idesc, s2, s2, acc);
-            mma_fp4(d2, a1, b1, idesc, s2, s2, 1u);
-            mma_fp4(d2, a2, b0, idesc, s2, s2, 1u);
-            mma_fp4(d2, a1, b2, idesc, s26, s2, 1u);
-            mma_fp4(d2, a2, b1, idesc, s2, s26, 1u);
-            mma_fp4(d2, a2, b2, idesc, s26, s26, 1u);
+            for (int ks = 0; ks < 2; ++ks) {
+              const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
+              const uint64_t a1 = smem_desc_sw64(st + 1 * kATile + ks * 32);
+              const uint64_t a2 = smem_desc_sw64(st + 2 * kATile + ks * 32);
+              const uint64_t b0 = smem_desc_sw64(st + 3 * kATile + 0 * C::kBTile + ks * 32);
+              const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * C::kBTile + ks * 32);
+              const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * C::kBTile + ks * 32);
+              const uint32_t acc = (kb == kb0 && ks == 0) ? 0u : 1u;
+              // Grouped by A limb so each A tile is read once per K step
+              // (collector buffer), with one A scale per group: the factor
+              // 13 sits on B's scale; A2 B2 (weight 169 = 26 * 26 / 4) needs
+              // the other A scale and is issued on its own.
+              mma_fp4_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+              mma_fp4_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
+              mma_fp4_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
+              mma_fp4_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+              mma_fp4_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
+              mma_fp4_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
+              mma_fp4_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
+              mma_fp4_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
+              mma_fp4(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+              if (ks == 0)
+                known_full = mbar_test_wait(&full[(it + 1) % C::kStages], ((it + 1) / C::kStages) & 1);
+            }
+            tc_commit(&empty[s]);
           }
-          tc_commit(&empty[s]);
+          if (ok) tc_commit(tfull);
         }
-        if (ok) tc_commit(tfull);
       }
       // All MMAs issued by this thread complete before teardown.
       tc_commit(mma_done);
       drain_wait(mma_done, 0, args.flags);
     }
+    __syncwarp();  // the whole warp reaches the final barrier together
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
     const int quarter = warp & 3;
+    const int half = ew >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int grow = tm * kBM + quarter * 32 + lane;
-    const float fm = args.em.m[l], finv = args.em.inv_m[l], fw = args.em.w169[l];
-    for (int c = 0; c < n_chunks; ++c) {
-      if (!warp_wait(tfull, c & 1, abort_word, args.flags)) break;
-      tc_fence_after();
-      const bool last = (c == n_chunks - 1);
-#pragma unroll 1
-      for (int cc = 0; cc < BN / 16; ++cc) {
-        uint32_t v1[16], v2[16], run[16];
-        tmem_ld16(tbase + lane_off + kColD1 + cc * 16, v1);
-        tmem_ld16(tbase + lane_off + kColD2 + cc * 16, v2);
-        if (c > 0) tmem_ld16(tbase + lane_off + kColRun + cc * 16, run);
+    const uint32_t col0 = static_cast<uint32_t>(half * CW);
+    int g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < args.total_tiles && ok; t += gridDim.x) {
+      int l, tm, tn;
+      tile_coords(t, args, l, tm, tn);
+      const int grow = tm * kBM + quarter * 32 + lane;
+      const float fm = args.em.m[l], finv = args.em.inv_m[l], fw = args.em.w169[l];
+      for (int c = 0; c < n_chunks; ++c, ++g) {
+        if (!warp_wait(tfull, g & 1, abort_word, args.flags)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v1[CW], v2[CW];
+        tmem_ld_cols<CW>(tbase + lane_off + kColD1 + col0, v1);
+        tmem_ld_cols<CW>(tbase + lane_off + kColD2 + col0, v2);
         tmem_wait_ld();
-        uint32_t out[16];
-        if constexpr (kResidue) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float r1 = fmod_small(__uint_as_float(v1[i]), fm, finv);
-            float r2 = fmod_small(__uint_as_float(v2[i]), fm, finv);
-            float v = fmaf(r2, fw, r1);
-            if (c > 0) v += __uint_as_float(run[i]);
-            v = fmod_small(v, fm, finv);
-            v = v < 0.f ? v + fm : v;
-            out[i] = last ? static_cast<uint32_t>(__float2int_rn(v)) : __float_as_uint(v);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            int v = __float2int_rn(__uint_as_float(v1[i])) + 169 * __float2int_rn(__uint_as_float(v2[i]));
-            if (c > 0) v += static_cast<int>(run[i]);
-            out[i] = static_cast<uint32_t>(v);
-          }
-        }
-        if (!last) {
-          tmem_st16(tbase + lane_off + kColRun + cc * 16, out);
-        } else if (grow < args.m) {
-          const int gcol = tn * BN + cc * 16;
-          if constexpr (kResidue) {
-            if (gcol < args.ldr) {
-              uint4 w;
-              w.x = out[0] | (out[1] << 8) | (out[2] << 16) | (out[3] << 24);
-              w.y = out[4] | (out[5] << 8) | (out[6] << 16) | (out[7] << 24);
-              w.z = out[8] | (out[9] << 8) | (out[10] << 16) | (out[11] << 24);
-              w.w = out[12] | (out[13] << 8) | (out[14] << 16) | (out[15] << 24);
-              *reinterpret_cast<uint4*>(args.res_out + (static_cast<long long>(l) * args.m + grow) * args.ldr +
-                                        gcol) = w;
-            }
-          } else {
-            int32_t* crow = args.c32 + static_cast<long long>(grow) * args.ldc;
-            const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.c32) & 15u) == 0) &&
-                             (gcol + 16 <= args.n);
-            if (vec) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<int4*>(crow + gcol + 4 * q) =
-                    make_int4(static_cast<int>(out[4 * q]), static_cast<int>(out[4 * q + 1]),
-                              static_cast<int>(out[4 * q + 2]), static_cast<int>(out[4 * q + 3]));
-            } else {
-              for (int i = 0; i < 16; ++i)
-                if (gcol + i < args.n) crow[gcol + i] = static_cast<int32_t>(out[i]);
-            }
-          }
-        }
-      }
-      if (!last) {
-        tmem_wait_st();
+        // Accumulators copied: the next chunk's MMAs may start.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty);
+
+        const bool last = (c == n_chunks - 1);
+        uint32_t out[CW];
+        if constexpr (kResidue) {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) {
+            const float r1 = fmod_small(__uint_as_float(v1[i]), fm, finv);
+            const float r2 = fmod_small(__uint_as_float(v2[i]), fm, finv);
+            out[i] = __float_as_uint(fmaf(r2, fw, r1));  // |.| < 2^17, exact
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < CW; ++i)
+            out[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v1[i])) +
+                                           169 * __float2int_rn(__uint_as_float(v2[i])));
+        }
+        if (c > 0) {
+          tmem_ld_cols<CW>(tbase + lane_off + kColRun + col0, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < CW; ++i) {
+            if constexpr (kResidue)
+              out[i] = __float_as_uint(__uint_as_float(out[i]) + __uint_as_float(v1[i]));
+            else
+              out[i] = static_cast<uint32_t>(static_cast<int>(out[i]) + static_cast<int>(v1[i]));
+          }
+        }
+        if constexpr (kResidue) {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) {
+            float v = fmod_small(__uint_as_float(out[i]), fm, finv);
+            v = v < 0.f ? v + fm : v;  // [0, m)
+            out[i] = last ? static_cast<uint32_t>(__float2int_rn(v)) : __float_as_uint(v);
+          }
+        }
+        if (!last) {
+          tmem_st_cols<CW>(tbase + lane_off + kColRun + col0, out);
+          tmem_wait_st();
+          continue;
+        }
+        if (grow >= args.m) continue;
+        const int gcol0 = tn * BN + static_cast<int>(col0);
+        if constexpr (kResidue) {
+          uint8_t* rrow = args.res_out + (static_cast<long long>(l) * args.m + grow) * args.ldr;
+#pragma unroll
+          for (int q = 0; q < CW; q += 16) {
+            if (CW >= 16) {
+              if (gcol0 + q < args.ldr) {
+                uint4 w;
+                w.x = out[q + 0] | (out[q + 1] << 8) | (out[q + 2] << 16) | (out[q + 3] << 24);
+                w.y = out[q + 4] | (out[q + 5] << 8) | (out[q + 6] << 16) | (out[q + 7] << 24);
+                w.z = out[q + 8] | (out[q + 9] << 8) | (out[q + 10] << 16) | (out[q + 11] << 24);
+                w.w = out[q + 12] | (out[q + 13] << 8) | (out[q + 14] << 16) | (out[q + 15] << 24);
+                *reinterpret_cast<uint4*>(rrow + gcol0 + q) = w;
+              }
+            } else {
+              if (gcol0 < args.ldr) {
+                uint2 w;
+                w.x = out[0] | (out[1] << 8) | (out[2] << 16) | (out[3] << 24);
+                w.y = out[4] | (out[5] << 8) | (out[6] << 16) | (out[7] << 24);
+                *reinterpret_cast<uint2*>(rrow + gcol0) = w;
+              }
+            }
+          }
+        } else {
+          int32_t* crow = args.c32 + static_cast<long long>(grow) * args.ldc;
+          const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.c32) & 15u) == 0);
+#pragma unroll
+          for (int q = 0; q < CW; q += 4) {
+            const int col = gcol0 + q;
+            if (vec && col + 4 <= args.n) {
+              *reinterpret_cast<int4*>(crow + col) =
+                  make_int4(static_cast<int>(out[q]), static_cast<int>(out[q + 1]), static_cast<int>(out[q + 2]),
+                            static_cast<int>(out[q + 3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (col + i < args.n) crow[col + i] = static_cast<int32_t>(out[q + i]);
+            }
+          }
+        }
       }
     }
   }
@@ -325,7 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -380,6 +470,7 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   a.rows_b_p = rows_b_p;
   a.tiles_m = (c.m + kBM - 1) / kBM;
   a.tiles_n = (c.n + BN - 1) / BN;
+  a.total_tiles = r * a.tiles_m * a.tiles_n;
   a.em = c.em;
   a.res_out = c.res_out;
   a.ldr = c.ldr;
@@ -389,8 +480,11 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   auto kern = limb_gemm_kernel<BN, kResidue>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(r) * a.tiles_m * a.tiles_n;
-  kern<<<static_cast<unsigned>(grid), kThreads, Cf::kSmem, stream>>>(ma, mb, a);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = a.total_tiles < sms ? a.total_tiles : sms;  // persistent: one CTA per SM
+  kern<<<grid, kThreads, Cf::kSmem, stream>>>(ma, mb, a);
   return cudaGetLastError();
 }
 

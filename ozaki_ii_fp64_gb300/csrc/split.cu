@@ -140,14 +140,14 @@ __device__ __forceinline__ void load8_f64(const double* rowp, int k, int k0, boo
   }
 }
 
-__global__ void __launch_bounds__(kSplitThreads) split_rows_f64_kernel(const double* __restrict__ X, long long ldx,
-                                                                      int rows, int k, int rows_p, int k_p, int p,
-                                                                      SplitModuli mods, uint8_t* __restrict__ planes,
-                                                                      int32_t* __restrict__ shifts,
-                                                                      uint32_t* flags) {
-  extern __shared__ __align__(16) uint32_t lut[];  // [r][kLutStride]
+template <int R>
+__global__ void __launch_bounds__(kSplitThreads, 3)
+    split_rows_f64_kernel(const double* __restrict__ X, long long ldx, int rows, int k, int rows_p, int k_p, int p,
+                          SplitModuli mods, uint8_t* __restrict__ planes, int32_t* __restrict__ shifts,
+                          uint32_t* flags) {
+  extern __shared__ __align__(16) uint32_t lut[];  // [R][kLutStride]
   __shared__ uint64_t red[kSplitThreads / 32];
-  const int r = mods.r;
+  constexpr int r = R;
   for (int l = 0; l < r; ++l) {
     const uint32_t m = mods.m[l];
     for (uint32_t i = threadIdx.x; i < 2 * m; i += kSplitThreads) {
@@ -205,25 +205,23 @@ __global__ void __launch_bounds__(kSplitThreads) split_rows_f64_kernel(const dou
       }
       uint32_t* o = reinterpret_cast<uint32_t*>(out_row + k0 / 2);
 #pragma unroll
-      for (int l = 0; l < kMaxModuli; ++l) {
-        if (l < r) {
-          const uint32_t c21 = mods.c21x4[l], c42 = mods.c42x4[l], mg = mods.magic4[l], m4 = mods.m[l] * 4u;
-          const char* lt = reinterpret_cast<const char*>(lut + l * kLutStride);
-          uint32_t c[8];
+      for (int l = 0; l < R; ++l) {
+        const uint32_t c21 = mods.c21x4[l], c42 = mods.c42x4[l], mg = mods.magic4[l], m4 = mods.m[l] * 4u;
+        const char* lt = reinterpret_cast<const char*>(lut + l * kLutStride);
+        uint32_t c[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            uint32_t v4 = a2[e] * c42 + (a1[e] * c21 + a0x4[e]);
-            uint32_t q = __umulhi(v4, mg);
-            uint32_t off = v4 - q * m4;
-            c[e] = *reinterpret_cast<const uint32_t*>(lt + off);
-          }
-          uint32_t w0, w1, w2;
-          pack8(c, w0, w1, w2);
-          const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
-          o[pl] = w0;
-          o[pl + plane_stride / 4] = w1;
-          o[pl + 2 * plane_stride / 4] = w2;
+        for (int e = 0; e < 8; ++e) {
+          uint32_t v4 = a2[e] * c42 + (a1[e] * c21 + a0x4[e]);
+          uint32_t q = __umulhi(v4, mg);
+          uint32_t off = v4 - q * m4;
+          c[e] = *reinterpret_cast<const uint32_t*>(lt + off);
         }
+        uint32_t w0, w1, w2;
+        pack8(c, w0, w1, w2);
+        const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
+        __stcs(o + pl, w0);
+        __stcs(o + pl + plane_stride / 4, w1);
+        __stcs(o + pl + 2 * plane_stride / 4, w2);
       }
     }
   }
@@ -286,22 +284,39 @@ int split_grid(int rows_p) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int g = sms * 4;
+  int g = sms * 3;  // three CTAs per SM fit (80 registers x 256 threads)
   return rows_p < g ? rows_p : g;
 }
 
 }  // namespace
 
+template <int R>
+cudaError_t launch_split_r(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
+                           uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+  const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
+  const size_t smem = static_cast<size_t>(R) * kLutStride * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  split_rows_f64_kernel<R><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p, p,
+                                                                                mods, planes, shifts, flags);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
                                   uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
-  const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
-  const size_t smem = static_cast<size_t>(mods.r) * kLutStride * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kMaxModuli * kLutStride * sizeof(uint32_t)));
-  if (e != cudaSuccess) return e;
-  split_rows_f64_kernel<<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p, p, mods,
-                                                                             planes, shifts, flags);
-  return cudaGetLastError();
+  switch (mods.r) {
+#define OZEMU_SPLIT_CASE(R) \
+  case R:                   \
+    return launch_split_r<R>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream);
+    OZEMU_SPLIT_CASE(1) OZEMU_SPLIT_CASE(2) OZEMU_SPLIT_CASE(3) OZEMU_SPLIT_CASE(4) OZEMU_SPLIT_CASE(5)
+    OZEMU_SPLIT_CASE(6) OZEMU_SPLIT_CASE(7) OZEMU_SPLIT_CASE(8) OZEMU_SPLIT_CASE(9) OZEMU_SPLIT_CASE(10)
+    OZEMU_SPLIT_CASE(11) OZEMU_SPLIT_CASE(12) OZEMU_SPLIT_CASE(13) OZEMU_SPLIT_CASE(14) OZEMU_SPLIT_CASE(15)
+    OZEMU_SPLIT_CASE(16)
+#undef OZEMU_SPLIT_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k, uint8_t* planes,
