@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-native", action="store_true")
+    ap.add_argument("--no-compare", action="store_true", help="skip the INT8 residue-GEMM comparison")
     return ap.parse_args()
 
 
@@ -202,6 +203,15 @@ def kernel_traffic():
     return d
 
 
+def gemm_kernel_name(n, k):
+    """The limb-GEMM kernel the library picks for a residue product."""
+    pair = n > 64 and (k + 127) // 128 <= 64 and os.environ.get("OZEMU_GEMM_PAIR", "1") != "0"
+    if pair:
+        return "limb_gemm_pair_kernel (CTA pair, 256x224 tiles)"
+    bn = 16 if n <= 16 else 32 if n <= 32 else 64 if n <= 64 else 128
+    return "limb_gemm_kernel<%d, residue> (one CTA, 128x%d tiles)" % (bn, bn)
+
+
 def workload_name(args, spec):
     base = WORKLOADS[args.workload]
     if all(spec[x] == base[x] for x in ("m", "n", "k")):
@@ -318,7 +328,7 @@ def run_gpu(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp4_peak, 4),
                 "traffic": (round(tr["bytes_per_launch"] * (m * n * k) / tr["mnk"]) if tr else None),
-                "kernel": "limb_gemm_kernel<128,residue>",
+                "kernel": gemm_kernel_name(n, k),
                 "peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (pk_kind, FP4_OVER_BF16),
                 "algorithmic": "9 r 2MNK FP4 flop per launch"}
     # Whole-step roofline: the slower of the FP4 term and the algorithmic bytes at HBM peak.
@@ -377,18 +387,76 @@ def run_gpu(args):
                        "ms_per_step": round(e_ms, 3), "steps": e_steps}
 
     if not args.no_native:
-        # Context: native fp64 GEMM (cuBLAS DGEMM via torch.matmul) on the same GPU.
-        torch.matmul(A[:1024], B)
+        # Context: native fp64 GEMM (cuBLAS DGEMM/DGEMV via torch.matmul) on the
+        # same GPU.  Warmed up on the same shape when that is cheap, median of
+        # up to 5 calls.
+        cheap = flop < 2e11
+        if cheap:
+            torch.matmul(A, B)
+        else:
+            torch.matmul(A[:512], B)
         torch.cuda.synchronize(dev)
-        n0 = torch.cuda.Event(enable_timing=True)
-        n1 = torch.cuda.Event(enable_timing=True)
-        n0.record(stream)
-        torch.matmul(A, B)
-        n1.record(stream)
-        torch.cuda.synchronize(dev)
-        nat_ms = n0.elapsed_time(n1)
+        times = []
+        for _ in range(5 if cheap else 1):
+            n0 = torch.cuda.Event(enable_timing=True)
+            n1 = torch.cuda.Event(enable_timing=True)
+            n0.record(stream)
+            torch.matmul(A, B)
+            n1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(n0.elapsed_time(n1))
+        nat_ms = statistics.median(times)
         line["native_dgemm"] = {"tflops": round(flop / (nat_ms / 1e3) / 1e12, 3), "ms": round(nat_ms, 3),
-                                "speedup_of_emulation": round(nat_ms / ms_per_step, 2)}
+                                "calls": len(times), "speedup_of_emulation": round(nat_ms / ms_per_step, 2)}
+
+    if not args.no_compare:
+        # Comparison: the residue products as one INT8 GEMM per modulus on the
+        # legacy mma.sync tensor path (the tcgen05 INT8 kind does not exist on
+        # sm_103a), and cuBLASLt INT8 (torch._int_mm) on the same residue
+        # matrices as a library reference.
+        a8 = torch.empty(oz.ozemu_res8_bytes(m, k, r), dtype=torch.int8, device=dev)
+        b8 = torch.empty(oz.ozemu_res8_bytes(n, k, r), dtype=torch.int8, device=dev)
+        res8 = torch.empty_like(res)
+        check(oz.ozemu_split_rows_f64_res8(m, k, A.data_ptr(), k, pA, r, a8.data_ptr(), sa.data_ptr(), sh), "res8 A")
+        check(oz.ozemu_split_cols_f64_res8(k, n, B.data_ptr(), n, pB, r, b8.data_ptr(), sb.data_ptr(), sh), "res8 B")
+
+        def i8_gemm():
+            check(oz.ozemu_residue_gemm_i8(m, n, k, r, a8.data_ptr(), b8.data_ptr(), res8.data_ptr(), sh), "i8 gemm")
+
+        i8_gemm()
+        torch.cuda.synchronize(dev)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(3):
+            i8_gemm()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        i8_ms = c0.elapsed_time(c1) / 3
+        same = bool(torch.equal(res8, res))
+        cmp = {"kernel": "residue_gemm_i8_kernel (mma.sync m16n8k32 s8)", "gemm_ms": round(i8_ms, 3),
+               "fp4_limb_gemm_ms": round(gemm_ms, 3), "fp4_speedup": round(i8_ms / gemm_ms, 2),
+               "int8_tops": round(r * flop / (i8_ms / 1e3) / 1e12, 1), "residues_identical": same}
+        rows_p, k_p = (m + 127) // 128 * 128, (k + 127) // 128 * 128
+        cols_p = (n + 127) // 128 * 128
+        if hasattr(torch, "_int_mm") and m >= 32 and n >= 8:
+            try:
+                Am = a8.view(r, rows_p, k_p)[0]
+                Bm = b8.view(r, cols_p, k_p)[0].t()
+                torch._int_mm(Am, Bm)
+                torch.cuda.synchronize(dev)
+                c0.record(stream)
+                for l in range(r):
+                    torch._int_mm(a8.view(r, rows_p, k_p)[l], b8.view(r, cols_p, k_p)[l].t())
+                c1.record(stream)
+                torch.cuda.synchronize(dev)
+                lt_ms = c0.elapsed_time(c1)
+                cmp["cublaslt_int8_ms"] = round(lt_ms, 3)
+                cmp["cublaslt_int8_tops"] = round(r * 2.0 * rows_p * cols_p * k_p / (lt_ms / 1e3) / 1e12, 1)
+            except RuntimeError as exc:  # shape or build constraints of the library call
+                cmp["cublaslt_int8"] = "unavailable: %s" % str(exc).splitlines()[0][:120]
+        line["int8_comparison"] = cmp
+        del a8, b8, res8
 
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_oracle(args.workload, r, CPU_MIN_SECONDS, shape={"m": m, "n": n, "k": k})

@@ -154,6 +154,33 @@ int ozemu_limb_gemm_s32(int m, int n, int k, const uint8_t* a_planes,
                         const uint8_t* b_planes, int32_t* C32, int ldc,
                         cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* INT8 residue-GEMM comparison path                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of the int8 residue planes of `rows` rows of length k, r moduli:
+ * r * round_up(rows, 128) * round_up(k, 128).  0 on bad arguments. host. */
+size_t ozemu_res8_bytes(int rows, int k, int r);
+
+/* Deconstruct the rows of X like ozemu_split_rows_f64 ([TME4] abstract:
+ * scale, round, reduce) but store the balanced residues themselves: int8
+ * [r][round_up(rows,128)][round_up(k,128)], residue of row i, element kk of
+ * modulus l at byte (l*rows_p + i)*k_p + kk; padding holds 0. */
+int ozemu_split_rows_f64_res8(int rows, int k, const double* X, int ldx, int p, int r,
+                              int8_t* res8, int32_t* shifts, cudaStream_t stream);
+
+/* Same for the columns of X (k x cols, row-major).  Uses the workspace. */
+int ozemu_split_cols_f64_res8(int k, int cols, const double* X, int ldx, int p, int r,
+                              int8_t* res8, int32_t* shifts, cudaStream_t stream);
+
+/* Residues of C' = A'B' modulo each modulus from int8 residue planes, one
+ * INT8 x INT8 -> INT32 GEMM per modulus on the warp-level mma.sync tensor
+ * path, then reduction modulo m_l.  The comparison variant of
+ * ozemu_residue_gemm (same output layout and values); the tcgen05 INT8
+ * kind does not exist on sm_103a.  k > 131071 -> OZEMU_ERR_K_OVERFLOW. */
+int ozemu_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8,
+                          const int8_t* b_res8, uint8_t* residues, cudaStream_t stream);
+
 /* Per-output reconstruction ([TME4] abstract): C' in (-M/2, M/2) from its r
  * residues by mixed-radix CRT, then C[i*ldc + j] = RN(C' 2^-(sA[i] + sB[j])),
  * one correct rounding (subnormal and overflow included). */

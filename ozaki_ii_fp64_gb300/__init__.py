@@ -60,6 +60,10 @@ _SIGNATURES = {
     "ozemu_get_status": (_I, [_P]),
     "ozemu_release": (None, []),
     "ozemu_dgemm_noalloc": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
+    "ozemu_res8_bytes": (_S, [_I, _I, _I]),
+    "ozemu_split_rows_f64_res8": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "ozemu_split_cols_f64_res8": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "ozemu_residue_gemm_i8": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
 }
 
 
@@ -149,6 +153,22 @@ def ozemu_residue_gemm(m, n, k, r, a_planes, b_planes, residues, stream):
 
 def ozemu_limb_gemm_s32(m, n, k, a_planes, b_planes, C32, ldc, stream):
     return _call("ozemu_limb_gemm_s32", m, n, k, a_planes, b_planes, C32, ldc, stream)
+
+
+def ozemu_res8_bytes(rows, k, r):
+    return _call("ozemu_res8_bytes", rows, k, r)
+
+
+def ozemu_split_rows_f64_res8(rows, k, X, ldx, p, r, res8, shifts, stream):
+    return _call("ozemu_split_rows_f64_res8", rows, k, X, ldx, p, r, res8, shifts, stream)
+
+
+def ozemu_split_cols_f64_res8(k, cols, X, ldx, p, r, res8, shifts, stream):
+    return _call("ozemu_split_cols_f64_res8", k, cols, X, ldx, p, r, res8, shifts, stream)
+
+
+def ozemu_residue_gemm_i8(m, n, k, r, a_res8, b_res8, residues, stream):
+    return _call("ozemu_residue_gemm_i8", m, n, k, r, a_res8, b_res8, residues, stream)
 
 
 def ozemu_crt_f64(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream):
@@ -276,6 +296,38 @@ def residue_gemm(m, n, k, r, a_planes, b_planes, out=None, stream=None):
     res = torch.empty((r, m, ldr), dtype=torch.uint8, device=a_planes.device) if out is None else out
     _check(ozemu_residue_gemm(m, n, k, r, a_planes.data_ptr(), b_planes.data_ptr(), res.data_ptr(),
                               _stream(stream)), "ozemu_residue_gemm")
+    return res
+
+
+def split_rows_f64_res8(X, p, r, stream=None):
+    """(int8 residues, shifts) of the rows of a cuda float64 matrix."""
+    torch = _torch()
+    rows, k = X.shape
+    res = torch.empty(ozemu_res8_bytes(rows, k, r), dtype=torch.int8, device=X.device)
+    shifts = torch.empty(rows, dtype=torch.int32, device=X.device)
+    _check(ozemu_split_rows_f64_res8(rows, k, X.data_ptr(), _ld(X), p, r, res.data_ptr(), shifts.data_ptr(),
+                                     _stream(stream)), "ozemu_split_rows_f64_res8")
+    return res, shifts
+
+
+def split_cols_f64_res8(X, p, r, stream=None):
+    """(int8 residues, shifts) of the columns of a cuda float64 matrix."""
+    torch = _torch()
+    k, cols = X.shape
+    res = torch.empty(ozemu_res8_bytes(cols, k, r), dtype=torch.int8, device=X.device)
+    shifts = torch.empty(cols, dtype=torch.int32, device=X.device)
+    _check(ozemu_split_cols_f64_res8(k, cols, X.data_ptr(), _ld(X), p, r, res.data_ptr(), shifts.data_ptr(),
+                                     _stream(stream)), "ozemu_split_cols_f64_res8")
+    return res, shifts
+
+
+def residue_gemm_i8(m, n, k, r, a_res8, b_res8, out=None, stream=None):
+    """Residues [r][m][round_up(n, 16)] by the INT8 mma.sync comparison path."""
+    torch = _torch()
+    ldr = (n + 15) // 16 * 16
+    res = torch.empty((r, m, ldr), dtype=torch.uint8, device=a_res8.device) if out is None else out
+    _check(ozemu_residue_gemm_i8(m, n, k, r, a_res8.data_ptr(), b_res8.data_ptr(), res.data_ptr(),
+                                 _stream(stream)), "ozemu_residue_gemm_i8")
     return res
 
 

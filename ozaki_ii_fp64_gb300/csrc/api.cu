@@ -392,6 +392,56 @@ int ozemu_split_cols_s8(int k, int cols, const int8_t* X, int ldx, uint8_t* plan
   return cuda_status(launch_split_rows_s8(t, k > 0 ? k : 1, cols, k, planes, stream));
 }
 
+size_t ozemu_res8_bytes(int rows, int k, int r) {
+  if (rows < 0 || k < 0 || r < 1 || r > kMaxModuli) return 0;
+  return static_cast<size_t>(r) * round_up(rows, kRowAlign) * static_cast<size_t>(round_up(k, kKAlign));
+}
+
+int ozemu_split_rows_f64_res8(int rows, int k, const double* X, int ldx, int p, int r, int8_t* res8,
+                              int32_t* shifts, cudaStream_t stream) {
+  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+    return OZEMU_ERR_INVALID_ARG;
+  if (rows == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !res8 || !shifts || !aligned16(res8) || !rows_ok(rows, r)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_split_rows_f64_res8(X, ldx, rows, k, p, split_moduli(r), res8, shifts, d->flags, stream));
+}
+
+int ozemu_split_cols_f64_res8(int k, int cols, const double* X, int ldx, int p, int r, int8_t* res8,
+                              int32_t* shifts, cudaStream_t stream) {
+  if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+    return OZEMU_ERR_INVALID_ARG;
+  if (cols == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !res8 || !shifts || !aligned16(res8) || !rows_ok(cols, r)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ws = nullptr;
+  s = workspace(d, align256(static_cast<size_t>(k > 0 ? k : 1) * cols * sizeof(double)), &ws);
+  if (s != OZEMU_OK) return s;
+  double* t = reinterpret_cast<double*>(ws);
+  if (k > 0 && launch_transpose_f64(X, ldx, k, cols, t, k, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  return cuda_status(
+      launch_split_rows_f64_res8(t, k > 0 ? k : 1, cols, k, p, split_moduli(r), res8, shifts, d->flags, stream));
+}
+
+int ozemu_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8, const int8_t* b_res8,
+                          uint8_t* residues, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (k > kMaxKInt32) return OZEMU_ERR_K_OVERFLOW;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!residues || !aligned16(residues) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  if (k > 0 && (!a_res8 || !b_res8 || !aligned16(a_res8) || !aligned16(b_res8))) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(cudaMemsetAsync(residues, 0, ozemu_residue_bytes(m, n, r), stream));
+  return cuda_status(launch_residue_gemm_i8(m, n, k, r, a_res8, b_res8, residues, round_up(n, 16), epi_moduli(r),
+                                            stream));
+}
+
 int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
                        uint8_t* residues, cudaStream_t stream) {
   if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;

@@ -123,6 +123,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ----------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+               "r"(bytes)
+               : "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -132,6 +156,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -158,6 +193,42 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+
+// Pair (2-SM) forms: allocation, MMA issued by the pair's first CTA, and a
+// commit that arrives on the same barrier in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+#define OZEMU_MMA_FP4_PAIR(NAME, SUFFIX)                                                                         \
+  __device__ __forceinline__ void NAME(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,      \
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {            \
+    asm volatile(                                                                                               \
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"                                                          \
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X" SUFFIX                             \
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),                                                  \
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)                     \
+        : "memory");                                                                                            \
+  }
+OZEMU_MMA_FP4_PAIR(mma_fp4_pair, "")
+OZEMU_MMA_FP4_PAIR(mma_fp4_pair_fill, ".collector::a::fill")
+OZEMU_MMA_FP4_PAIR(mma_fp4_pair_use, ".collector::a::use")
+OZEMU_MMA_FP4_PAIR(mma_fp4_pair_lastuse, ".collector::a::lastuse")
+#undef OZEMU_MMA_FP4_PAIR
 
 // Block-scaled FP4 MMA, NVFP4 form: A, B e2m1 from shared-memory
 // descriptors, one UE4M3 scale per 16 K-elements read from TMEM.
@@ -237,13 +308,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
 }
 
 // Instruction descriptor: kind::mxf4nvf4, A and B e2m1, K-major, UE4M3
-// scales, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_fp4(int n) {
+// scales, M = m (128 for one CTA, 256 for a CTA pair), N = n.
+__host__ __device__ constexpr uint32_t idesc_fp4(int n, int m = 128) {
   return (1u << 7)                                // A format: e2m1
          | (1u << 10)                             // B format: e2m1
          | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8
          | (0u << 23)                             // scale type UE4M3
-         | (static_cast<uint32_t>(128 >> 4) << 24);  // M / 16
+         | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
 
 }  // namespace ozemu

@@ -36,6 +36,7 @@
 // = warp % 4, half of the tile's columns each).  Every wait is bounded in time; on expiry the kernel flags a
 // time-out, drains what it issued, frees TMEM and exits.
 #include <cstdint>
+#include <cstdlib>
 #include <cuda.h>
 
 #include "common.cuh"
@@ -52,7 +53,7 @@ constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each half
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColD1 = 0, kColD2 = 128, kColRun = 256, kColSf2 = 384, kColSf26 = 416;
-constexpr int kGroupM = 8;               // tile-row group for L2 reuse
+constexpr int kGroupM = 32;              // tile-row group for L2 reuse (32 x 1.5 MB of A planes stay resident)
 
 template <int BN>
 struct Cfg {
@@ -421,6 +422,273 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant: the two CTAs of a cluster compute one 256 x 224 tile with
+// the 2-SM form of the MMA (M = 256): each CTA holds its 128 rows of the A
+// limb tiles and one half (112 rows) of the B limb tiles.  Each MMA then does
+// 1.75x the work of a 128 x 128 one per A-tile read and per stage barrier:
+// the 128 x 128 single-CTA MMA reads shared memory at about the full port
+// rate, which leaves no room for the TMA fills and barrier reads.
+// Used for residue products with n > 64 and a single exact K chunk.
+// ---------------------------------------------------------------------------
+constexpr int kBN2 = 224;                        // pair tile N
+constexpr int kBHalf = kBN2 / 2;                 // B rows per CTA
+constexpr int kBTile2 = kBHalf * kBKBytes;       // 7168 B
+constexpr int kStage2 = 3 * kATile + 3 * kBTile2;
+constexpr int kStages2 = 4;
+constexpr int kSmem2 = 1024 + kStages2 * kStage2 + 256;
+constexpr int kTmemCols2 = 512;
+constexpr uint32_t kColD1p = 0, kColD2p = 224, kColSf2p = 448, kColSf26p = 464;
+constexpr int kPairCols = kBN2 / 2;              // accumulator columns per epilogue thread (two per lane quarter)
+constexpr int kGroupM2 = 16;                     // pair-tile rows per raster group
+
+struct PairArgs {
+  int m, n, kb_total;
+  int rows_a_p, rows_b_p;
+  int tiles_m2, tiles_n2, total_tiles;
+  EpiModuli em;
+  uint8_t* res_out;
+  long long ldr;
+  uint32_t* flags;
+};
+
+__device__ __forceinline__ void pair_tile_coords(int t, const PairArgs& a, int& l, int& tm2, int& tn) {
+  const int per_mod = a.tiles_m2 * a.tiles_n2;
+  l = t / per_mod;
+  const int u = t % per_mod;
+  const int group = kGroupM2 * a.tiles_n2;
+  const int first_m = (u / group) * kGroupM2;
+  const int gm = min(kGroupM2, a.tiles_m2 - first_m);
+  tm2 = first_m + (u % group) % gm;
+  tn = (u % group) / gm;
+}
+
+// After an abort, give copies already issued (whose completion may be
+// signalled in the other CTA) time to land before the pair tears down.
+__device__ __forceinline__ void settle_after_abort() {
+  const uint64_t t0 = globaltimer();
+  while (globaltimer() - t0 < 50000ull) {
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    limb_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const PairArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2);
+  uint64_t* empty = full + kStages2;
+  uint64_t* tfull = empty + kStages2;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* mma_done = tempty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = (rank == 0);
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(&full[s], 1);   // armed by the first CTA with both CTAs' bytes
+      mbar_init(&empty[s], 1);  // one commit from the pair's MMA issuer
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * kEpiWarps);
+    mbar_init(mma_done, 1);
+    *abort_word = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, kTmemCols2);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+  if (warp >= 2 && warp < 6) {
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0x40404040u;
+    tmem_st16(tbase + lane_off + kColSf2p, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0x5D5D5D5Du;
+    tmem_st16(tbase + lane_off + kColSf26p, v);
+    tmem_wait_st();
+  }
+  // Both CTAs' barriers initialised and scales written before any remote
+  // signal or pair MMA.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+
+  const int kb_total = args.kb_total;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      int it = 0;
+      bool ok = true;
+      for (int t = pair; t < args.total_tiles && ok; t += npairs) {
+        int l, tm2, tn;
+        pair_tile_coords(t, args, l, tm2, tn);
+        const int a_row = l * 3 * args.rows_a_p + tm2 * 256 + static_cast<int>(rank) * kBM;
+        const int b_row = l * 3 * args.rows_b_p + tn * kBN2 + static_cast<int>(rank) * kBHalf;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % kStages2;
+          const uint32_t ph = (it / kStages2) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_word, args.flags)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStage2;
+          const uint32_t full_leader = mapa_shared(&full[s], 0);
+          // Only the first CTA arms the barrier (with both CTAs' bytes): a
+          // remote release-arrive from the second CTA would wait for its
+          // earlier bulk copies and serialise the stages.  The phase cannot
+          // complete before it is armed, and the second CTA cannot fill a
+          // stage of the next phase before the pair's MMAs freed it.
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStage2);
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            tma_load_2d_pair(st + j * kATile, &tmA, full_leader, kb * kBKBytes, a_row + j * args.rows_a_p);
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            tma_load_2d_pair(st + 3 * kATile + j * kBTile2, &tmB, full_leader, kb * kBKBytes,
+                             b_row + j * args.rows_b_p);
+        }
+      }
+      if (!ok) settle_after_abort();
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_fp4(kBN2, 256);
+      const uint32_t d1 = tbase + kColD1p, d2 = tbase + kColD2p;
+      const uint32_t s2 = tbase + kColSf2p, s26 = tbase + kColSf26p;
+      int it = 0, g = 0;
+      bool ok = true;
+      bool known_full = false;
+      for (int t = pair; t < args.total_tiles && ok; t += npairs, ++g) {
+        if (g > 0) {
+          if (!mbar_wait(tempty, (g - 1) & 1, abort_word, args.flags)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % kStages2;
+          const uint32_t ph = (it / kStages2) & 1;
+          if (!known_full && !mbar_wait(&full[s], ph, abort_word, args.flags)) {
+            ok = false;
+            break;
+          }
+          known_full = false;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * kStage2);
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
+            const uint64_t a1 = smem_desc_sw64(st + 1 * kATile + ks * 32);
+            const uint64_t a2 = smem_desc_sw64(st + 2 * kATile + ks * 32);
+            const uint64_t b0 = smem_desc_sw64(st + 3 * kATile + 0 * kBTile2 + ks * 32);
+            const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * kBTile2 + ks * 32);
+            const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * kBTile2 + ks * 32);
+            const uint32_t acc = (kb == 0 && ks == 0) ? 0u : 1u;
+            mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+            mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
+            mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
+            mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+            mma_fp4_pair_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
+            mma_fp4_pair_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
+            mma_fp4_pair_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
+            mma_fp4_pair_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
+            mma_fp4_pair(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+            if (ks == 0)
+              known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
+          }
+          tc_commit_pair_multicast(&empty[s], 0x3);
+        }
+        if (ok) tc_commit_pair_multicast(tfull, 0x3);
+      }
+      tc_commit_pair_multicast(mma_done, 0x1);
+      drain_wait(mma_done, 0, args.flags);
+      if (!ok) settle_after_abort();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // 112 columns per thread: fold D1, D2 to residues 16 columns at a time
+    // (packed four to a register), release TMEM, then store.
+    constexpr int CW = kPairCols;
+    constexpr int kSlice = 16;
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half * CW);
+    const uint32_t tempty_leader = mapa_shared(tempty, 0);
+    int g = 0;
+    for (int t = pair; t < args.total_tiles; t += npairs, ++g) {
+      int l, tm2, tn;
+      pair_tile_coords(t, args, l, tm2, tn);
+      const int grow = tm2 * 256 + static_cast<int>(rank) * kBM + quarter * 32 + lane;
+      const float fm = args.em.m[l], finv = args.em.inv_m[l], fw = args.em.w169[l];
+      if (!warp_wait(tfull, g & 1, abort_word, args.flags)) break;
+      tc_fence_after();
+      uint32_t packed[CW / 4];
+#pragma unroll
+      for (int c = 0; c < CW; c += kSlice) {
+        uint32_t v1[kSlice], v2[kSlice];
+        tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0 + c, v1);
+        tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0 + c, v2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < kSlice; i += 4) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float r1 = fmod_small(__uint_as_float(v1[i + e]), fm, finv);
+            const float r2 = fmod_small(__uint_as_float(v2[i + e]), fm, finv);
+            float v = fmod_small(fmaf(r2, fw, r1), fm, finv);
+            v = v < 0.f ? v + fm : v;
+            w |= static_cast<uint32_t>(__float2int_rn(v)) << (8 * e);
+          }
+          packed[(c + i) / 4] = w;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader);
+      if (grow >= args.m) continue;
+      uint8_t* rrow = args.res_out + (static_cast<long long>(l) * args.m + grow) * args.ldr;
+      const int gcol0 = tn * kBN2 + static_cast<int>(col0);
+#pragma unroll
+      for (int q = 0; q < CW; q += 16) {
+        if (gcol0 + q < args.ldr)
+          *reinterpret_cast<uint4*>(rrow + gcol0 + q) =
+              make_uint4(packed[q / 4], packed[q / 4 + 1], packed[q / 4 + 2], packed[q / 4 + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the pair's MMAs, commits and remote signals are all done
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, kTmemCols2);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -488,6 +756,67 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
+  const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
+  const int k_p = round_up(c.k, kKAlign);
+  CUtensorMap ma, mb;
+  if (!make_plane_map(&ma, c.a_planes, k_p, 3LL * c.r * rows_a_p, kBM)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&mb, c.b_planes, k_p, 3LL * c.r * rows_b_p, kBHalf)) return cudaErrorInvalidValue;
+  PairArgs a;
+  a.m = c.m;
+  a.n = c.n;
+  a.kb_total = k_p / 128;
+  a.rows_a_p = rows_a_p;
+  a.rows_b_p = rows_b_p;
+  a.tiles_m2 = (c.m + 255) / 256;
+  a.tiles_n2 = (c.n + kBN2 - 1) / kBN2;
+  a.total_tiles = c.r * a.tiles_m2 * a.tiles_n2;
+  a.em = c.em;
+  a.res_out = c.res_out;
+  a.ldr = c.ldr;
+  a.flags = c.flags;
+  cudaError_t e = cudaFuncSetAttribute(limb_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2);
+  if (e != cudaSuccess) return e;
+  // A persistent grid must not exceed the clusters that can be resident at
+  // once, or the excess clusters start only when others finish.
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem2;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, limb_gemm_pair_kernel, &cfg);
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      int sms = 148;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      n = sms / 2;
+    }
+    max_pairs[dev] = n;
+  }
+  const int pairs = a.total_tiles < max_pairs[dev] ? a.total_tiles : max_pairs[dev];
+  limb_gemm_pair_kernel<<<2 * pairs, kThreads, kSmem2, stream>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+bool use_pair(const LimbGemmCall& c) {
+  if (!c.residue_mode || c.n <= 64) return false;
+  if (round_up(c.k, kKAlign) / 128 > c.kc_blocks) return false;  // one exact K chunk only
+  if (const char* s = std::getenv("OZEMU_GEMM_PAIR")) return s[0] != '0';
+  return true;
+}
+
 template <bool kResidue>
 cudaError_t launch_mode(const LimbGemmCall& c, cudaStream_t stream) {
   if (c.n <= 16) return launch_bn<16, kResidue>(c, stream);
@@ -499,6 +828,7 @@ cudaError_t launch_mode(const LimbGemmCall& c, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream) {
+  if (use_pair(call)) return launch_pair(call, stream);
   return call.residue_mode ? launch_mode<true>(call, stream) : launch_mode<false>(call, stream);
 }
 

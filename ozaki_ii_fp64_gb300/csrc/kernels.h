@@ -13,6 +13,9 @@ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 // Deconstruction of the rows of X into limb planes (split.cu).
 cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
                                   uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream);
+cudaError_t launch_split_rows_f64_res8(const double* X, long long ldx, int rows, int k, int p,
+                                       const SplitModuli& mods, int8_t* res8, int32_t* shifts, uint32_t* flags,
+                                       cudaStream_t stream);
 cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k, uint8_t* planes,
                                  cudaStream_t stream);
 cudaError_t launch_transpose_f64(const double* in, long long ldin, int rows, int cols, double* out,
@@ -37,6 +40,11 @@ struct LimbGemmCall {
   uint32_t* flags;
 };
 cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream);
+
+// INT8 residue GEMM with legacy mma.sync (igemm_mma.cu): the comparison
+// variant computing each modulus's residue product in one INT8 GEMM.
+cudaError_t launch_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8, const int8_t* b_res8,
+                                   uint8_t* res_out, long long ldr, const EpiModuli& em, cudaStream_t stream);
 
 // CRT and scale back (crt.cu).
 cudaError_t launch_crt_f64(int m, int n, const uint8_t* residues, long long ldr, const int32_t* sa,

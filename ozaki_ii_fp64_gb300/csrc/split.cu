@@ -140,7 +140,10 @@ __device__ __forceinline__ void load8_f64(const double* rowp, int k, int k0, boo
   }
 }
 
-template <int R>
+// kRes8 = false: FP4 limb planes [r][3][rows_p][k_p/2] (the FP4 path).
+// kRes8 = true: the balanced residues themselves as int8 [r][rows_p][k_p]
+// (input of the INT8 comparison GEMM).
+template <int R, bool kRes8>
 __global__ void __launch_bounds__(kSplitThreads, 3)
     split_rows_f64_kernel(const double* __restrict__ X, long long ldx, int rows, int k, int rows_p, int k_p, int p,
                           SplitModuli mods, uint8_t* __restrict__ planes, int32_t* __restrict__ shifts,
@@ -153,22 +156,23 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
     for (uint32_t i = threadIdx.x; i < 2 * m; i += kSplitThreads) {
       uint32_t res = (i + m - mods.off[l]) % m;  // residue of x' = u - 2^62
       int bal = static_cast<int>(res) - (res > (m - 1) / 2 ? static_cast<int>(m) : 0);
-      lut[l * kLutStride + i] = limb_code(bal);
+      lut[l * kLutStride + i] = kRes8 ? static_cast<uint32_t>(static_cast<uint8_t>(bal)) : limb_code(bal);
     }
   }
   __syncthreads();
 
-  const long long row_bytes = k_p / 2;
+  const long long row_bytes = kRes8 ? k_p : k_p / 2;
   const long long plane_stride = static_cast<long long>(rows_p) * row_bytes;
+  constexpr int kPlanesPerModulus = kRes8 ? 1 : 3;
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0);
 
   for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
     uint8_t* out_row = planes + static_cast<long long>(row) * row_bytes;
-    if (row >= rows) {  // padding row: digit 0 everywhere
+    if (row >= rows) {  // padding row: digit (or residue) 0 everywhere
       for (int l = 0; l < r; ++l)
-        for (int j = 0; j < 3; ++j) {
-          uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (l * 3 + j) * plane_stride);
-          for (int w = threadIdx.x; w < k_p / 8; w += kSplitThreads) o[w] = 0u;
+        for (int j = 0; j < kPlanesPerModulus; ++j) {
+          uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (l * kPlanesPerModulus + j) * plane_stride);
+          for (int w = threadIdx.x; w < row_bytes / 4; w += kSplitThreads) o[w] = 0u;
         }
       continue;
     }
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
         a1[e] = static_cast<uint32_t>(u >> 21) & 0x1FFFFFu;
         a2[e] = static_cast<uint32_t>(u >> 42);
       }
-      uint32_t* o = reinterpret_cast<uint32_t*>(out_row + k0 / 2);
+      uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : k0 / 2));
 #pragma unroll
       for (int l = 0; l < R; ++l) {
         const uint32_t c21 = mods.c21x4[l], c42 = mods.c42x4[l], mg = mods.magic4[l], m4 = mods.m[l] * 4u;
@@ -216,12 +220,19 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
           uint32_t off = v4 - q * m4;
           c[e] = *reinterpret_cast<const uint32_t*>(lt + off);
         }
-        uint32_t w0, w1, w2;
-        pack8(c, w0, w1, w2);
-        const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
-        __stcs(o + pl, w0);
-        __stcs(o + pl + plane_stride / 4, w1);
-        __stcs(o + pl + 2 * plane_stride / 4, w2);
+        if constexpr (kRes8) {
+          uint2 w;
+          w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+          w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+          __stcs(reinterpret_cast<uint2*>(o + static_cast<long long>(l) * plane_stride / 4), w);
+        } else {
+          uint32_t w0, w1, w2;
+          pack8(c, w0, w1, w2);
+          const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
+          __stcs(o + pl, w0);
+          __stcs(o + pl + plane_stride / 4, w1);
+          __stcs(o + pl + 2 * plane_stride / 4, w2);
+        }
       }
     }
   }
@@ -290,25 +301,26 @@ int split_grid(int rows_p) {
 
 }  // namespace
 
-template <int R>
+template <int R, bool kRes8>
 cudaError_t launch_split_r(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
                            uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
   const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
   const size_t smem = static_cast<size_t>(R) * kLutStride * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R, kRes8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  split_rows_f64_kernel<R><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p, p,
-                                                                                mods, planes, shifts, flags);
+  split_rows_f64_kernel<R, kRes8><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p,
+                                                                                       p, mods, planes, shifts, flags);
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
-                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+template <bool kRes8>
+cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
+                              uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
   switch (mods.r) {
 #define OZEMU_SPLIT_CASE(R) \
   case R:                   \
-    return launch_split_r<R>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream);
+    return launch_split_r<R, kRes8>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream);
     OZEMU_SPLIT_CASE(1) OZEMU_SPLIT_CASE(2) OZEMU_SPLIT_CASE(3) OZEMU_SPLIT_CASE(4) OZEMU_SPLIT_CASE(5)
     OZEMU_SPLIT_CASE(6) OZEMU_SPLIT_CASE(7) OZEMU_SPLIT_CASE(8) OZEMU_SPLIT_CASE(9) OZEMU_SPLIT_CASE(10)
     OZEMU_SPLIT_CASE(11) OZEMU_SPLIT_CASE(12) OZEMU_SPLIT_CASE(13) OZEMU_SPLIT_CASE(14) OZEMU_SPLIT_CASE(15)
@@ -317,6 +329,17 @@ cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int 
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
+                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+  return launch_split_mode<false>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream);
+}
+
+cudaError_t launch_split_rows_f64_res8(const double* X, long long ldx, int rows, int k, int p,
+                                       const SplitModuli& mods, int8_t* res8, int32_t* shifts, uint32_t* flags,
+                                       cudaStream_t stream) {
+  return launch_split_mode<true>(X, ldx, rows, k, p, mods, reinterpret_cast<uint8_t*>(res8), shifts, flags, stream);
 }
 
 cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k, uint8_t* planes,

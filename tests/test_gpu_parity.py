@@ -223,3 +223,56 @@ def test_repeated_calls_and_release(oz):
         status_ok(oz)
         assert (C.cpu().numpy().view(np.int64) == Cref.view(np.int64)).all()
         oz.ozemu_release()
+
+
+# ------------------------------------------------- INT8 comparison path
+
+@pytest.mark.parametrize("rows,k,p,r", [(300, 1000, 44, 13), (129, 257, 30, 5)])
+def test_split_res8_parity(oz, rows, k, p, r):
+    A = special_matrix(rows, k, seed=rows * 5 + k)
+    res, shifts = oz.split_rows_f64_res8(to_dev(A), p, r)
+    status_ok(oz)
+    ref = oracle.deconstruct(A, p, r)
+    assert (shifts.cpu().numpy() == ref["shift"]).all()
+    rows_p, k_p = (rows + 127) // 128 * 128, (k + 127) // 128 * 128
+    got = res.cpu().numpy().reshape(r, rows_p, k_p).astype(np.int64)
+    assert (got[:, :rows, :k] == ref["res"]).all()
+    assert (got[:, rows:, :] == 0).all() and (got[:, :, k:] == 0).all()
+
+
+@pytest.mark.parametrize("m,n,k,r,dist", [(200, 150, 300, 13, "uniform"), (130, 20, 1000, 14, "wide"),
+                                          (256, 256, 9000, 12, "normal")])
+def test_residue_gemm_i8_matches_oracle_and_fp4_path(oz, m, n, k, r, dist):
+    A, B = make_pair(m, n, k, seed=m + 2 * n + k, dist=dist)
+    pA, pB = oz.ozemu_bit_budget(k, r)
+    a8, sa = oz.split_rows_f64_res8(to_dev(A), pA, r)
+    b8, sb = oz.split_cols_f64_res8(to_dev(B), pB, r)
+    res_i8 = oz.residue_gemm_i8(m, n, k, r, a8, b8)
+    ap, _ = oz.split_rows_f64(to_dev(A), pA, r)
+    bp, _ = oz.split_cols_f64(to_dev(B), pB, r)
+    res_fp4 = oz.residue_gemm(m, n, k, r, ap, bp)
+    C = oz.crt_f64(m, n, r, res_i8, sa, sb)
+    status_ok(oz)
+    Cref, st = oracle.dgemm(A, B, r, stages=True)
+    got = res_i8.cpu().numpy()[:, :, :n].astype(np.int64)
+    assert (got == st["res"]).all()
+    assert torch.equal(res_i8[:, :, :n], res_fp4[:, :, :n])
+    assert (C.cpu().numpy().view(np.int64) == Cref.view(np.int64)).all()
+
+
+@pytest.mark.parametrize("m,n,k,r", [(200, 150, 300, 13), (513, 257, 4000, 12), (256, 65, 8192, 13)])
+def test_pair_and_single_cta_gemm_agree(oz, m, n, k, r, monkeypatch):
+    # The CTA-pair kernel (256 x 112 tiles) and the single-CTA kernel (128 x
+    # 128 tiles) must produce identical residues, equal to the oracle's.
+    A, B = make_pair(m, n, k, seed=m + n + 7 * k, dist="wide")
+    pA, pB = oz.ozemu_bit_budget(k, r)
+    ap, _ = oz.split_rows_f64(to_dev(A), pA, r)
+    bp, _ = oz.split_cols_f64(to_dev(B), pB, r)
+    monkeypatch.setenv("OZEMU_GEMM_PAIR", "1")
+    res_pair = oz.residue_gemm(m, n, k, r, ap, bp)
+    monkeypatch.setenv("OZEMU_GEMM_PAIR", "0")
+    res_one = oz.residue_gemm(m, n, k, r, ap, bp)
+    status_ok(oz)
+    assert torch.equal(res_pair[:, :, :n], res_one[:, :, :n])
+    _, st = oracle.dgemm(A, B, r, stages=True)
+    assert (res_pair.cpu().numpy()[:, :, :n].astype(np.int64) == st["res"]).all()

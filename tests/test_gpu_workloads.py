@@ -1,0 +1,92 @@
+"""The workloads at their full sizes, through the C ABI, against the oracle.
+
+The GPU computes every output; the oracle computes sampled rows and columns
+at the full inner dimension (its row/column exponents always see the whole
+row/column).  Sampled fp64 entries must match the oracle bit for bit and lie
+within |C - C_exact| <= 2 K 2^-53 (|A||B|)_ij; the shifts of every row and
+column and the residues of the sampled block must match exactly.  The INT8
+product is compared in full.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import WORKLOADS, workload_inputs, sample_indices
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def oz():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import ozaki_ii_fp64_gb300 as oz
+    oz.load()
+    return oz
+
+
+def run_stages(oz, A_h, B_h, r):
+    """Full product through the stage calls; returns device tensors."""
+    m, k = A_h.shape
+    n = B_h.shape[1]
+    A = torch.from_numpy(A_h).to(DEV)
+    B = torch.from_numpy(B_h).to(DEV)
+    pA, pB = oz.ozemu_bit_budget(k, r)
+    ap, sa = oz.split_rows_f64(A, pA, r)
+    bp, sb = oz.split_cols_f64(B, pB, r)
+    res = oz.residue_gemm(m, n, k, r, ap, bp)
+    C = oz.crt_f64(m, n, r, res, sa, sb)
+    assert oz.get_status() == oz.OZEMU_OK
+    C_direct = oz.dgemm(A, B, r)
+    assert oz.get_status() == oz.OZEMU_OK
+    assert torch.equal(C.view(torch.int64), C_direct.view(torch.int64))
+    del ap, bp, A, B, C_direct
+    return sa.cpu().numpy(), sb.cpu().numpy(), res, C.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,n_rows,n_cols", [
+    ("dgemm_8192_wide", 12, 12),
+    ("dgemv_16384_n1", 96, 1),
+    ("dgemv_16384_n8", 48, 8),
+    ("dgemm_4096_k65536", 8, 8),
+])
+def test_workload_parity_sampled(oz, name, n_rows, n_cols):
+    A_h, B_h, spec = workload_inputs(name)
+    r = spec["r"]
+    m, n, k = spec["m"], spec["n"], spec["k"]
+    sa, sb, res, C = run_stages(oz, A_h, B_h, r)
+    _, pA, pB = oracle.bit_budget(k, r)
+    # shifts of every row of A and every column of B
+    assert (sa == oracle.row_shifts(A_h, pA)).all()
+    assert (sb == oracle.row_shifts(B_h.T, pB)).all()
+    rows = sample_indices(m, n_rows, seed=11)
+    cols = sample_indices(n, n_cols, seed=12)
+    Cref, st = oracle.dgemm_block(A_h, B_h, r, rows=rows, cols=cols, stages=True)
+    got_res = res[:, rows][:, :, cols].cpu().numpy().astype(np.int64)
+    assert (got_res == st["res"]).all()
+    Cs = C[np.ix_(rows, cols)]
+    assert (Cs.view(np.int64) == Cref.view(np.int64)).all()
+    ratio = oracle.error_bound_ratio(A_h[rows], B_h[:, cols], Cs)
+    print("%s r=%d max |C - C_exact| / bound = %.4f" % (name, r, ratio))
+    assert ratio <= 1.0
+
+
+def test_igemm_s8_4096_full(oz):
+    A_h, B_h, spec = workload_inputs("igemm_s8_4096")
+    C = oz.igemm_s8(torch.from_numpy(A_h).to(DEV), torch.from_numpy(B_h).to(DEV))
+    assert oz.get_status() == oz.OZEMU_OK
+    ref = oracle.igemm_s8_direct(A_h, B_h)
+    assert (C.cpu().numpy() == ref).all()
+    # and the limb path of the oracle on a block of it
+    rows = sample_indices(4096, 64, seed=3)
+    cols = sample_indices(4096, 64, seed=4)
+    assert (oracle.igemm_s8(A_h[rows], B_h[:, cols]) == C.cpu().numpy()[np.ix_(rows, cols)]).all()
+
+
+def test_workload_table_is_what_the_tests_cover():
+    assert set(WORKLOADS) == {"dgemm_256_uniform", "igemm_s8_4096", "dgemm_8192_wide", "dgemv_16384_n1",
+                              "dgemv_16384_n8", "dgemm_4096_k65536"}
