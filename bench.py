@@ -186,9 +186,10 @@ def cpu_oracle(name, r, min_seconds, max_steps=0, sample=CPU_SAMPLE, shape=None)
 
 # ------------------------------------------------------------------ GPU arm
 
-def kernel_traffic():
-    """DRAM bytes per launch of the limb GEMM from the committed ncu summary,
-    valid only while the kernel sources are unchanged since the capture."""
+def kernel_traffic(workload):
+    """DRAM bytes per launch of the limb GEMM from the committed ncu record,
+    used only for the workload it was captured on and only while the kernel
+    sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "limb_gemm_traffic.json")
     if not os.path.exists(path):
         return None
@@ -198,7 +199,7 @@ def kernel_traffic():
     for fn in ("gemm_fp4.cu", "common.cuh"):
         with open(os.path.join(ROOT, "ozaki_ii_fp64_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
-    if d.get("source_sha256") != h.hexdigest():
+    if d.get("source_sha256") != h.hexdigest() or d.get("workload") != workload:
         return None
     return d
 
@@ -324,10 +325,10 @@ def run_gpu(args):
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16  # TFLOP/s, burst
     fp4_flop = 9.0 * r * flop
     achieved = fp4_flop / (gemm_ms / 1e3) / 1e12
-    tr = kernel_traffic()
+    tr = kernel_traffic(workload_name(args, spec))
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp4_peak, 4),
-                "traffic": (round(tr["bytes_per_launch"] * (m * n * k) / tr["mnk"]) if tr else None),
+                "traffic": (int(tr["bytes_per_launch"]) if tr else None),
                 "kernel": gemm_kernel_name(n, k),
                 "peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (pk_kind, FP4_OVER_BF16),
                 "algorithmic": "9 r 2MNK FP4 flop per launch"}
