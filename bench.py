@@ -33,6 +33,7 @@ from workloads import WORKLOADS, make_pair  # noqa: E402
 
 METRIC = "emulated DGEMM TFLOP/s (2MNK/t) and % of FP4 roofline at 1 GB300"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
+NARROW_MAX_K = 1 << 24       # k limit of the fused narrow path
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CPU_SAMPLE = 128        # sampled rows and columns of C per oracle step
 CPU_MIN_SECONDS = 10.0  # bounded CPU baseline: repeat the sample at least this long
@@ -255,21 +256,56 @@ def run_gpu(args):
     sb = torch.empty(n, dtype=torch.int32, device=dev)
     res = torch.empty(oz.ozemu_residue_bytes(m, n, r), dtype=torch.uint8, device=dev)
     C = torch.empty((m, n), dtype=torch.float64, device=dev)
-    launches_per_step = 5  # split rows, transpose, split rows of B^T, limb GEMM, CRT
+    # n <= ozemu_narrow_max_n(): the library's fused narrow path (what
+    # ozemu_dgemm runs for such shapes); otherwise the limb-plane path.
+    narrow = n <= oz.ozemu_narrow_max_n() and k <= NARROW_MAX_K and os.environ.get("OZEMU_NARROW", "1") != "0"
 
     def check(st, what):
         if st != 0:
             raise oz.OzemuError(st, what)
 
-    def step(ev0=None, ev1=None):
+    def split_a():
         check(oz.ozemu_split_rows_f64(m, k, A.data_ptr(), k, pA, r, ap.data_ptr(), sa.data_ptr(), sh), "split A")
+
+    def split_b():
         check(oz.ozemu_split_cols_f64(k, n, B.data_ptr(), n, pB, r, bp.data_ptr(), sb.data_ptr(), sh), "split B")
-        if ev0 is not None:
-            ev0.record(stream)
+
+    def limb_gemm():
         check(oz.ozemu_residue_gemm(m, n, k, r, ap.data_ptr(), bp.data_ptr(), res.data_ptr(), sh), "limb gemm")
-        if ev1 is not None:
-            ev1.record(stream)
+
+    def narrow_residues():
+        check(oz.ozemu_residues_narrow_f64(m, n, k, r, A.data_ptr(), k, B.data_ptr(), n, res.data_ptr(),
+                                           sa.data_ptr(), sb.data_ptr(), sh), "narrow residues")
+
+    def crt():
         check(oz.ozemu_crt_f64(m, n, r, res.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), n, sh), "crt")
+
+    # The bracketed stage (ev0 .. ev1) is the step's dominant kernel.
+    if narrow:
+        stages = [("narrow_residues", narrow_residues), ("crt", crt)]
+        dominant = "narrow_residues"
+        launches_per_step = 3  # B's column residues, fused pass over A, CRT
+    else:
+        stages = [("split_A", split_a), ("split_B", split_b), ("limb_gemm", limb_gemm), ("crt", crt)]
+        dominant = "limb_gemm"
+        launches_per_step = 5  # split rows, transpose, split rows of B^T, limb GEMM, CRT
+
+    def step(ev0=None, ev1=None):
+        for name, fn in stages:
+            if name == dominant and ev0 is not None:
+                ev0.record(stream)
+            fn()
+            if name == dominant and ev1 is not None:
+                ev1.record(stream)
+
+    def stage_times(which):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(which) + 1)]
+        evs[0].record(stream)
+        for i, (_, fn) in enumerate(which):
+            fn()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        return {name: evs[i].elapsed_time(evs[i + 1]) for i, (name, _) in enumerate(which)}
 
     for _ in range(args.warmup):
         step()
@@ -278,19 +314,7 @@ def run_gpu(args):
         raise SystemExit("device status not OK after warm-up")
 
     # Per-stage durations (one untimed pass, for the report only).
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    evs[0].record(stream)
-    check(oz.ozemu_split_rows_f64(m, k, A.data_ptr(), k, pA, r, ap.data_ptr(), sa.data_ptr(), sh), "split A")
-    evs[1].record(stream)
-    check(oz.ozemu_split_cols_f64(k, n, B.data_ptr(), n, pB, r, bp.data_ptr(), sb.data_ptr(), sh), "split B")
-    evs[2].record(stream)
-    check(oz.ozemu_residue_gemm(m, n, k, r, ap.data_ptr(), bp.data_ptr(), res.data_ptr(), sh), "limb gemm")
-    evs[3].record(stream)
-    check(oz.ozemu_crt_f64(m, n, r, res.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), n, sh), "crt")
-    evs[4].record(stream)
-    torch.cuda.synchronize(dev)
-    stage_ms = {"split_A": evs[0].elapsed_time(evs[1]), "split_B": evs[1].elapsed_time(evs[2]),
-                "limb_gemm": evs[2].elapsed_time(evs[3]), "crt": evs[3].elapsed_time(evs[4])}
+    stage_ms = stage_times(stages)
 
     # Timed region.
     g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -311,7 +335,7 @@ def run_gpu(args):
     if ws > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    gemm_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
+    dom_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
     status = oz.ozemu_get_status(sh)
     if status != 0:
         raise SystemExit("device status %d after the timed region" % status)
@@ -324,31 +348,58 @@ def run_gpu(args):
     pk, pk_kind = peaks()
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16  # TFLOP/s, burst
     fp4_flop = 9.0 * r * flop
-    achieved = fp4_flop / (gemm_ms / 1e3) / 1e12
-    tr = kernel_traffic(workload_name(args, spec))
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / fp4_peak, 4),
-                "traffic": (int(tr["bytes_per_launch"]) if tr else None),
-                "kernel": gemm_kernel_name(n, k),
-                "peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (pk_kind, FP4_OVER_BF16),
-                "algorithmic": "9 r 2MNK FP4 flop per launch"}
-    # Whole-step roofline: the slower of the FP4 term and the algorithmic bytes at HBM peak.
-    # K1 reads 8 B and writes 1.5 r B per input element, K2 reads the planes
-    # once (1.5 r B per input element) and writes r B per output, K3 reads
-    # r B and writes 8 B per output.
-    bytes_alg = (m * k + k * n) * (8 + 3.0 * r) + m * n * (2.0 * r + 8)
-    t_roof = max(fp4_flop / (fp4_peak * 1e12), bytes_alg / (pk["hbm_gbs"] * 1e9))
+    if narrow:
+        # HBM-bound: A and B read once, residues written once.
+        kbytes = 8.0 * (m * k + k * n) + r * m * n
+        achieved = kbytes / (dom_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(pk["hbm_gbs"], 1),
+                    "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                    "kernel": "dgemv_fused_kernel (fused deconstruction + product, narrow B)",
+                    "peak_source": "%s HBM copy bandwidth" % pk_kind,
+                    "algorithmic": "8 (mk + kn) + r m n bytes per launch"}
+        bytes_alg = 8.0 * (m * k + k * n + m * n)
+        t_roof = bytes_alg / (pk["hbm_gbs"] * 1e9)
+    else:
+        achieved = fp4_flop / (dom_ms / 1e3) / 1e12
+        tr = kernel_traffic(workload_name(args, spec))
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
+                    "traffic": (int(tr["bytes_per_launch"]) if tr else None),
+                    "kernel": gemm_kernel_name(n, k),
+                    "peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (pk_kind, FP4_OVER_BF16),
+                    "algorithmic": "9 r 2MNK FP4 flop per launch"}
+        # Whole-step roofline: the slower of the FP4 term and the algorithmic
+        # bytes at HBM peak.  K1 reads 8 B and writes 1.5 r B per input
+        # element, K2 reads the planes once (1.5 r B per input element) and
+        # writes r B per output, K3 reads r B and writes 8 B per output.
+        bytes_alg = (m * k + k * n) * (8 + 3.0 * r) + m * n * (2.0 * r + 8)
+        t_roof = max(fp4_flop / (fp4_peak * 1e12), bytes_alg / (pk["hbm_gbs"] * 1e9))
     pct_roof = 100.0 * t_roof / (ms_per_step / 1e3)
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args, spec), "m": m, "n": n, "k": k, "r": r, "dist": spec["dist"],
-                       "seed": spec["seed"], "l2": "inputs larger than L2 (%d MiB per operand), no flush"
-                                                    % (m * k * 8 >> 20)},
-            "pct_fp4_roofline": round(pct_roof, 2), "roofline": roofline,
+                       "seed": spec["seed"], "path": "narrow (fused)" if narrow else "limb planes",
+                       "l2": "inputs larger than L2 (%d MiB per operand), no flush" % (m * k * 8 >> 20)},
+            "pct_fp4_roofline" if not narrow else "pct_io_roofline": round(pct_roof, 2), "roofline": roofline,
             "stage_ms": {kk: round(v, 3) for kk, v in stage_ms.items()},
             "gpu_launches": launches_per_step * args.steps, "clocks": clk}
+
+    # The limb-plane path on the same narrow problem, for comparison.
+    plane_stages = [("split_A", split_a), ("split_B", split_b), ("limb_gemm", limb_gemm), ("crt", crt)]
+    if narrow:
+        C_narrow = C.clone()
+        stage_times(plane_stages)
+        pl = stage_times(plane_stages)
+        if not torch.equal(C.view(torch.int64), C_narrow.view(torch.int64)):
+            raise SystemExit("narrow and limb-plane paths differ")
+        line["limb_plane_path"] = {"stage_ms": {kk: round(v, 3) for kk, v in pl.items()},
+                                   "ms_per_step": round(sum(pl.values()), 3),
+                                   "narrow_speedup": round(sum(pl.values()) / ms_per_step, 2)}
+        gemm_ms = pl["limb_gemm"]
+    else:
+        gemm_ms = dom_ms
 
     # End to end through the C ABI with host buffers: H2D of A and B from
     # pinned memory, ozemu_dgemm, D2H of C, every step.
@@ -381,7 +432,7 @@ def run_gpu(args):
         if oz.ozemu_get_status(sh) != 0:
             raise SystemExit("device status not OK after e2e")
         # the result must be the device-timed path's result
-        if not torch.equal(C_pin, C.cpu()):
+        if not torch.equal(C_pin.view(torch.int64), C.cpu().view(torch.int64)):
             raise SystemExit("e2e result differs from the staged result")
         line["e2e"] = {"value": round(ws * flop / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": int(A_h.nbytes + B_h.nbytes), "d2h_bytes_per_step": int(m * n * 8),

@@ -91,7 +91,11 @@ int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B,
  * recombination ([AWE] abstract), CRT and one correct rounding per entry of
  * C' 2^-(s_i + t_j).  Requires 2k < m_1...m_r (else OZEMU_ERR_INVALID_ARG).
  * m, n or k = 0 is a no-op (k = 0 zeroes C).  Inf/NaN in A or B sets the
- * non-finite flag; C is then unspecified.  Uses the cached workspace. */
+ * non-finite flag; C is then unspecified.  Uses the cached workspace.
+ * For n <= ozemu_narrow_max_n(), k <= 2^24 and p_A <= 52 (every k when
+ * r <= 13) the residues come from the fused narrow path
+ * (ozemu_residues_narrow_f64) instead of limb planes; the result is the same
+ * bit for bit. */
 int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
                 int ldb, double* C, int ldc, int r, cudaStream_t stream);
 
@@ -153,6 +157,28 @@ int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes,
 int ozemu_limb_gemm_s32(int m, int n, int k, const uint8_t* a_planes,
                         const uint8_t* b_planes, int32_t* C32, int ldc,
                         cudaStream_t stream);
+
+/* Largest n taken by ozemu_residues_narrow_f64 (2). host. */
+int ozemu_narrow_max_n(void);
+
+/* Residues of C' = A'B' for a narrow product, 1 <= n <= ozemu_narrow_max_n()
+ * and 1 <= k <= 2^24, without limb planes: the deconstruction of A's rows is
+ * fused with the products.  [TME4] abstract: below the critical intensity
+ * OI* the deconstruction of the streamed operand (the fourth term of the TME
+ * model) bounds the emulation, so each element of A is read once, scaled,
+ * rounded and reduced modulo every m_l in registers and multiplied with B's
+ * residues at once; the modular reduction of the sums happens once per
+ * output.  A (m x k, lda >= k) and B (k x n, ldb >= n) are row-major fp64
+ * device pointers.  Writes shifts_a[m] and shifts_b[n] (int32, s_i and t_j
+ * for the budget ozemu_bit_budget(k, r)) and the residues (residue layout
+ * above, 16-byte aligned): the same bytes as ozemu_split_rows_f64 +
+ * ozemu_split_cols_f64 + ozemu_residue_gemm.  Inf/NaN set the non-finite
+ * flag.  Uses the cached workspace for B's residues.  n or k out of range,
+ * 2k >= m_1...m_r, or a budget p_A > 52 (r >= 14 with small k) ->
+ * OZEMU_ERR_INVALID_ARG. */
+int ozemu_residues_narrow_f64(int m, int n, int k, int r, const double* A, int lda,
+                              const double* B, int ldb, uint8_t* residues,
+                              int32_t* shifts_a, int32_t* shifts_b, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* INT8 residue-GEMM comparison path                                        */

@@ -64,6 +64,8 @@ _SIGNATURES = {
     "ozemu_split_rows_f64_res8": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
     "ozemu_split_cols_f64_res8": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
     "ozemu_residue_gemm_i8": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
+    "ozemu_narrow_max_n": (_I, []),
+    "ozemu_residues_narrow_f64": (_I, [_I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P]),
 }
 
 
@@ -169,6 +171,14 @@ def ozemu_split_cols_f64_res8(k, cols, X, ldx, p, r, res8, shifts, stream):
 
 def ozemu_residue_gemm_i8(m, n, k, r, a_res8, b_res8, residues, stream):
     return _call("ozemu_residue_gemm_i8", m, n, k, r, a_res8, b_res8, residues, stream)
+
+
+def ozemu_narrow_max_n():
+    return _call("ozemu_narrow_max_n")
+
+
+def ozemu_residues_narrow_f64(m, n, k, r, A, lda, B, ldb, residues, shifts_a, shifts_b, stream):
+    return _call("ozemu_residues_narrow_f64", m, n, k, r, A, lda, B, ldb, residues, shifts_a, shifts_b, stream)
 
 
 def ozemu_crt_f64(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream):
@@ -337,6 +347,22 @@ def limb_gemm_s32(m, n, k, a_planes, b_planes, out=None, stream=None):
     _check(ozemu_limb_gemm_s32(m, n, k, a_planes.data_ptr(), b_planes.data_ptr(), C.data_ptr(), _ld(C),
                                _stream(stream)), "ozemu_limb_gemm_s32")
     return C
+
+
+def residues_narrow_f64(A, B, r, stream=None):
+    """(residues, shifts_a, shifts_b) of A @ B for a narrow B (n <= 2) by the
+    fused path: no limb planes."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2:
+        raise ValueError("inner dimensions differ")
+    res = torch.empty(ozemu_residue_bytes(m, n, r), dtype=torch.uint8, device=A.device)
+    sa = torch.empty(m, dtype=torch.int32, device=A.device)
+    sb = torch.empty(n, dtype=torch.int32, device=A.device)
+    _check(ozemu_residues_narrow_f64(m, n, k, r, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), res.data_ptr(),
+                                     sa.data_ptr(), sb.data_ptr(), _stream(stream)), "ozemu_residues_narrow_f64")
+    return res.view(r, m, (n + 15) // 16 * 16), sa, sb
 
 
 def crt_f64(m, n, r, residues, shifts_a, shifts_b, out=None, stream=None):

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIBNAME = "libozemu.so"
-SOURCES = ["api.cu", "split.cu", "gemm_fp4.cu", "crt.cu", "igemm_mma.cu"]
+SOURCES = ["api.cu", "split.cu", "gemm_fp4.cu", "crt.cu", "igemm_mma.cu", "gemv.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

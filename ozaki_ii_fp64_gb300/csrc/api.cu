@@ -94,6 +94,26 @@ SplitModuli split_moduli(int r) {
   return s;
 }
 
+NarrowModuli narrow_moduli(int r) {
+  NarrowModuli nm;
+  std::memset(&nm, 0, sizeof(nm));
+  nm.r = r;
+  for (int l = 0; l < r; ++l) {
+    const uint32_t m = moduli().m[l];
+    nm.m[l] = m;
+    nm.c21[l] = pow_mod(2, 21, m);
+    nm.c42[l] = pow_mod(2, 42, m);
+    nm.off62[l] = pow_mod(2, 62, m);
+  }
+  return nm;
+}
+
+// The fused narrow-N path is used for n <= kNarrowMaxN unless OZEMU_NARROW=0.
+bool narrow_enabled() {
+  const char* s = std::getenv("OZEMU_NARROW");
+  return !(s && s[0] == '0');
+}
+
 EpiModuli epi_moduli(int r) {
   EpiModuli e;
   std::memset(&e, 0, sizeof(e));
@@ -245,6 +265,55 @@ int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* b
   c.em = epi_moduli(r);
   c.flags = d->flags;
   return cuda_status(launch_limb_gemm(c, st));
+}
+
+// Residues and shifts of C' = A'B' for n <= kNarrowMaxN: B's column
+// residues, then the fused pass over A's rows.  Same bytes as the
+// limb-plane path.
+int narrow_residues(int m, int n, int k, const double* A, long long lda, const double* B, long long ldb, int r,
+                    int pa_bits, int pb_bits, uint8_t* res, int32_t* sa, int32_t* sb, DeviceState* d,
+                    cudaStream_t st) {
+  NarrowCall c;
+  c.m = m;
+  c.n = n;
+  c.k = k;
+  c.kp = round_up(k, 16);
+  c.pA = pa_bits;
+  c.pB = pb_bits;
+  c.A = A;
+  c.lda = lda;
+  c.B = B;
+  c.ldb = ldb;
+  c.nm = narrow_moduli(r);
+  c.ldr = round_up(n, 16);
+  const size_t bres = align256(static_cast<size_t>(n) * r * c.kp);
+  uint8_t* ws = nullptr;
+  int s = workspace(d, bres, &ws);
+  if (s != OZEMU_OK) return s;
+  c.bres = ws;
+  c.res = res;
+  c.sa = sa;
+  c.sb = sb;
+  c.flags = d->flags;
+  return cuda_status(launch_narrow_residues(c, st));
+}
+
+// C = A B for n <= kNarrowMaxN through narrow_residues and the CRT.
+int dgemm_narrow(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc, int r,
+                 int pa_bits, int pb_bits, DeviceState* d, cudaStream_t st) {
+  const size_t bres = align256(static_cast<size_t>(n) * r * round_up(k, 16));
+  const size_t rb = align256(ozemu_residue_bytes(m, n, r));
+  const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
+  uint8_t* ws = nullptr;
+  int s = workspace(d, bres + rb + sa + sb, &ws);
+  if (s != OZEMU_OK) return s;
+  // narrow_residues takes the front of the same workspace for B's residues.
+  uint8_t* res = ws + bres;
+  int32_t* sap = reinterpret_cast<int32_t*>(res + rb);
+  int32_t* sbp = reinterpret_cast<int32_t*>(res + rb + sa);
+  s = narrow_residues(m, n, k, A, lda, B, ldb, r, pa_bits, pb_bits, res, sap, sbp, d, st);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), st));
 }
 
 int limb_gemm_s32(int m, int n, int k, const uint8_t* ap, const uint8_t* bp, int32_t* C, long long ldc,
@@ -472,6 +541,24 @@ int ozemu_limb_gemm_s32(int m, int n, int k, const uint8_t* a_planes, const uint
   return limb_gemm_s32(m, n, k, a_planes, b_planes, C32, ldc, d, stream);
 }
 
+int ozemu_narrow_max_n(void) { return kNarrowMaxN; }
+
+int ozemu_residues_narrow_f64(int m, int n, int k, int r, const double* A, int lda, const double* B, int ldb,
+                              uint8_t* residues, int32_t* shifts_a, int32_t* shifts_b, cudaStream_t stream) {
+  if (m < 0 || n < 1 || n > kNarrowMaxN || k < 1 || k > kNarrowMaxK || r < 1 || r > kMaxModuli)
+    return OZEMU_ERR_INVALID_ARG;
+  if (lda < k || ldb < n) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0) return OZEMU_OK;
+  if (!A || !B || !residues || !aligned16(residues) || !shifts_a || !shifts_b || !rows_ok(m, r))
+    return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (ozemu_bit_budget(k, r, &pa_bits, &pb_bits) != OZEMU_OK || pa_bits > kNarrowMaxP) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  return narrow_residues(m, n, k, A, lda, B, ldb, r, pa_bits, pb_bits, residues, shifts_a, shifts_b, d, stream);
+}
+
 int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a, const int32_t* shifts_b,
                   double* C, int ldc, cudaStream_t stream) {
   if (m < 0 || n < 0 || r < 1 || r > kMaxModuli || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
@@ -519,6 +606,8 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   int s = device_state(&d);
   if (s != OZEMU_OK) return s;
   if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
+  if (n <= kNarrowMaxN && k <= kNarrowMaxK && pa_bits <= kNarrowMaxP && narrow_enabled())
+    return dgemm_narrow(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, d, stream);
   const size_t pa = align256(plane_bytes(m, k, r)), pb = align256(plane_bytes(n, k, r));
   const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
   const size_t rb = align256(ozemu_residue_bytes(m, n, r));

@@ -34,6 +34,15 @@ struct SplitModuli {
   uint32_t off[kMaxModuli];     // 2^62 mod m
 };
 
+// Per-modulus constants for the fused narrow-N path.
+struct NarrowModuli {
+  int r;
+  uint32_t m[kMaxModuli];
+  uint32_t c21[kMaxModuli];    // 2^21 mod m
+  uint32_t c42[kMaxModuli];    // 2^42 mod m
+  uint32_t off62[kMaxModuli];  // 2^62 mod m
+};
+
 // Per-modulus constants for the GEMM epilogue.
 struct EpiModuli {
   float m[kMaxModuli];

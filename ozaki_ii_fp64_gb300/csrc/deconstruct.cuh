@@ -1,0 +1,83 @@
+// Device helpers of the deconstruction step shared by the split kernels and
+// the fused narrow-N kernel: the row (column) exponent, and the power-of-two
+// scaling with round-half-even to an integer, all as integer bit arithmetic
+// on the fp64 pattern ([TME4] abstract: operands are scaled, rounded and
+// reduced modulo each modulus; no fp64 arithmetic is used here).
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace ozemu {
+
+// round-half-even(x 2^s) + 2^62 for the finite double with bit pattern `bits`
+// (|result - 2^62| <= 2^62 is guaranteed by the row shift).  Non-finite -> 0.
+__device__ __forceinline__ uint64_t scaled_offset(uint64_t bits, int s) {
+  uint32_t E = static_cast<uint32_t>(bits >> 52) & 0x7FFu;
+  uint64_t mant = bits & 0xFFFFFFFFFFFFFull;
+  int e0 = -1074;
+  if (E != 0) {
+    mant |= 1ull << 52;
+    e0 = static_cast<int>(E) - 1075;
+  }
+  if (E == 0x7FFu) mant = 0;
+  uint64_t q = 0;
+  if (mant != 0) {
+    int sh = e0 + s;
+    if (sh >= 0) {
+      q = mant << sh;
+    } else {
+      int d = -sh;
+      d = d > 63 ? 63 : d;
+      q = mant >> d;
+      uint64_t rem = mant & ((1ull << d) - 1ull);
+      uint64_t half = 1ull << (d - 1);
+      q += static_cast<uint64_t>((rem > half) | ((rem == half) & (q & 1ull)));
+    }
+  }
+  int64_t v = (bits >> 63) ? -static_cast<int64_t>(q) : static_cast<int64_t>(q);
+  return static_cast<uint64_t>(v + (1ll << 62));
+}
+
+// frexp exponent of the double with (non-negative, nonzero) bit pattern b.
+__device__ __forceinline__ int frexp_exp_bits(uint64_t b) {
+  uint32_t E = static_cast<uint32_t>(b >> 52);
+  if (E) return static_cast<int>(E) - 1022;
+  return (64 - __clzll(static_cast<long long>(b))) - 1074;
+}
+
+template <int kThreads>
+__device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* red) {
+  for (int o = 16; o > 0; o >>= 1) {
+    uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
+  }
+  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  uint64_t m = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) m = red[w] > m ? red[w] : m;
+  return m;
+}
+
+__device__ __forceinline__ void load8_f64(const double* rowp, int k, int k0, bool vec_ok, uint64_t (&b)[8],
+                                          bool last_use) {
+  if (vec_ok && k0 + 8 <= k) {
+    const double2* p = reinterpret_cast<const double2*>(rowp + k0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      double2 v = last_use ? __ldcs(p + q) : __ldg(p + q);
+      b[2 * q] = static_cast<uint64_t>(__double_as_longlong(v.x));
+      b[2 * q + 1] = static_cast<uint64_t>(__double_as_longlong(v.y));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      b[e] = (k0 + e < k) ? static_cast<uint64_t>(__double_as_longlong(rowp[k0 + e])) : 0ull;
+  }
+}
+
+}  // namespace ozemu

@@ -46,6 +46,29 @@ cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream);
 cudaError_t launch_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8, const int8_t* b_res8,
                                    uint8_t* res_out, long long ldr, const EpiModuli& em, cudaStream_t stream);
 
+// Fused deconstruction + product for narrow B (gemv.cu): residues of
+// C = A B for n <= kNarrowMaxN columns without limb planes.  Writes the
+// residues [r][m][ldr] and shifts that launch_crt_f64 consumes.
+constexpr int kNarrowMaxN = 2;
+constexpr int kNarrowMaxK = 1 << 24;
+constexpr int kNarrowMaxP = 52;  // p_A: scaled elements are right shifts of the significand
+struct NarrowCall {
+  int m, n, k, kp;  // kp: k rounded up to 16
+  int pA, pB;
+  const double* A;
+  long long lda;
+  const double* B;
+  long long ldb;
+  NarrowModuli nm;
+  uint8_t* bres;    // [n][r][kp] residues of B's columns
+  uint8_t* res;     // [r][m][ldr]
+  long long ldr;
+  int32_t* sa;
+  int32_t* sb;
+  uint32_t* flags;
+};
+cudaError_t launch_narrow_residues(const NarrowCall& call, cudaStream_t stream);
+
 // CRT and scale back (crt.cu).
 cudaError_t launch_crt_f64(int m, int n, const uint8_t* residues, long long ldr, const int32_t* sa,
                            const int32_t* sb, double* C, long long ldc, const CrtModuli& cm, cudaStream_t stream);

@@ -97,6 +97,13 @@ FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
     lambda oz: oz.ozemu_residue_gemm(4, 4, 4, 13, FAKE, FAKE, FAKE + 4, NULL),    # unaligned residues
     lambda oz: oz.ozemu_limb_gemm_s32(4, 4, 4, FAKE, FAKE, FAKE, 3, NULL),        # ldc < n
     lambda oz: oz.ozemu_crt_f64(4, 4, 13, FAKE, FAKE, NULL, FAKE, 4, NULL),
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 3, 4, 13, FAKE, 4, FAKE, 3, FAKE, FAKE, FAKE, NULL),  # n > 2
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 0, 13, FAKE, 1, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # k < 1
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 1 << 25, 16, FAKE, 1 << 25, FAKE, 1, FAKE, FAKE, FAKE, NULL),
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 2, 4, 13, FAKE, 4, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # ldb < n
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 4, 13, FAKE, 4, FAKE, 1, FAKE + 8, FAKE, FAKE, NULL),
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 200, 1, FAKE, 200, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # 2k >= M
+    lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 5, 16, FAKE, 5, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # p_A > 52
 ])
 def test_invalid_arguments_rejected_on_host(oz, call):
     assert call(oz) == oz.OZEMU_ERR_INVALID_ARG
@@ -105,6 +112,10 @@ def test_invalid_arguments_rejected_on_host(oz, call):
 def test_k_overflow_rejected_on_host(oz):
     assert oz.ozemu_igemm_s8(4, 4, 131072, FAKE, FAKE, FAKE, NULL) == oz.OZEMU_ERR_K_OVERFLOW
     assert oz.ozemu_limb_gemm_s32(4, 4, 131072, FAKE, FAKE, FAKE, 4, NULL) == oz.OZEMU_ERR_K_OVERFLOW
+
+
+def test_narrow_limit(oz):
+    assert oz.ozemu_narrow_max_n() == 2
 
 
 def test_empty_problems_are_noops(oz):
