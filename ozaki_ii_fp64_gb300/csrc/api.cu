@@ -94,7 +94,7 @@ SplitModuli split_moduli(int r) {
   return s;
 }
 
-NarrowModuli narrow_moduli(int r) {
+NarrowModuli narrow_moduli(int r, int pA) {
   NarrowModuli nm;
   std::memset(&nm, 0, sizeof(nm));
   nm.r = r;
@@ -104,6 +104,8 @@ NarrowModuli narrow_moduli(int r) {
     nm.c21[l] = pow_mod(2, 21, m);
     nm.c42[l] = pow_mod(2, 42, m);
     nm.off62[l] = pow_mod(2, 62, m);
+    nm.offA[l] = pow_mod(2, static_cast<uint64_t>(pA), m);
+    for (int c = 0; c < 4; ++c) nm.w16[l][c] = pow_mod(2, 16ull * c, m);
   }
   return nm;
 }
@@ -284,13 +286,15 @@ int narrow_residues(int m, int n, int k, const double* A, long long lda, const d
   c.lda = lda;
   c.B = B;
   c.ldb = ldb;
-  c.nm = narrow_moduli(r);
+  c.nm = narrow_moduli(r, pa_bits);
   c.ldr = round_up(n, 16);
   const size_t bres = align256(static_cast<size_t>(n) * r * c.kp);
+  const size_t cs = align256(static_cast<size_t>(n) * r * 4);
   uint8_t* ws = nullptr;
-  int s = workspace(d, bres, &ws);
+  int s = workspace(d, bres + cs, &ws);
   if (s != OZEMU_OK) return s;
   c.bres = ws;
+  c.colsum = reinterpret_cast<int32_t*>(ws + bres);
   c.res = res;
   c.sa = sa;
   c.sb = sb;
@@ -302,13 +306,14 @@ int narrow_residues(int m, int n, int k, const double* A, long long lda, const d
 int dgemm_narrow(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc, int r,
                  int pa_bits, int pb_bits, DeviceState* d, cudaStream_t st) {
   const size_t bres = align256(static_cast<size_t>(n) * r * round_up(k, 16));
+  const size_t cs = align256(static_cast<size_t>(n) * r * 4);
   const size_t rb = align256(ozemu_residue_bytes(m, n, r));
   const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
   uint8_t* ws = nullptr;
-  int s = workspace(d, bres + rb + sa + sb, &ws);
+  int s = workspace(d, bres + cs + rb + sa + sb, &ws);
   if (s != OZEMU_OK) return s;
   // narrow_residues takes the front of the same workspace for B's residues.
-  uint8_t* res = ws + bres;
+  uint8_t* res = ws + bres + cs;
   int32_t* sap = reinterpret_cast<int32_t*>(res + rb);
   int32_t* sbp = reinterpret_cast<int32_t*>(res + rb + sa);
   s = narrow_residues(m, n, k, A, lda, B, ldb, r, pa_bits, pb_bits, res, sap, sbp, d, st);

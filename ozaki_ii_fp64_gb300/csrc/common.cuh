@@ -41,6 +41,8 @@ struct NarrowModuli {
   uint32_t c21[kMaxModuli];    // 2^21 mod m
   uint32_t c42[kMaxModuli];    // 2^42 mod m
   uint32_t off62[kMaxModuli];  // 2^62 mod m
+  uint32_t offA[kMaxModuli];   // 2^(p_A) mod m
+  uint32_t w16[kMaxModuli][4]; // 2^(16 c) mod m
 };
 
 // Per-modulus constants for the GEMM epilogue.

@@ -61,6 +61,7 @@ struct NarrowCall {
   long long ldb;
   NarrowModuli nm;
   uint8_t* bres;    // [n][r][kp] residues of B's columns
+  int32_t* colsum;  // [n][r] sum_k b mod m
   uint8_t* res;     // [r][m][ldr]
   long long ldr;
   int32_t* sa;
