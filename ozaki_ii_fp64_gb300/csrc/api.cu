@@ -1,5 +1,6 @@
 // C ABI of libozemu.so: argument checks, per-call constants, the cached
 // per-device workspace and status flags, and the staging of the kernels.
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -147,6 +148,22 @@ CrtModuli crt_moduli(int r) {
     for (int w = 0; w < 4; ++w) c.prefix[l][w] = static_cast<uint32_t>(pref >> (32 * w));
     pref *= m;
   }
+  // Direct form.  pref is now M (< 2^126).
+  const u128 M = pref;
+  for (int l = 0; l < r; ++l) {
+    const uint32_t m = moduli().m[l];
+    const u128 Ml = M / m;
+    const u128 W = Ml * inv_mod(static_cast<uint32_t>(Ml % m), m);  // < M
+    for (int w = 0; w < 16; ++w) c.wb[l / 4][w] |= static_cast<uint32_t>((W >> (8 * w)) & 0xFF) << (8 * (l % 4));
+  }
+  for (int t = 0; t < 9; ++t) c.m16[t] = t < 8 ? static_cast<uint32_t>((M >> (16 * t)) & 0xFFFF) : 0u;
+  int bits = 0;
+  while (bits < 128 && (M >> bits) != 0) ++bits;
+  if (bits != kCrtBits[r]) c.r = 0;  // table mismatch: the launch refuses r = 0
+  const int ny = (bits + 12 + 15) / 16;
+  const long double Md = static_cast<long double>(M);
+  c.g_hi = static_cast<float>(std::ldexp(1.0L, 16 * (ny - 2)) / Md);
+  c.g_lo = static_cast<float>(std::ldexp(1.0L, 16 * (ny - 3)) / Md);
   return c;
 }
 

@@ -53,6 +53,10 @@ struct EpiModuli {
 };
 
 // Mixed-radix CRT constants.
+// Bit length of M = m_1 ... m_r for the moduli table (greedy pairwise-coprime
+// integers from 256 down), r = 0..16; the host checks it against the table.
+constexpr int kCrtBits[kMaxModuli + 1] = {0, 9, 16, 24, 32, 40, 48, 56, 64, 72, 80, 88, 95, 103, 111, 118, 126};
+
 struct CrtModuli {
   int r;
   uint32_t m[kMaxModuli];
@@ -60,6 +64,10 @@ struct CrtModuli {
   uint32_t inv[kMaxModuli];               // (m_0 ... m_{l-1})^-1 mod m_l
   uint32_t g[kMaxModuli][kMaxModuli];     // g[l][j] = (m_0...m_{j-1}) inv_l mod m_l, j < l
   uint32_t prefix[kMaxModuli][4];         // m_0 ... m_{l-1} as 128-bit little-endian words
+  // Direct form: C' = sum_l c_l W_l - q M with W_l = (M/m_l) ((M/m_l)^-1 mod m_l).
+  uint32_t wb[4][16];                     // byte w of W_{4q+i} at byte i of wb[q][w]
+  uint32_t m16[9];                        // M in 16-bit limbs
+  float g_hi, g_lo;                       // 2^(16 (NY-2)) / M, 2^(16 (NY-3)) / M
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -1,11 +1,12 @@
-// Per-output reconstruction: residues -> C' by mixed-radix (Garner) CRT ->
+// Per-output reconstruction: residues -> C' by the CRT in direct form
+// (integer dot products with the CRT basis and one quotient estimate) ->
 // one correct rounding of C' 2^-(s_i + t_j) to fp64.
 //
 // [TME4] abstract: the per-output reconstruction term of the TME model.
 // [AWE] abstract: the residue number system of Ozaki scheme II.
 //
-// The digit recurrence, Horner evaluation and rounding live in
-// crt_device.cuh.
+// The mixed-radix form (used where the direct form's quotient estimate is
+// ambiguous) and the rounding live in crt_device.cuh.
 #include <cstdint>
 
 #include "common.cuh"
@@ -18,11 +19,33 @@ namespace {
 
 constexpr int kCrtThreads = 128;
 
+__device__ __forceinline__ uint32_t dp4a_u8(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// One thread per 4 consecutive outputs of a row.  For each output the
+// residues c_l (bytes of four moduli per word) are dotted with the bytes of
+// the constants W_l = (M/m_l) ((M/m_l)^-1 mod m_l) by dp4a:
+//   S_w = sum_l c_l byte_w(W_l) < 2^20,   Y = sum_w S_w 2^(8w) = sum_l c_l W_l < 2^12 M,
+// Y is carried into 16-bit limbs, q = round(Y / M) is estimated in fp32
+// from Y's top 48 bits (error below 2^-10), and C' = Y - q M is formed
+// modulo 2^(16 NX) (|C'| < M/2 fits).  When Y/M lies within 2^-9 of a
+// half-integer the estimate may be off by one: that output takes the
+// mixed-radix digits instead (crt_round), which are exact for any input.
 template <int R>
 __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const uint8_t* __restrict__ res,
                                                           long long ldr, const int32_t* __restrict__ sa,
                                                           const int32_t* __restrict__ sb, double* __restrict__ C,
                                                           long long ldc, const CrtModuli cm) {
+  constexpr int NQ = (R + 3) / 4;             // words of four residues
+  constexpr int BM = kCrtBits[R];             // bit length of M
+  constexpr int NL = (BM + 7) / 8;            // bytes of W_l
+  constexpr int NT = (NL + 1) / 2;            // 16-bit positions the S_w pairs cover
+  constexpr int NY = (BM + 12 + 15) / 16;     // 16-bit limbs of Y
+  constexpr int NX = (BM + 15) / 16;          // 16-bit limbs of C' (two's complement)
+  static_assert(NX <= 8 && NY <= 9, "C' fits 128 bits");
   const long long groups_per_row = (n + 3) / 4;
   const long long total = static_cast<long long>(m) * groups_per_row;
   const long long plane = static_cast<long long>(m) * ldr;
@@ -30,19 +53,82 @@ __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const ui
        g += static_cast<long long>(gridDim.x) * kCrtThreads) {
     const int i = static_cast<int>(g / groups_per_row);
     const int j0 = static_cast<int>(g % groups_per_row) * 4;
-    uint32_t word[R];
+    uint32_t word[4 * NQ];
     const uint8_t* base = res + static_cast<long long>(i) * ldr + j0;
 #pragma unroll
-    for (int l = 0; l < R; ++l) word[l] = __ldcs(reinterpret_cast<const uint32_t*>(base + l * plane));
+    for (int l = 0; l < 4 * NQ; ++l)
+      word[l] = l < R ? __ldcs(reinterpret_cast<const uint32_t*>(base + l * plane)) : 0u;
+    // cw[e][q]: residues of moduli 4q .. 4q+3 of output j0 + e.
+    uint32_t cw[4][NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const uint32_t t0 = __byte_perm(word[4 * q], word[4 * q + 1], 0x5140);
+      const uint32_t t1 = __byte_perm(word[4 * q + 2], word[4 * q + 3], 0x5140);
+      const uint32_t t2 = __byte_perm(word[4 * q], word[4 * q + 1], 0x7362);
+      const uint32_t t3 = __byte_perm(word[4 * q + 2], word[4 * q + 3], 0x7362);
+      cw[0][q] = __byte_perm(t0, t1, 0x5410);
+      cw[1][q] = __byte_perm(t0, t1, 0x7632);
+      cw[2][q] = __byte_perm(t2, t3, 0x5410);
+      cw[3][q] = __byte_perm(t2, t3, 0x7632);
+    }
     const int si = sa[i];
-#pragma unroll 1
+#pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = j0 + e;
-      if (j >= n) break;
-      uint32_t c[R];
+      if (j >= n) continue;
+      // Y in 16-bit limbs.
+      uint32_t y[NY];
+      uint32_t carry = 0;
 #pragma unroll
-      for (int l = 0; l < R; ++l) c[l] = (word[l] >> (8 * e)) & 0xFFu;
-      const uint64_t bits = crt_round<R>(c, si + sb[j], cm);
+      for (int t = 0; t < NY; ++t) {
+        uint32_t v = carry;
+        if (t < NT) {
+          uint32_t s0 = 0, s1 = 0;
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            s0 = dp4a_u8(cw[e][q], cm.wb[q][2 * t], s0);
+            if (2 * t + 1 < NL) s1 = dp4a_u8(cw[e][q], cm.wb[q][2 * t + 1], s1);
+          }
+          v += s0 + (s1 << 8);
+        }
+        y[t] = v & 0xFFFFu;
+        carry = v >> 16;
+      }
+      // q = round(Y / M) from the top 48 bits.
+      const uint32_t hi32 = (y[NY - 1] << 16) | (NY >= 2 ? y[NY - 2] : 0u);
+      const uint32_t lo16 = NY >= 3 ? y[NY - 3] : 0u;
+      const float yf = fmaf(static_cast<float>(hi32), cm.g_hi, static_cast<float>(lo16) * cm.g_lo);
+      const float qf = rintf(yf);
+      const int S = si + sb[j];
+      uint64_t bits;
+      if (fabsf(yf - qf) < 0.5f - 1.0f / 512.0f) {
+        const int q = static_cast<int>(qf);
+        // C' = Y - q M modulo 2^(16 NX), two's complement.
+        uint32_t x[NX];
+        int cr = 0;
+#pragma unroll
+        for (int t = 0; t < NX; ++t) {
+          const int v = static_cast<int>(y[t]) - q * static_cast<int>(cm.m16[t]) + cr;
+          x[t] = static_cast<uint32_t>(v) & 0xFFFFu;
+          cr = v >> 16;
+        }
+        uint32_t wds[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t lo = 2 * w < NX ? x[2 * w] : 0u;
+          const uint32_t hi = 2 * w + 1 < NX ? x[2 * w + 1] : 0u;
+          wds[w] = lo | (hi << 16);
+        }
+        i128 X = (static_cast<i128>(wds[3]) << 96) | (static_cast<i128>(wds[2]) << 64) |
+                 (static_cast<i128>(wds[1]) << 32) | static_cast<i128>(wds[0]);
+        X = (X << (128 - 16 * NX)) >> (128 - 16 * NX);  // sign-extend from bit 16 NX - 1
+        bits = round_scaled(X, S);
+      } else {
+        uint32_t c[R];
+#pragma unroll
+        for (int l = 0; l < R; ++l) c[l] = (word[l] >> (8 * e)) & 0xFFu;
+        bits = crt_round<R>(c, S, cm);
+      }
       C[static_cast<long long>(i) * ldc + j] = __longlong_as_double(static_cast<long long>(bits));
     }
   }
@@ -70,6 +156,7 @@ int grid_for(long long work, int threads) {
 template <int R>
 cudaError_t launch_crt_r(int m, int n, const uint8_t* residues, long long ldr, const int32_t* sa, const int32_t* sb,
                          double* C, long long ldc, const CrtModuli& cm, cudaStream_t stream) {
+  if (cm.r != R) return cudaErrorInvalidValue;
   const long long work = static_cast<long long>(m) * ((n + 3) / 4);
   crt_kernel<R><<<grid_for(work, kCrtThreads), kCrtThreads, 0, stream>>>(m, n, residues, ldr, sa, sb, C, ldc, cm);
   return cudaGetLastError();
