@@ -124,7 +124,8 @@ EpiModuli epi_moduli(int r) {
     const uint32_t m = moduli().m[l];
     e.m[l] = static_cast<float>(m);
     e.inv_m[l] = 1.0f / static_cast<float>(m);
-    e.w169[l] = static_cast<float>(169u % m);
+    const int w = static_cast<int>(169u % m);
+    e.w169[l] = static_cast<float>(w > static_cast<int>(m / 2) ? w - static_cast<int>(m) : w);  // balanced
   }
   return e;
 }

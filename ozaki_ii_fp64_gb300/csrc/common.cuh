@@ -49,7 +49,7 @@ struct NarrowModuli {
 struct EpiModuli {
   float m[kMaxModuli];
   float inv_m[kMaxModuli];      // 1/m rounded to fp32
-  float w169[kMaxModuli];       // 169 mod m
+  float w169[kMaxModuli];       // 169 mod m, balanced: |w| <= m/2
 };
 
 // Mixed-radix CRT constants.
@@ -280,6 +280,18 @@ OZEMU_MMA_FP4_COLLECTOR(mma_fp4_lastuse, "lastuse")
 #undef OZEMU_MMA_FP4_COLLECTOR
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tcgen05.wait::ld that also takes the registers of the outstanding loads
+// as operands, so that no use of them is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+        "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]),
+        "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+        "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+      :
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x N columns of 32-bit words: register i holds column i of the

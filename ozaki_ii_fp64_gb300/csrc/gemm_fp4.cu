@@ -98,10 +98,17 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
   }
 }
 
+// x - m round(x / m) for an integer-valued |x| < 2^24: the quotient is
+// rounded by adding 1.5 2^23 (one fma and one add on the full-rate pipes;
+// a quotient off by one at a tie still leaves |result| <= m/2 + 1).
 __device__ __forceinline__ float fmod_small(float x, float m, float inv_m) {
-  float q = rintf(x * inv_m);
+  const float q = fmaf(x, inv_m, 12582912.0f) - 12582912.0f;
   return fmaf(-q, m, x);
 }
+
+// The residue byte of an integer-valued v in [0, 256), without a conversion
+// instruction: v + 2^23 holds v in its low mantissa bits.
+__device__ __forceinline__ uint32_t byte_of_float(float v) { return __float_as_uint(v + 8388608.0f); }
 
 // Tile t -> (modulus l, tile row tm, tile column tn): modulus-major, then
 // groups of kGroupM tile rows swept column by column (L2 reuse).
@@ -645,24 +652,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!warp_wait(tfull, g & 1, abort_word, args.flags)) break;
       tc_fence_after();
       uint32_t packed[CW / 4];
+      // Slice c + 1 is loaded from TMEM while slice c is folded.
+      uint32_t v1[kSlice], v2[kSlice], n1[kSlice], n2[kSlice];
+      tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0, n1);
+      tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0, n2);
 #pragma unroll
       for (int c = 0; c < CW; c += kSlice) {
-        uint32_t v1[kSlice], v2[kSlice];
-        tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0 + c, v1);
-        tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0 + c, v2);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(n1, n2);
+#pragma unroll
+        for (int i = 0; i < kSlice; ++i) {
+          v1[i] = n1[i];
+          v2[i] = n2[i];
+        }
+        if (c + kSlice < CW) {
+          tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0 + c + kSlice, n1);
+          tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0 + c + kSlice, n2);
+        }
 #pragma unroll
         for (int i = 0; i < kSlice; i += 4) {
-          uint32_t w = 0;
+          uint32_t b[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float r1 = fmod_small(__uint_as_float(v1[i + e]), fm, finv);
+            // |D1| <= 1728 * 8192 and |r2 w169| <= 129 * 128, so D1 + r2 w169 stays
+            // below 2^24 and exact.
             const float r2 = fmod_small(__uint_as_float(v2[i + e]), fm, finv);
-            float v = fmod_small(fmaf(r2, fw, r1), fm, finv);
+            float v = fmod_small(fmaf(r2, fw, __uint_as_float(v1[i + e])), fm, finv);
             v = v < 0.f ? v + fm : v;
-            w |= static_cast<uint32_t>(__float2int_rn(v)) << (8 * e);
+            b[e] = byte_of_float(v);
           }
-          packed[(c + i) / 4] = w;
+          packed[(c + i) / 4] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
         }
       }
       tc_fence_before();
