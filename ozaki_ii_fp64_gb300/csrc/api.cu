@@ -161,10 +161,8 @@ CrtModuli crt_moduli(int r) {
   int bits = 0;
   while (bits < 128 && (M >> bits) != 0) ++bits;
   if (bits != kCrtBits[r]) c.r = 0;  // table mismatch: the launch refuses r = 0
-  const int ny = (bits + 12 + 15) / 16;
   const long double Md = static_cast<long double>(M);
-  c.g_hi = static_cast<float>(std::ldexp(1.0L, 16 * (ny - 2)) / Md);
-  c.g_lo = static_cast<float>(std::ldexp(1.0L, 16 * (ny - 3)) / Md);
+  for (int t = 0; t < 9; ++t) c.gt[t] = static_cast<float>(std::ldexp(1.0L, 16 * t) / Md);
   return c;
 }
 

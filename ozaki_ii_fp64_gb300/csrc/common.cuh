@@ -67,7 +67,7 @@ struct CrtModuli {
   // Direct form: C' = sum_l c_l W_l - q M with W_l = (M/m_l) ((M/m_l)^-1 mod m_l).
   uint32_t wb[4][16];                     // byte w of W_{4q+i} at byte i of wb[q][w]
   uint32_t m16[9];                        // M in 16-bit limbs
-  float g_hi, g_lo;                       // 2^(16 (NY-2)) / M, 2^(16 (NY-3)) / M
+  float gt[9];                            // 2^(16 t) / M
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -27,25 +27,26 @@ __device__ __forceinline__ uint32_t dp4a_u8(uint32_t a, uint32_t b, uint32_t c) 
 
 // One thread per 4 consecutive outputs of a row.  For each output the
 // residues c_l (bytes of four moduli per word) are dotted with the bytes of
-// the constants W_l = (M/m_l) ((M/m_l)^-1 mod m_l) by dp4a:
-//   S_w = sum_l c_l byte_w(W_l) < 2^20,   Y = sum_w S_w 2^(8w) = sum_l c_l W_l < 2^12 M,
-// Y is carried into 16-bit limbs, q = round(Y / M) is estimated in fp32
-// from Y's top 48 bits (error below 2^-10), and C' = Y - q M is formed
-// modulo 2^(16 NX) (|C'| < M/2 fits).  When Y/M lies within 2^-9 of a
-// half-integer the estimate may be off by one: that output takes the
-// mixed-radix digits instead (crt_round), which are exact for any input.
+// the constants W_l = (M/m_l) ((M/m_l)^-1 mod m_l) by dp4a (a last single
+// modulus by 32-bit multiply-adds on 16-bit limbs):
+//   T_t = sum_l c_l limb16_t(W_l) < 2^29,   Y = sum_t T_t 2^(16 t) = sum_l c_l W_l < 2^12 M,
+// q = round(Y / M) is estimated in fp32 from the three top T_t (error below
+// 2^-9.5), and C' = Y - q M is carried once into 16-bit limbs modulo
+// 2^(16 NX) (|C'| < M/2 fits).  When Y/M lies within 2^-8 of a half-integer
+// the estimate may be off by one: that output takes the mixed-radix digits
+// instead (crt_round), which are exact for any input.
 template <int R>
 __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const uint8_t* __restrict__ res,
                                                           long long ldr, const int32_t* __restrict__ sa,
                                                           const int32_t* __restrict__ sb, double* __restrict__ C,
                                                           long long ldc, const CrtModuli cm) {
-  constexpr int NQ = (R + 3) / 4;             // words of four residues
+  constexpr bool kLastByMad = (R % 4) == 1;   // a lone last modulus: multiply-adds, not dp4a
+  constexpr int NQ = kLastByMad ? R / 4 : (R + 3) / 4;  // words of four residues through dp4a
   constexpr int BM = kCrtBits[R];             // bit length of M
   constexpr int NL = (BM + 7) / 8;            // bytes of W_l
-  constexpr int NT = (NL + 1) / 2;            // 16-bit positions the S_w pairs cover
-  constexpr int NY = (BM + 12 + 15) / 16;     // 16-bit limbs of Y
+  constexpr int NT = (NL + 1) / 2;            // 16-bit positions of Y's partial sums
   constexpr int NX = (BM + 15) / 16;          // 16-bit limbs of C' (two's complement)
-  static_assert(NX <= 8 && NY <= 9, "C' fits 128 bits");
+  static_assert(NX <= 8 && NX <= NT, "C' fits 128 bits");
   const long long groups_per_row = (n + 3) / 4;
   const long long total = static_cast<long long>(m) * groups_per_row;
   const long long plane = static_cast<long long>(m) * ldr;
@@ -53,13 +54,14 @@ __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const ui
        g += static_cast<long long>(gridDim.x) * kCrtThreads) {
     const int i = static_cast<int>(g / groups_per_row);
     const int j0 = static_cast<int>(g % groups_per_row) * 4;
-    uint32_t word[4 * NQ];
+    constexpr int NW = 4 * ((R + 3) / 4);
+    uint32_t word[NW];
     const uint8_t* base = res + static_cast<long long>(i) * ldr + j0;
 #pragma unroll
-    for (int l = 0; l < 4 * NQ; ++l)
+    for (int l = 0; l < NW; ++l)
       word[l] = l < R ? __ldcs(reinterpret_cast<const uint32_t*>(base + l * plane)) : 0u;
     // cw[e][q]: residues of moduli 4q .. 4q+3 of output j0 + e.
-    uint32_t cw[4][NQ];
+    uint32_t cw[4][NQ > 0 ? NQ : 1];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       const uint32_t t0 = __byte_perm(word[4 * q], word[4 * q + 1], 0x5140);
@@ -76,39 +78,37 @@ __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const ui
     for (int e = 0; e < 4; ++e) {
       const int j = j0 + e;
       if (j >= n) continue;
-      // Y in 16-bit limbs.
-      uint32_t y[NY];
-      uint32_t carry = 0;
+      uint32_t T[NT];
 #pragma unroll
-      for (int t = 0; t < NY; ++t) {
-        uint32_t v = carry;
-        if (t < NT) {
-          uint32_t s0 = 0, s1 = 0;
+      for (int t = 0; t < NT; ++t) {
+        uint32_t s0 = 0, s1 = 0;
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) {
-            s0 = dp4a_u8(cw[e][q], cm.wb[q][2 * t], s0);
-            if (2 * t + 1 < NL) s1 = dp4a_u8(cw[e][q], cm.wb[q][2 * t + 1], s1);
-          }
-          v += s0 + (s1 << 8);
+        for (int q = 0; q < NQ; ++q) {
+          s0 = dp4a_u8(cw[e][q], cm.wb[q][2 * t], s0);
+          if (2 * t + 1 < NL) s1 = dp4a_u8(cw[e][q], cm.wb[q][2 * t + 1], s1);
         }
-        y[t] = v & 0xFFFFu;
-        carry = v >> 16;
+        T[t] = s0 + (s1 << 8);
+        if (kLastByMad) {
+          const uint32_t c_last = (word[R - 1] >> (8 * e)) & 0xFFu;
+          const uint32_t wl = (cm.wb[R / 4][2 * t] & 0xFFu) | ((2 * t + 1 < NL ? cm.wb[R / 4][2 * t + 1] & 0xFFu : 0u) << 8);
+          T[t] += c_last * wl;
+        }
       }
-      // q = round(Y / M) from the top 48 bits.
-      const uint32_t hi32 = (y[NY - 1] << 16) | (NY >= 2 ? y[NY - 2] : 0u);
-      const uint32_t lo16 = NY >= 3 ? y[NY - 3] : 0u;
-      const float yf = fmaf(static_cast<float>(hi32), cm.g_hi, static_cast<float>(lo16) * cm.g_lo);
+      // q = round(Y / M) from the three top partial sums.
+      float yf = 0.f;
+#pragma unroll
+      for (int t = NT - 3 < 0 ? 0 : NT - 3; t < NT; ++t) yf = fmaf(static_cast<float>(T[t]), cm.gt[t], yf);
       const float qf = rintf(yf);
       const int S = si + sb[j];
       uint64_t bits;
-      if (fabsf(yf - qf) < 0.5f - 1.0f / 512.0f) {
+      if (fabsf(yf - qf) < 0.5f - 1.0f / 256.0f) {
         const int q = static_cast<int>(qf);
-        // C' = Y - q M modulo 2^(16 NX), two's complement.
+        // C' = Y - q M modulo 2^(16 NX), two's complement 16-bit limbs.
         uint32_t x[NX];
         int cr = 0;
 #pragma unroll
         for (int t = 0; t < NX; ++t) {
-          const int v = static_cast<int>(y[t]) - q * static_cast<int>(cm.m16[t]) + cr;
+          const int v = static_cast<int>(T[t]) - q * static_cast<int>(cm.m16[t]) + cr;
           x[t] = static_cast<uint32_t>(v) & 0xFFFFu;
           cr = v >> 16;
         }
@@ -117,12 +117,12 @@ __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const ui
         for (int w = 0; w < 4; ++w) {
           const uint32_t lo = 2 * w < NX ? x[2 * w] : 0u;
           const uint32_t hi = 2 * w + 1 < NX ? x[2 * w + 1] : 0u;
-          wds[w] = lo | (hi << 16);
+          wds[w] = __byte_perm(lo, hi, 0x5410);
         }
         i128 X = (static_cast<i128>(wds[3]) << 96) | (static_cast<i128>(wds[2]) << 64) |
                  (static_cast<i128>(wds[1]) << 32) | static_cast<i128>(wds[0]);
         X = (X << (128 - 16 * NX)) >> (128 - 16 * NX);  // sign-extend from bit 16 NX - 1
-        bits = round_scaled(X, S);
+        bits = round_scaled_fast(X, S);
       } else {
         uint32_t c[R];
 #pragma unroll

@@ -64,6 +64,43 @@ __device__ inline uint64_t round_scaled(i128 X, int S) {
   return neg ? (bits | 0x8000000000000000ull) : bits;
 }
 
+// round_scaled for the common case, on the words of X: a normal (or
+// overflowing) result takes the top 64 bits of |X| and a sticky bit; a
+// result in the subnormal range goes through round_scaled.
+__device__ __forceinline__ uint64_t round_scaled_fast(i128 X, int S) {
+  if (X == 0) return 0ull;
+  const bool neg = X < 0;
+  const u128 mag = neg ? static_cast<u128>(-X) : static_cast<u128>(X);
+  const uint64_t hi = static_cast<uint64_t>(mag >> 64), lo = static_cast<uint64_t>(mag);
+  uint64_t M;
+  bool sticky;
+  int e;  // index of the leading bit of |X|
+  if (hi != 0) {
+    const int lz = __clzll(static_cast<long long>(hi));
+    M = lz ? (hi << lz) | (lo >> (64 - lz)) : hi;
+    sticky = lz ? (lo << lz) != 0 : lo != 0;
+    e = 127 - lz;
+  } else {
+    const int lz = __clzll(static_cast<long long>(lo));
+    M = lo << lz;
+    sticky = false;
+    e = 63 - lz;
+  }
+  int b = e - S;  // exponent of the result's leading bit
+  if (b < -1022) return round_scaled(X, S);
+  uint64_t q = M >> 11;
+  const uint64_t rb = (M >> 10) & 1ull;
+  const bool st = sticky || (M & 0x3FFull) != 0;
+  q += rb & static_cast<uint64_t>(st | (q & 1ull));
+  if (q >> 53) {
+    q >>= 1;
+    ++b;
+  }
+  const uint64_t bits =
+      b > 1023 ? 0x7FF0000000000000ull : (static_cast<uint64_t>(b + 1023) << 52) | (q & 0xFFFFFFFFFFFFFull);
+  return neg ? (bits | 0x8000000000000000ull) : bits;
+}
+
 // Number of 32-bit words that hold +-M/2 for the first R moduli (M < 2^(8R),
 // and M < 2^126 for every R <= 16, so four words always suffice).
 template <int R>
