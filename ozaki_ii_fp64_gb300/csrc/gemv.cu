@@ -83,23 +83,6 @@ __global__ void __launch_bounds__(kNarrowColThreads) narrow_cols_kernel(const do
   }
 }
 
-// A' + 2^p for the fp64 pattern `bits` of an element of a row whose largest
-// magnitude is a normal number, with p <= 52: |x 2^s| is then a right shift
-// of the 53-bit significand by d = (1075 - s) - max(E, 1) >= 1, rounded half
-// to even.  Non-finite elements give an unspecified value (they set the
-// non-finite flag elsewhere).
-__device__ __forceinline__ uint64_t offset_integer_fast(uint64_t bits, int d0, uint64_t off) {
-  const uint32_t hi = static_cast<uint32_t>(bits >> 32), lo = static_cast<uint32_t>(bits);
-  const uint32_t E = (hi >> 20) & 0x7FFu;
-  const uint32_t mhi = (hi & 0xFFFFFu) | (E ? 0x100000u : 0u);
-  int d = d0 - static_cast<int>(E > 1u ? E : 1u);
-  d = d < 1 ? 1 : (d > 63 ? 63 : d);
-  const uint64_t M = (static_cast<uint64_t>(mhi) << 32) | lo;
-  const uint64_t q = (M + ((1ull << (d - 1)) - 1ull) + ((M >> d) & 1ull)) >> d;
-  const uint64_t neg = static_cast<uint64_t>(static_cast<long long>(static_cast<int>(hi) >> 31));  // 0 or ~0
-  return off + ((q ^ neg) - neg);
-}
-
 __device__ __forceinline__ uint32_t dp2a_lo(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("dp2a.lo.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));

@@ -73,6 +73,53 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
   w2 = __byte_perm(ulo, uhi, 0x5410);
 }
 
+// Pass 2 of the row split over the row's elements: integers, residues and
+// limb codes (or residue bytes), packed and stored.
+template <int R, bool kRes8, bool kFast>
+__device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, bool vec_ok, int s,
+                                            const SplitModuli& mods, const uint32_t* lut, uint8_t* out_row,
+                                            long long plane_stride) {
+  for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
+    uint64_t b[8];
+    load8_f64(rowp, k, k0, vec_ok, b, true);
+    uint32_t a2[8], a1[8], a0x4[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint64_t u = kFast ? offset_integer_fast(b[e], 1075 - s, 1ull << 62) : scaled_offset(b[e], s);
+      a0x4[e] = (static_cast<uint32_t>(u) & 0x1FFFFFu) << 2;
+      a1[e] = static_cast<uint32_t>(u >> 21) & 0x1FFFFFu;
+      a2[e] = static_cast<uint32_t>(u >> 42);
+    }
+    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : k0 / 2));
+#pragma unroll
+    for (int l = 0; l < R; ++l) {
+      const uint32_t c21 = mods.c21x4[l], c42 = mods.c42x4[l], mg = mods.magic4[l], m4 = mods.m[l] * 4u;
+      const char* lt = reinterpret_cast<const char*>(lut + l * kLutStride);
+      uint32_t c[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        uint32_t v4 = a2[e] * c42 + (a1[e] * c21 + a0x4[e]);
+        uint32_t q = __umulhi(v4, mg);
+        uint32_t off = v4 - q * m4;
+        c[e] = *reinterpret_cast<const uint32_t*>(lt + off);
+      }
+      if constexpr (kRes8) {
+        uint2 w;
+        w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+        w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+        __stcs(reinterpret_cast<uint2*>(o + static_cast<long long>(l) * plane_stride / 4), w);
+      } else {
+        uint32_t w0, w1, w2;
+        pack8(c, w0, w1, w2);
+        const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
+        __stcs(o + pl, w0);
+        __stcs(o + pl + plane_stride / 4, w1);
+        __stcs(o + pl + 2 * plane_stride / 4, w2);
+      }
+    }
+  }
+}
+
 // kRes8 = false: FP4 limb planes [r][3][rows_p][k_p/2] (the FP4 path).
 // kRes8 = true: the balanced residues themselves as int8 [r][rows_p][k_p]
 // (input of the INT8 comparison GEMM).
@@ -128,46 +175,12 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
     if (mx >= 0x7FF0000000000000ull && threadIdx.x == 0) atomicOr(flags, kFlagNonFinite);
     if (threadIdx.x == 0) shifts[row] = s;
 
-    // Pass 2: integers, residues, limbs.
-    for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
-      uint64_t b[8];
-      load8_f64(rowp, k, k0, vec_ok, b, true);
-      uint32_t a2[8], a1[8], a0x4[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        uint64_t u = scaled_offset(b[e], s);
-        a0x4[e] = (static_cast<uint32_t>(u) & 0x1FFFFFu) << 2;
-        a1[e] = static_cast<uint32_t>(u >> 21) & 0x1FFFFFu;
-        a2[e] = static_cast<uint32_t>(u >> 42);
-      }
-      uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : k0 / 2));
-#pragma unroll
-      for (int l = 0; l < R; ++l) {
-        const uint32_t c21 = mods.c21x4[l], c42 = mods.c42x4[l], mg = mods.magic4[l], m4 = mods.m[l] * 4u;
-        const char* lt = reinterpret_cast<const char*>(lut + l * kLutStride);
-        uint32_t c[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          uint32_t v4 = a2[e] * c42 + (a1[e] * c21 + a0x4[e]);
-          uint32_t q = __umulhi(v4, mg);
-          uint32_t off = v4 - q * m4;
-          c[e] = *reinterpret_cast<const uint32_t*>(lt + off);
-        }
-        if constexpr (kRes8) {
-          uint2 w;
-          w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-          w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-          __stcs(reinterpret_cast<uint2*>(o + static_cast<long long>(l) * plane_stride / 4), w);
-        } else {
-          uint32_t w0, w1, w2;
-          pack8(c, w0, w1, w2);
-          const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
-          __stcs(o + pl, w0);
-          __stcs(o + pl + plane_stride / 4, w1);
-          __stcs(o + pl + 2 * plane_stride / 4, w2);
-        }
-      }
-    }
+    // Pass 2: integers, residues, limbs.  Rows whose largest magnitude is
+    // normal (with p <= 52) take the right-shift rounding.
+    if ((mx >> 52) != 0 && p <= 52)
+      split_pass2<R, kRes8, true>(rowp, k, k_p, vec_ok, s, mods, lut, out_row, plane_stride);
+    else
+      split_pass2<R, kRes8, false>(rowp, k, k_p, vec_ok, s, mods, lut, out_row, plane_stride);
   }
 }
 
