@@ -207,7 +207,7 @@ def kernel_traffic(workload):
 
 def gemm_kernel_name(n, k):
     """The limb-GEMM kernel the library picks for a residue product."""
-    pair = n > 64 and (k + 127) // 128 <= 64 and os.environ.get("OZEMU_GEMM_PAIR", "1") != "0"
+    pair = n > 64 and os.environ.get("OZEMU_GEMM_PAIR", "1") != "0"
     if pair:
         return "limb_gemm_pair_kernel (CTA pair, 256x224 tiles)"
     bn = 16 if n <= 16 else 32 if n <= 32 else 64 if n <= 64 else 128

@@ -436,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 1.75x the work of a 128 x 128 one per A-tile read and per stage barrier:
 // the 128 x 128 single-CTA MMA reads shared memory at about the full port
 // rate, which leaves no room for the TMA fills and barrier reads.
-// Used for residue products with n > 64 and a single exact K chunk.
+// Used for residue products with n > 64; for K beyond one exact chunk each
+// chunk is an accumulation round whose residues the epilogue adds, modulo
+// m_l, to the ones it keeps in registers (four per register).
 // ---------------------------------------------------------------------------
 constexpr int kBN2 = 224;                        // pair tile N
 constexpr int kBHalf = kBN2 / 2;                 // B rows per CTA
@@ -451,6 +453,7 @@ constexpr int kGroupM2 = 16;                     // pair-tile rows per raster gr
 
 struct PairArgs {
   int m, n, kb_total;
+  int kc_blocks;  // 128-wide K blocks per exactly accumulated chunk
   int rows_a_p, rows_b_p;
   int tiles_m2, tiles_n2, total_tiles;
   EpiModuli em;
@@ -583,48 +586,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int it = 0, g = 0;
       bool ok = true;
       bool known_full = false;
-      for (int t = pair; t < args.total_tiles && ok; t += npairs, ++g) {
-        if (g > 0) {
-          if (!mbar_wait(tempty, (g - 1) & 1, abort_word, args.flags)) {
-            ok = false;
-            break;
+      // g counts accumulation rounds: one per K chunk of each tile.
+      for (int t = pair; t < args.total_tiles && ok; t += npairs) {
+        for (int kc0 = 0; kc0 < kb_total && ok; kc0 += args.kc_blocks, ++g) {
+          if (g > 0) {
+            if (!mbar_wait(tempty, (g - 1) & 1, abort_word, args.flags)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
-        }
-        for (int kb = 0; kb < kb_total; ++kb, ++it) {
-          const int s = it % kStages2;
-          const uint32_t ph = (it / kStages2) & 1;
-          if (!known_full && !mbar_wait(&full[s], ph, abort_word, args.flags)) {
-            ok = false;
-            break;
-          }
-          known_full = false;
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * kStage2);
+          const int kc1 = kc0 + args.kc_blocks < kb_total ? kc0 + args.kc_blocks : kb_total;
+          for (int kb = kc0; kb < kc1; ++kb, ++it) {
+            const int s = it % kStages2;
+            const uint32_t ph = (it / kStages2) & 1;
+            if (!known_full && !mbar_wait(&full[s], ph, abort_word, args.flags)) {
+              ok = false;
+              break;
+            }
+            known_full = false;
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + s * kStage2);
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
-            const uint64_t a1 = smem_desc_sw64(st + 1 * kATile + ks * 32);
-            const uint64_t a2 = smem_desc_sw64(st + 2 * kATile + ks * 32);
-            const uint64_t b0 = smem_desc_sw64(st + 3 * kATile + 0 * kBTile2 + ks * 32);
-            const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * kBTile2 + ks * 32);
-            const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * kBTile2 + ks * 32);
-            const uint32_t acc = (kb == 0 && ks == 0) ? 0u : 1u;
-            mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
-            mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
-            mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
-            mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
-            mma_fp4_pair_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
-            mma_fp4_pair_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
-            mma_fp4_pair_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
-            mma_fp4_pair_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
-            mma_fp4_pair(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
-            if (ks == 0)
-              known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
+            for (int ks = 0; ks < 2; ++ks) {
+              const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
+              const uint64_t a1 = smem_desc_sw64(st + 1 * kATile + ks * 32);
+              const uint64_t a2 = smem_desc_sw64(st + 2 * kATile + ks * 32);
+              const uint64_t b0 = smem_desc_sw64(st + 3 * kATile + 0 * kBTile2 + ks * 32);
+              const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * kBTile2 + ks * 32);
+              const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * kBTile2 + ks * 32);
+              const uint32_t acc = (kb == kc0 && ks == 0) ? 0u : 1u;
+              mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+              mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
+              mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
+              mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+              mma_fp4_pair_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
+              mma_fp4_pair_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
+              mma_fp4_pair_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
+              mma_fp4_pair_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
+              mma_fp4_pair(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+              if (ks == 0)
+                known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
+            }
+            tc_commit_pair_multicast(&empty[s], 0x3);
           }
-          tc_commit_pair_multicast(&empty[s], 0x3);
+          if (ok) tc_commit_pair_multicast(tfull, 0x3);
         }
-        if (ok) tc_commit_pair_multicast(tfull, 0x3);
       }
       tc_commit_pair_multicast(mma_done, 0x1);
       drain_wait(mma_done, 0, args.flags);
@@ -643,50 +650,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = static_cast<uint32_t>(half * CW);
     const uint32_t tempty_leader = mapa_shared(tempty, 0);
-    int g = 0;
-    for (int t = pair; t < args.total_tiles; t += npairs, ++g) {
+    int g = 0;  // accumulation rounds, as counted by the MMA issuer
+    bool live = true;
+    for (int t = pair; t < args.total_tiles && live; t += npairs) {
       int l, tm2, tn;
       pair_tile_coords(t, args, l, tm2, tn);
       const int grow = tm2 * 256 + static_cast<int>(rank) * kBM + quarter * 32 + lane;
       const float fm = args.em.m[l], finv = args.em.inv_m[l], fw = args.em.w169[l];
-      if (!warp_wait(tfull, g & 1, abort_word, args.flags)) break;
-      tc_fence_after();
+      // Residues of this thread's 112 outputs, four to a register; chunks
+      // after the first are added to them modulo m.
       uint32_t packed[CW / 4];
-      // Slice c + 1 is loaded from TMEM while slice c is folded.
-      uint32_t v1[kSlice], v2[kSlice], n1[kSlice], n2[kSlice];
-      tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0, n1);
-      tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0, n2);
-#pragma unroll
-      for (int c = 0; c < CW; c += kSlice) {
-        tmem_wait_ld_regs(n1, n2);
-#pragma unroll
-        for (int i = 0; i < kSlice; ++i) {
-          v1[i] = n1[i];
-          v2[i] = n2[i];
+      for (int kc0 = 0; kc0 < kb_total; kc0 += args.kc_blocks, ++g) {
+        const bool first = (kc0 == 0);
+        if (!warp_wait(tfull, g & 1, abort_word, args.flags)) {
+          live = false;
+          break;
         }
-        if (c + kSlice < CW) {
-          tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0 + c + kSlice, n1);
-          tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0 + c + kSlice, n2);
-        }
+        tc_fence_after();
+        // Slice c + 1 is loaded from TMEM while slice c is folded.
+        uint32_t v1[kSlice], v2[kSlice], n1[kSlice], n2[kSlice];
+        tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0, n1);
+        tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0, n2);
 #pragma unroll
-        for (int i = 0; i < kSlice; i += 4) {
-          uint32_t b[4];
+        for (int c = 0; c < CW; c += kSlice) {
+          tmem_wait_ld_regs(n1, n2);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // |D1| <= 1728 * 8192 and |r2 w169| <= 129 * 128, so D1 + r2 w169 stays
-            // below 2^24 and exact.
-            const float r2 = fmod_small(__uint_as_float(v2[i + e]), fm, finv);
-            float v = fmod_small(fmaf(r2, fw, __uint_as_float(v1[i + e])), fm, finv);
-            v = v < 0.f ? v + fm : v;
-            b[e] = byte_of_float(v);
+          for (int i = 0; i < kSlice; ++i) {
+            v1[i] = n1[i];
+            v2[i] = n2[i];
           }
-          packed[(c + i) / 4] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+          if (c + kSlice < CW) {
+            tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0 + c + kSlice, n1);
+            tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0 + c + kSlice, n2);
+          }
+#pragma unroll
+          for (int i = 0; i < kSlice; i += 4) {
+            uint32_t b[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // |D1| <= 1728 * 8192 and |r2 w169| <= 129 * 128, so D1 + r2 w169 stays
+              // below 2^24 and exact.
+              const float r2 = fmod_small(__uint_as_float(v2[i + e]), fm, finv);
+              float v = fmod_small(fmaf(r2, fw, __uint_as_float(v1[i + e])), fm, finv);
+              v = v < 0.f ? v + fm : v;
+              if (!first) {  // + the residue of the earlier chunks, modulo m
+                v += __uint_as_float(__byte_perm(packed[(c + i) / 4], 0x4B000000u, 0x7650u | (e & 3))) - 8388608.0f;
+                v = v >= fm ? v - fm : v;
+              }
+              b[e] = byte_of_float(v);
+            }
+            packed[(c + i) / 4] =
+                __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader);
-      if (grow >= args.m) continue;
+      if (!live || grow >= args.m) continue;
       uint8_t* rrow = args.res_out + (static_cast<long long>(l) * args.m + grow) * args.ldr;
       const int gcol0 = tn * kBN2 + static_cast<int>(col0);
 #pragma unroll
@@ -784,6 +805,7 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   a.m = c.m;
   a.n = c.n;
   a.kb_total = k_p / 128;
+  a.kc_blocks = c.kc_blocks;
   a.rows_a_p = rows_a_p;
   a.rows_b_p = rows_b_p;
   a.tiles_m2 = (c.m + 255) / 256;
@@ -829,8 +851,7 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
 }
 
 bool use_pair(const LimbGemmCall& c) {
-  if (!c.residue_mode || c.n <= 64) return false;
-  if (round_up(c.k, kKAlign) / 128 > c.kc_blocks) return false;  // one exact K chunk only
+  if (!c.residue_mode || c.n <= 64 || c.kc_blocks < 1) return false;
   if (const char* s = std::getenv("OZEMU_GEMM_PAIR")) return s[0] != '0';
   return true;
 }

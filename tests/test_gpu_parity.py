@@ -260,10 +260,12 @@ def test_residue_gemm_i8_matches_oracle_and_fp4_path(oz, m, n, k, r, dist):
     assert (C.cpu().numpy().view(np.int64) == Cref.view(np.int64)).all()
 
 
-@pytest.mark.parametrize("m,n,k,r", [(200, 150, 300, 13), (513, 257, 4000, 12), (256, 65, 8192, 13)])
+@pytest.mark.parametrize("m,n,k,r", [(200, 150, 300, 13), (513, 257, 4000, 12), (256, 65, 8192, 13),
+                                     (300, 230, 8193, 13), (130, 250, 20000, 12), (257, 449, 16384, 11)])
 def test_pair_and_single_cta_gemm_agree(oz, m, n, k, r, monkeypatch):
-    # The CTA-pair kernel (256 x 112 tiles) and the single-CTA kernel (128 x
-    # 128 tiles) must produce identical residues, equal to the oracle's.
+    # The CTA-pair kernel (256 x 224 tiles) and the single-CTA kernel (128 x
+    # 128 tiles) must produce identical residues, equal to the oracle's; for
+    # k > 8192 both accumulate exact chunks of 8192 and add their residues.
     A, B = make_pair(m, n, k, seed=m + n + 7 * k, dist="wide")
     pA, pB = oz.ozemu_bit_budget(k, r)
     ap, _ = oz.split_rows_f64(to_dev(A), pA, r)
