@@ -99,6 +99,22 @@ int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B,
 int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
                 int ldb, double* C, int ldc, int r, cudaStream_t stream);
 
+/* ozemu_dgemm with HOST buffers: A (m x k, lda), B (k x n, ldb) and C
+ * (m x n, ldc) are row-major host pointers; the result is the same as
+ * ozemu_dgemm's, bit for bit.  The copies in and out are pipelined with the
+ * work: B and row chunks of A are copied on a copy stream while earlier
+ * chunks are deconstructed and multiplied on `stream`, each chunk's CRT runs
+ * on a second stream beside the next chunk's GEMM, and each finished chunk of
+ * C is copied out at once.  Page-locked (pinned) host buffers are needed for
+ * the copies to overlap; pageable ones give the same result, serialised.
+ * All work is ordered after what `stream` already holds, and `stream`
+ * completes only after C is on the host: synchronise `stream` (or call
+ * ozemu_get_status on it) before reading C.  The source pages have no
+ * counterpart; this is the end-to-end entry point.  Errors as ozemu_dgemm.
+ * Uses the cached workspace (it also holds device copies of A, B and C). */
+int ozemu_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B,
+                     int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Host-side queries (no device work)                                       */
 /* ------------------------------------------------------------------------ */

@@ -65,6 +65,7 @@ _SIGNATURES = {
     "ozemu_split_cols_f64_res8": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
     "ozemu_residue_gemm_i8": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
     "ozemu_narrow_max_n": (_I, []),
+    "ozemu_dgemm_host": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
     "ozemu_residues_narrow_f64": (_I, [_I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P]),
 }
 
@@ -173,6 +174,10 @@ def ozemu_residue_gemm_i8(m, n, k, r, a_res8, b_res8, residues, stream):
     return _call("ozemu_residue_gemm_i8", m, n, k, r, a_res8, b_res8, residues, stream)
 
 
+def ozemu_dgemm_host(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
+    return _call("ozemu_dgemm_host", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
+
+
 def ozemu_narrow_max_n():
     return _call("ozemu_narrow_max_n")
 
@@ -241,6 +246,22 @@ def dgemm(A, B, r, out=None, stream=None):
     C = torch.empty((m, n), dtype=torch.float64, device=A.device) if out is None else out
     _check(ozemu_dgemm(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
                        _stream(stream)), "ozemu_dgemm")
+    return C
+
+
+def dgemm_host(A, B, r, out=None, stream=None):
+    """Emulated fp64 A @ B of CPU float64 tensors (pinned for overlap) through
+    ozemu_dgemm_host; returns the CPU result after synchronising the stream."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2 or A.device.type != "cpu" or B.device.type != "cpu":
+        raise ValueError("expected CPU matrices with matching inner dimension")
+    C = torch.empty((m, n), dtype=torch.float64, pin_memory=A.is_pinned()) if out is None else out
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(ozemu_dgemm_host(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
+                            s.cuda_stream), "ozemu_dgemm_host")
+    s.synchronize()
     return C
 
 

@@ -167,12 +167,17 @@ CrtModuli crt_moduli(int r) {
 }
 
 // ----------------------------------------------------------- device state
+constexpr int kHostEvents = 32;
 struct DeviceState {
   bool checked = false;
   bool supported = false;
   uint32_t* flags = nullptr;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  // Host-buffer product: a copy stream, a CRT stream and their events.
+  cudaStream_t copy_stream = nullptr;
+  cudaStream_t crt_stream = nullptr;
+  cudaEvent_t ev[kHostEvents] = {};
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -335,6 +340,17 @@ int dgemm_narrow(int m, int n, int k, const double* A, int lda, const double* B,
   s = narrow_residues(m, n, k, A, lda, B, ldb, r, pa_bits, pb_bits, res, sap, sbp, d, st);
   if (s != OZEMU_OK) return s;
   return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), st));
+}
+
+// Streams and events of the host-buffer product, created on first use.
+int pipeline_state(DeviceState* d) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (d->copy_stream) return OZEMU_OK;
+  if (cudaStreamCreateWithFlags(&d->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (cudaStreamCreateWithFlags(&d->crt_stream, cudaStreamNonBlocking) != cudaSuccess) return OZEMU_ERR_CUDA;
+  for (int i = 0; i < kHostEvents; ++i)
+    if (cudaEventCreateWithFlags(&d->ev[i], cudaEventDisableTiming) != cudaSuccess) return OZEMU_ERR_CUDA;
+  return OZEMU_OK;
 }
 
 int limb_gemm_s32(int m, int n, int k, const uint8_t* ap, const uint8_t* bp, int32_t* C, long long ldc,
@@ -649,6 +665,146 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   s = residue_gemm(m, n, k, r, ap, bp, res, d, stream);
   if (s != OZEMU_OK) return s;
   return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), stream));
+}
+
+int ozemu_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                     int r, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (k > 0 && ozemu_bit_budget(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  s = pipeline_state(d);
+  if (s != OZEMU_OK) return s;
+  const size_t szA = align256(static_cast<size_t>(m) * (k > 0 ? k : 1) * 8);
+  const size_t szB = align256(static_cast<size_t>(k > 0 ? k : 1) * n * 8);
+  const size_t szC = align256(static_cast<size_t>(m) * n * 8);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  const bool narrow = k == 0 || (n <= kNarrowMaxN && k <= kNarrowMaxK && pa_bits <= kNarrowMaxP && narrow_enabled());
+  if (narrow) {
+    // Small work: copy in, the device product, copy out, all on the caller's stream.
+    uint8_t* buf = nullptr;
+    s = workspace(d, szA + szB + szC + align256(static_cast<size_t>(n) * r * round_up(k > 0 ? k : 1, 16)) +
+                         align256(static_cast<size_t>(n) * r * 4) + align256(ozemu_residue_bytes(m, n, r)) +
+                         align256(static_cast<size_t>(m) * 4) + align256(static_cast<size_t>(n) * 4), &buf);
+    if (s != OZEMU_OK) return s;
+    double* Ad = reinterpret_cast<double*>(buf);
+    double* Bd = reinterpret_cast<double*>(buf + szA);
+    double* Cd = reinterpret_cast<double*>(buf + szA + szB);
+    if (k == 0) {
+      if (launch_zero_f64(Cd, m, n, n, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+    } else {
+      if (cudaMemcpy2DAsync(Ad, k * 8, A, static_cast<size_t>(lda) * 8, static_cast<size_t>(k) * 8, m, h2d, stream) !=
+              cudaSuccess ||
+          cudaMemcpy2DAsync(Bd, n * 8, B, static_cast<size_t>(ldb) * 8, static_cast<size_t>(n) * 8, k, h2d, stream) !=
+              cudaSuccess)
+        return OZEMU_ERR_CUDA;
+      // The narrow path's own buffers follow the copies in the same workspace.
+      uint8_t* rest = buf + szA + szB + szC;
+      const size_t bres = align256(static_cast<size_t>(n) * r * round_up(k, 16));
+      const size_t cs = align256(static_cast<size_t>(n) * r * 4);
+      const size_t rb = align256(ozemu_residue_bytes(m, n, r));
+      uint8_t* res = rest + bres + cs;
+      int32_t* sap = reinterpret_cast<int32_t*>(res + rb);
+      int32_t* sbp = reinterpret_cast<int32_t*>(res + rb + align256(static_cast<size_t>(m) * 4));
+      NarrowCall c;
+      c.m = m;
+      c.n = n;
+      c.k = k;
+      c.kp = round_up(k, 16);
+      c.pA = pa_bits;
+      c.pB = pb_bits;
+      c.A = Ad;
+      c.lda = k;
+      c.B = Bd;
+      c.ldb = n;
+      c.nm = narrow_moduli(r, pa_bits);
+      c.ldr = round_up(n, 16);
+      c.bres = rest;
+      c.colsum = reinterpret_cast<int32_t*>(rest + bres);
+      c.res = res;
+      c.sa = sap;
+      c.sb = sbp;
+      c.flags = d->flags;
+      if (launch_narrow_residues(c, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+      if (launch_crt_f64(m, n, res, c.ldr, sap, sbp, Cd, n, crt_moduli(r), stream) != cudaSuccess)
+        return OZEMU_ERR_CUDA;
+    }
+    return cuda_status(
+        cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 8, Cd, n * 8, static_cast<size_t>(n) * 8, m, d2h, stream));
+  }
+
+  // Row chunks of A, each an independent product A_c B, pipelined:
+  //   copy stream: B in, A_0 in, A_1 in, ..., then C_c out as each is ready;
+  //   caller's stream: split of B's columns, then per chunk split + limb GEMM;
+  //   CRT stream: per chunk CRT, beside the next chunk's GEMM.
+  const int chunk = m >= 2048 ? round_up((m + 3) / 4, 256) : m;
+  const int nch = (m + chunk - 1) / chunk;
+  const size_t szBt = szB;
+  const size_t szBp = align256(plane_bytes(n, k, r)), szSb = align256(static_cast<size_t>(n) * 4);
+  const size_t szAp = align256(plane_bytes(chunk, k, r)), szSa = align256(static_cast<size_t>(chunk) * 4);
+  const size_t szRes = align256(ozemu_residue_bytes(chunk, n, r));
+  uint8_t* buf = nullptr;
+  s = workspace(d, szA + szB + szC + szBt + szBp + szSb + nch * (szAp + szSa + szRes), &buf);
+  if (s != OZEMU_OK) return s;
+  double* Ad = reinterpret_cast<double*>(buf);
+  double* Bd = reinterpret_cast<double*>(buf + szA);
+  double* Cd = reinterpret_cast<double*>(buf + szA + szB);
+  double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
+  uint8_t* bp = buf + szA + szB + szC + szBt;
+  int32_t* sbp = reinterpret_cast<int32_t*>(bp + szBp);
+  uint8_t* per_chunk = bp + szBp + szSb;
+  cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
+  cudaEvent_t* ev = d->ev;
+  const int evStart = 0, evB = 1, evA = 2, evG = 2 + 8, evC = 2 + 16, evD = 2 + 24;
+  const CrtModuli cm = crt_moduli(r);
+  // The helper streams start after everything the caller queued before.
+  if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  if (cudaMemcpy2DAsync(Bd, n * 8, B, static_cast<size_t>(ldb) * 8, static_cast<size_t>(n) * 8, k, h2d, cs) !=
+          cudaSuccess ||
+      cudaEventRecord(ev[evB], cs) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  for (int c = 0; c < nch; ++c) {
+    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
+    if (cudaMemcpy2DAsync(Ad + static_cast<size_t>(row0) * k, k * 8, A + static_cast<size_t>(row0) * lda,
+                          static_cast<size_t>(lda) * 8, static_cast<size_t>(k) * 8, mc, h2d, cs) != cudaSuccess ||
+        cudaEventRecord(ev[evA + c], cs) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+  }
+  if (cudaStreamWaitEvent(stream, ev[evB], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
+  s = split_cols_f64(k, n, Bd, n, pb_bits, r, bp, sbp, Bt, d, stream);
+  if (s != OZEMU_OK) return s;
+  for (int c = 0; c < nch; ++c) {
+    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
+    uint8_t* ap = per_chunk + c * (szAp + szSa + szRes);
+    int32_t* sap = reinterpret_cast<int32_t*>(ap + szAp);
+    uint8_t* res = ap + szAp + szSa;
+    if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
+    s = split_rows_f64(mc, k, Ad + static_cast<size_t>(row0) * k, k, pa_bits, r, ap, sap, d, stream);
+    if (s != OZEMU_OK) return s;
+    s = residue_gemm(mc, n, k, r, ap, bp, res, d, stream);
+    if (s != OZEMU_OK) return s;
+    if (cudaEventRecord(ev[evG + c], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG + c], 0) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (launch_crt_f64(mc, n, res, round_up(n, 16), sap, sbp, Cd + static_cast<size_t>(row0) * n, n, cm, xs) !=
+            cudaSuccess ||
+        cudaEventRecord(ev[evC + c], xs) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evC + c], 0) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc, static_cast<size_t>(ldc) * 8,
+                          Cd + static_cast<size_t>(row0) * n, n * 8, static_cast<size_t>(n) * 8, mc, d2h, cs) !=
+        cudaSuccess)
+      return OZEMU_ERR_CUDA;
+  }
+  // The caller's stream completes only after the last copy out.
+  if (cudaEventRecord(ev[evD], cs) != cudaSuccess || cudaStreamWaitEvent(stream, ev[evD], 0) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  return OZEMU_OK;
 }
 
 int ozemu_get_status(cudaStream_t stream) {

@@ -97,6 +97,9 @@ FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
     lambda oz: oz.ozemu_residue_gemm(4, 4, 4, 13, FAKE, FAKE, FAKE + 4, NULL),    # unaligned residues
     lambda oz: oz.ozemu_limb_gemm_s32(4, 4, 4, FAKE, FAKE, FAKE, 3, NULL),        # ldc < n
     lambda oz: oz.ozemu_crt_f64(4, 4, 13, FAKE, FAKE, NULL, FAKE, 4, NULL),
+    lambda oz: oz.ozemu_dgemm_host(4, 4, 4, FAKE, 3, FAKE, 4, FAKE, 4, 13, NULL),  # lda < k
+    lambda oz: oz.ozemu_dgemm_host(4, 4, 4, FAKE, 4, FAKE, 4, NULL, 4, 13, NULL),  # null C
+    lambda oz: oz.ozemu_dgemm_host(4, 4, 200, FAKE, 200, FAKE, 4, FAKE, 4, 1, NULL),  # 2k >= 256
     lambda oz: oz.ozemu_residues_narrow_f64(4, 3, 4, 13, FAKE, 4, FAKE, 3, FAKE, FAKE, FAKE, NULL),  # n > 2
     lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 0, 13, FAKE, 1, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # k < 1
     lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 1 << 25, 16, FAKE, 1 << 25, FAKE, 1, FAKE, FAKE, FAKE, NULL),
@@ -121,6 +124,7 @@ def test_narrow_limit(oz):
 def test_empty_problems_are_noops(oz):
     assert oz.ozemu_dgemm(0, 5, 5, NULL, 5, NULL, 5, NULL, 5, 13, NULL) == oz.OZEMU_OK
     assert oz.ozemu_dgemm(5, 0, 5, NULL, 5, NULL, 1, NULL, 1, 13, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_dgemm_host(0, 5, 5, NULL, 5, NULL, 5, NULL, 5, 13, NULL) == oz.OZEMU_OK
     assert oz.ozemu_igemm_s8(0, 0, 7, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
     assert oz.ozemu_split_rows_f64(0, 9, NULL, 9, 30, 13, NULL, NULL, NULL) == oz.OZEMU_OK
     assert oz.ozemu_residue_gemm(0, 3, 3, 13, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
