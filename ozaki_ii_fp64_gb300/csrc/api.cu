@@ -742,7 +742,7 @@ int ozemu_dgemm_host(int m, int n, int k, const double* A, int lda, const double
   //   copy stream: B in, A_0 in, A_1 in, ..., then C_c out as each is ready;
   //   caller's stream: split of B's columns, then per chunk split + limb GEMM;
   //   CRT stream: per chunk CRT, beside the next chunk's GEMM.
-  const int chunk = m >= 2048 ? round_up((m + 3) / 4, 256) : m;
+  const int chunk = m >= 4096 ? round_up((m + 7) / 8, 256) : (m >= 2048 ? round_up((m + 3) / 4, 256) : m);
   const int nch = (m + chunk - 1) / chunk;
   const size_t szBt = szB;
   const size_t szBp = align256(plane_bytes(n, k, r)), szSb = align256(static_cast<size_t>(n) * 4);
