@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-native", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the INT8 residue-GEMM comparison")
+    ap.add_argument("--no-igemm", action="store_true", help="skip the exact INT8 product leg (4096^3)")
     return ap.parse_args()
 
 
@@ -505,6 +506,47 @@ def run_gpu(args):
                 cmp["cublaslt_int8"] = "unavailable: %s" % str(exc).splitlines()[0][:120]
         line["int8_comparison"] = cmp
         del a8, b8, res8
+
+    if not args.no_igemm:
+        # The exact INT8 x INT8 -> INT32 product (9 FP4 limb GEMMs) on the
+        # 4096^3 int8 workload, beside cuBLASLt's INT8 GEMM on the same matrices.
+        Ai_h, Bi_h = make_pair(4096, 4096, 4096, WORKLOADS["igemm_s8_4096"]["seed"], "int8")
+        Ai = torch.from_numpy(Ai_h).to(dev)
+        Bi = torch.from_numpy(Bi_h).to(dev)
+        Ci = torch.empty((4096, 4096), dtype=torch.int32, device=dev)
+
+        def igemm():
+            check(oz.ozemu_igemm_s8(4096, 4096, 4096, Ai.data_ptr(), Bi.data_ptr(), Ci.data_ptr(), sh), "igemm")
+
+        igemm()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(5):
+            i0 = torch.cuda.Event(enable_timing=True)
+            i1 = torch.cuda.Event(enable_timing=True)
+            i0.record(stream)
+            igemm()
+            i1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(i0.elapsed_time(i1))
+        ig_ms = statistics.median(times)
+        iflop = 2.0 * 4096 ** 3
+        leg = {"ms": round(ig_ms, 3), "tops": round(iflop / (ig_ms / 1e3) / 1e12, 1),
+               "fp4_frac": round(9 * iflop / (ig_ms / 1e3) / 1e12 / fp4_peak, 4),
+               "launches": "split A, transpose B, split B^T, limb GEMM (int32 epilogue)"}
+        if hasattr(torch, "_int_mm"):
+            ref = torch._int_mm(Ai, Bi)
+            torch.cuda.synchronize(dev)
+            i0 = torch.cuda.Event(enable_timing=True)
+            i1 = torch.cuda.Event(enable_timing=True)
+            i0.record(stream)
+            torch._int_mm(Ai, Bi)
+            i1.record(stream)
+            torch.cuda.synchronize(dev)
+            leg["exact_vs_cublaslt"] = bool(torch.equal(ref, Ci))
+            leg["cublaslt_int8_ms"] = round(i0.elapsed_time(i1), 3)
+        line["igemm_s8_4096"] = leg
+        del Ai, Bi, Ci
 
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_oracle(args.workload, r, CPU_MIN_SECONDS, shape={"m": m, "n": n, "k": k})
