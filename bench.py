@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-native", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the INT8 residue-GEMM comparison")
     ap.add_argument("--no-igemm", action="store_true", help="skip the exact INT8 product leg (4096^3)")
+    ap.add_argument("--chunks", type=int, default=4,
+                    help="row chunks of A in the timed step (1: the stages one after another)")
     return ap.parse_args()
 
 
@@ -291,13 +293,61 @@ def run_gpu(args):
         dominant = "limb_gemm"
         launches_per_step = 5  # split rows, transpose, split rows of B^T, limb GEMM, CRT
 
-    def step(ev0=None, ev1=None):
-        for name, fn in stages:
-            if name == dominant and ev0 is not None:
-                ev0.record(stream)
-            fn()
-            if name == dominant and ev1 is not None:
-                ev1.record(stream)
+    # The timed step.  Limb-plane path: the stage calls pipelined over row
+    # chunks of A on three streams -- B's split, then each chunk's split
+    # (split stream), limb GEMM (main stream, bracketed by events) and CRT
+    # (CRT stream, beside the next chunk's GEMM); the same schedule as the
+    # library's host-buffer entry point.  Narrow path: its two calls in order.
+    chunks = 1 if narrow else max(1, args.chunks)
+    crows = m if chunks == 1 else ((m + chunks - 1) // chunks + 255) // 256 * 256
+    chunk_bufs = []
+    for row0 in range(0, m, crows):
+        mc = min(crows, m - row0)
+        chunk_bufs.append((row0, mc, torch.empty(oz.ozemu_plane_bytes(mc, k, r), dtype=torch.uint8, device=dev),
+                           torch.empty(mc, dtype=torch.int32, device=dev),
+                           torch.empty(oz.ozemu_residue_bytes(mc, n, r), dtype=torch.uint8, device=dev)))
+    nch = len(chunk_bufs)
+    s_split = torch.cuda.Stream(dev)
+    s_crt = torch.cuda.Stream(dev)
+    ev_start = torch.cuda.Event()
+    evA = [torch.cuda.Event() for _ in range(nch)]
+    evG = [torch.cuda.Event() for _ in range(nch)]
+    evC = [torch.cuda.Event() for _ in range(nch)]
+    if not narrow:
+        launches_per_step = 2 + 3 * nch  # transpose + split of B; per chunk split, limb GEMM, CRT
+    n_dominant = 1 if narrow else nch
+
+    def step(gev=None):
+        if narrow:
+            if gev is not None:
+                gev[0][0].record(stream)
+            narrow_residues()
+            if gev is not None:
+                gev[0][1].record(stream)
+            crt()
+            return
+        ev_start.record(stream)
+        s_split.wait_event(ev_start)
+        s_crt.wait_event(ev_start)
+        split_b()
+        for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
+            check(oz.ozemu_split_rows_f64(mc, k, A.data_ptr() + row0 * k * 8, k, pA, r, apc.data_ptr(),
+                                          sac.data_ptr(), s_split.cuda_stream), "split A chunk")
+            evA[c].record(s_split)
+        for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
+            stream.wait_event(evA[c])
+            if gev is not None:
+                gev[c][0].record(stream)
+            check(oz.ozemu_residue_gemm(mc, n, k, r, apc.data_ptr(), bp.data_ptr(), resc.data_ptr(), sh),
+                  "limb gemm chunk")
+            if gev is not None:
+                gev[c][1].record(stream)
+            evG[c].record(stream)
+            s_crt.wait_event(evG[c])
+            check(oz.ozemu_crt_f64(mc, n, r, resc.data_ptr(), sac.data_ptr(), sb.data_ptr(),
+                                   C.data_ptr() + row0 * n * 8, n, s_crt.cuda_stream), "crt chunk")
+            evC[c].record(s_crt)
+        stream.wait_event(evC[nch - 1])
 
     def stage_times(which):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(which) + 1)]
@@ -316,10 +366,11 @@ def run_gpu(args):
 
     # Per-stage durations (one untimed pass, for the report only).
     stage_ms = stage_times(stages)
+    C_staged = C.clone()
 
     # Timed region.
-    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    gev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dominant)]
+           for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
@@ -329,17 +380,19 @@ def run_gpu(args):
     clocks.start()
     t_start.record(stream)
     for i in range(args.steps):
-        step(g0[i], g1[i])
+        step(gev[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if ws > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    dom_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
+    dom_ms = sum(a.elapsed_time(b) for g in gev for a, b in g) / args.steps  # per step
     status = oz.ozemu_get_status(sh)
     if status != 0:
         raise SystemExit("device status %d after the timed region" % status)
+    if not torch.equal(C.view(torch.int64), C_staged.view(torch.int64)):
+        raise SystemExit("the timed step's result differs from the stages run one after another")
     elapsed_ms = max_over_ranks(elapsed_ms, dist if ws > 1 else None, dev)
 
     ms_per_step = elapsed_ms / args.steps
@@ -382,6 +435,7 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args, spec), "m": m, "n": n, "k": k, "r": r, "dist": spec["dist"],
                        "seed": spec["seed"], "path": "narrow (fused)" if narrow else "limb planes",
+                       "row_chunks": nch,
                        "l2": "inputs larger than L2 (%d MiB per operand), no flush" % (m * k * 8 >> 20)},
             "pct_fp4_roofline" if not narrow else "pct_io_roofline": round(pct_roof, 2), "roofline": roofline,
             "stage_ms": {kk: round(v, 3) for kk, v in stage_ms.items()},
