@@ -45,6 +45,10 @@
  *   uint8 [r][m][ldr], ldr = round_up(n, 16): residue of C' modulo m_l in
  *   [0, m_l) at byte (l*m + i)*ldr + j.  Total bytes: ozemu_residue_bytes.
  *
+ * Concurrency: the workspace is cached per device and shared by the calls
+ * that use it, so calls on one device must not overlap in time on different
+ * streams (issue them on one stream, or synchronise in between).
+ *
  * Errors: calls return an ozemu_status.  Argument checks happen on the host
  * before anything is enqueued.  Device-side conditions (non-finite input,
  * a pipeline wait that hit its time limit) set a per-device flag that
