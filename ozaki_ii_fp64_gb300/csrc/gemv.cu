@@ -103,13 +103,9 @@ template <int R, int NCH, bool kFast, int kThreads>
 __device__ __forceinline__ void fused_pass2(const double* rowp, int k, int kbeg, int kend, bool vec_ok, int s, int d0,
                                             uint64_t off, const uint8_t* __restrict__ bres, int kp,
                                             uint32_t (&acc)[NCH][R]) {
-  uint64_t nxt[8];
-  if (kbeg < kend) load8_f64(rowp, k, kbeg, vec_ok, nxt, true);
   for (int k0 = kbeg; k0 < kend; k0 += kThreads * 8) {
     uint64_t b[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) b[e] = nxt[e];
-    if (k0 + kThreads * 8 < kend) load8_f64(rowp, k, k0 + kThreads * 8, vec_ok, nxt, true);
+    load8_f64(rowp, k, k0, vec_ok, b, true);
     uint32_t W[4][NCH];  // element pair q = (2q, 2q + 1): chunk c of both as 16-bit halves
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -198,13 +194,13 @@ __device__ __forceinline__ void group_sum_into(uint32_t (&v)[V], uint32_t* buf, 
   group_sync(bar);
 }
 
-// One CTA of 256 threads per row at a time, two CTAs per SM: pass 1 finds
-// the row's exponent while the other CTA computes, pass 2 re-reads the row
+// One CTA of 256 threads per row at a time, three CTAs per SM: pass 1 finds
+// the row's exponent while the other CTAs compute, pass 2 re-reads the row
 // from L2 and B's residues through L1 (every row re-reads them, so the
 // kernel asks for little shared memory).  Dynamic shared memory: the
 // reduction buffer.
 template <int R, int N, int NCH>
-__global__ void __launch_bounds__(kGroup, 2)
+__global__ void __launch_bounds__(kGroup, 3)
     dgemv_fused_kernel(const double* __restrict__ A, long long lda, int m, int k, int kp, int p,
                        const NarrowModuli nm, const uint8_t* __restrict__ bres, const int32_t* __restrict__ colsum,
                        uint8_t* __restrict__ res, long long ldr, int32_t* __restrict__ shifts, uint32_t* flags) {
@@ -289,7 +285,7 @@ cudaError_t launch_narrow_r(const NarrowCall& c, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const bool three = c.pA <= 46;  // u = A' + 2^p <= 2^47 fits three 16-bit chunks
-  const int grid = c.m < sm_count() * 2 ? c.m : sm_count() * 2;  // two CTAs per SM
+  const int grid = c.m < sm_count() * 3 ? c.m : sm_count() * 3;  // three CTAs per SM
 #define OZEMU_FUSED(NN, NCH)                                                                                      \
   do {                                                                                                          \
     const int dyn = (kGroup / 4) * (NCH * R + 1) * 4;                                                           \
