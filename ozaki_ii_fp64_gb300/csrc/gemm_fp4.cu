@@ -459,6 +459,8 @@ struct PairArgs {
   EpiModuli em;
   uint8_t* res_out;
   long long ldr;
+  int32_t* c32;   // INT8 mode: C32 = D1 + 169 D2, leading dimension ldc
+  long long ldc;
   uint32_t* flags;
 };
 
@@ -481,6 +483,9 @@ __device__ __forceinline__ void settle_after_abort() {
   }
 }
 
+// kInt: the INT8 product (r = 1, one exact K chunk): the epilogue writes the
+// int32 sums D1 + 169 D2 slice by slice instead of residues.
+template <bool kInt>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     limb_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const PairArgs args) {
@@ -683,31 +688,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0 + c + kSlice, n1);
             tmem_ld_cols<kSlice>(tbase + lane_off + kColD2p + col0 + c + kSlice, n2);
           }
+          if constexpr (kInt) {
+            if (grow < args.m) {
+              int32_t* crow = args.c32 + static_cast<long long>(grow) * args.ldc;
+              const int col = tn * kBN2 + static_cast<int>(col0) + c;
+              int v[kSlice];
 #pragma unroll
-          for (int i = 0; i < kSlice; i += 4) {
-            uint32_t b[4];
+              for (int i = 0; i < kSlice; ++i)
+                v[i] = __float2int_rn(__uint_as_float(v1[i])) + 169 * __float2int_rn(__uint_as_float(v2[i]));
+              if (((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.c32) & 15u) == 0) &&
+                  col + kSlice <= args.n) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              // |D1| <= 1728 * 8192 and |r2 w169| <= 129 * 128, so D1 + r2 w169 stays
-              // below 2^24 and exact.
-              const float r2 = fmod_small(__uint_as_float(v2[i + e]), fm, finv);
-              float v = fmod_small(fmaf(r2, fw, __uint_as_float(v1[i + e])), fm, finv);
-              v = v < 0.f ? v + fm : v;
-              if (!first) {  // + the residue of the earlier chunks, modulo m
-                v += __uint_as_float(__byte_perm(packed[(c + i) / 4], 0x4B000000u, 0x7650u | (e & 3))) - 8388608.0f;
-                v = v >= fm ? v - fm : v;
+                for (int q = 0; q < kSlice; q += 4)
+                  *reinterpret_cast<int4*>(crow + col + q) = make_int4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < kSlice; ++i)
+                  if (col + i < args.n) crow[col + i] = v[i];
               }
-              b[e] = byte_of_float(v);
             }
-            packed[(c + i) / 4] =
-                __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kSlice; i += 4) {
+              uint32_t b[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // |D1| <= 1728 * 8192 and |r2 w169| <= 129 * 128, so D1 + r2 w169 stays
+                // below 2^24 and exact.
+                const float r2 = fmod_small(__uint_as_float(v2[i + e]), fm, finv);
+                float v = fmod_small(fmaf(r2, fw, __uint_as_float(v1[i + e])), fm, finv);
+                v = v < 0.f ? v + fm : v;
+                if (!first) {  // + the residue of the earlier chunks, modulo m
+                  v += __uint_as_float(__byte_perm(packed[(c + i) / 4], 0x4B000000u, 0x7650u | (e & 3))) - 8388608.0f;
+                  v = v >= fm ? v - fm : v;
+                }
+                b[e] = byte_of_float(v);
+              }
+              packed[(c + i) / 4] =
+                  __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty_leader);
       }
-      if (!live || grow >= args.m) continue;
+      if (kInt || !live || grow >= args.m) continue;
       uint8_t* rrow = args.res_out + (static_cast<long long>(l) * args.m + grow) * args.ldr;
       const int gcol0 = tn * kBN2 + static_cast<int>(col0);
 #pragma unroll
@@ -795,6 +821,7 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <bool kInt>
 cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
   const int k_p = round_up(c.k, kKAlign);
@@ -814,12 +841,15 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   a.em = c.em;
   a.res_out = c.res_out;
   a.ldr = c.ldr;
+  a.c32 = c.c32;
+  a.ldc = c.ldc;
   a.flags = c.flags;
-  cudaError_t e = cudaFuncSetAttribute(limb_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2);
+  cudaError_t e =
+      cudaFuncSetAttribute(limb_gemm_pair_kernel<kInt>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2);
   if (e != cudaSuccess) return e;
   // A persistent grid must not exceed the clusters that can be resident at
   // once, or the excess clusters start only when others finish.
-  static int max_pairs[64] = {0};
+  static int max_pairs[64] = {0};  // the two instantiations have the same resources
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -836,7 +866,7 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, limb_gemm_pair_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, limb_gemm_pair_kernel<kInt>, &cfg);
     if (e != cudaSuccess || n < 1) {
       cudaGetLastError();
       int sms = 148;
@@ -846,12 +876,14 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
     max_pairs[dev] = n;
   }
   const int pairs = a.total_tiles < max_pairs[dev] ? a.total_tiles : max_pairs[dev];
-  limb_gemm_pair_kernel<<<2 * pairs, kThreads, kSmem2, stream>>>(ma, mb, a);
+  limb_gemm_pair_kernel<kInt><<<2 * pairs, kThreads, kSmem2, stream>>>(ma, mb, a);
   return cudaGetLastError();
 }
 
 bool use_pair(const LimbGemmCall& c) {
-  if (!c.residue_mode || c.n <= 64 || c.kc_blocks < 1) return false;
+  if (c.n <= 64 || c.kc_blocks < 1) return false;
+  // The INT8 product keeps no running value across K chunks in this kernel.
+  if (!c.residue_mode && round_up(c.k, kKAlign) / 128 > c.kc_blocks) return false;
   if (const char* s = std::getenv("OZEMU_GEMM_PAIR")) return s[0] != '0';
   return true;
 }
@@ -867,7 +899,7 @@ cudaError_t launch_mode(const LimbGemmCall& c, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream) {
-  if (use_pair(call)) return launch_pair(call, stream);
+  if (use_pair(call)) return call.residue_mode ? launch_pair<false>(call, stream) : launch_pair<true>(call, stream);
   return call.residue_mode ? launch_mode<true>(call, stream) : launch_mode<false>(call, stream);
 }
 
