@@ -353,6 +353,103 @@ int pipeline_state(DeviceState* d) {
   return OZEMU_OK;
 }
 
+// C = A B over row chunks of A, each an independent product A_c B, pipelined
+// on the caller's stream and two helper streams.  With host buffers
+// (from_host): the copy stream brings B in, then A_0, A_1, ...; the caller's
+// stream splits B's columns, then per chunk splits its rows and runs the limb
+// GEMM; the CRT stream runs each chunk's CRT beside the next chunk's GEMM;
+// the copy stream sends each chunk of C out as soon as it is ready.  With
+// device buffers the helper stream splits the chunks' rows ahead of the GEMMs
+// instead.  The caller's stream completes after the last CRT (device) or
+// copy out (host); the helper streams start after everything the caller
+// queued before.
+int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc, int r,
+                  int pa_bits, int pb_bits, bool from_host, DeviceState* d, cudaStream_t stream) {
+  int s = pipeline_state(d);
+  if (s != OZEMU_OK) return s;
+  const int chunk = from_host ? (m >= 4096 ? round_up((m + 7) / 8, 256) : (m >= 2048 ? round_up((m + 3) / 4, 256) : m))
+                              : (m >= 2048 ? round_up((m + 3) / 4, 256) : m);
+  const int nch = (m + chunk - 1) / chunk;
+  const size_t szA = from_host ? align256(static_cast<size_t>(m) * k * 8) : 0;
+  const size_t szB = from_host ? align256(static_cast<size_t>(k) * n * 8) : 0;
+  const size_t szC = from_host ? align256(static_cast<size_t>(m) * n * 8) : 0;
+  const size_t szBt = align256(static_cast<size_t>(k) * n * 8);
+  const size_t szBp = align256(plane_bytes(n, k, r)), szSb = align256(static_cast<size_t>(n) * 4);
+  const size_t szAp = align256(plane_bytes(chunk, k, r)), szSa = align256(static_cast<size_t>(chunk) * 4);
+  const size_t szRes = align256(ozemu_residue_bytes(chunk, n, r));
+  uint8_t* buf = nullptr;
+  s = workspace(d, szA + szB + szC + szBt + szBp + szSb + nch * (szAp + szSa + szRes), &buf);
+  if (s != OZEMU_OK) return s;
+  // Operands on the device: copies in the workspace, or the caller's buffers.
+  const double* Ad = from_host ? reinterpret_cast<const double*>(buf) : A;
+  const double* Bd = from_host ? reinterpret_cast<const double*>(buf + szA) : B;
+  double* Cd = from_host ? reinterpret_cast<double*>(buf + szA + szB) : C;
+  const long long ldad = from_host ? k : lda, ldbd = from_host ? n : ldb, ldcd = from_host ? n : ldc;
+  double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
+  uint8_t* bp = buf + szA + szB + szC + szBt;
+  int32_t* sbp = reinterpret_cast<int32_t*>(bp + szBp);
+  uint8_t* per_chunk = bp + szBp + szSb;
+  cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
+  cudaEvent_t* ev = d->ev;
+  const int evStart = 0, evB = 1, evA = 2, evG = 2 + 8, evC = 2 + 16, evD = 2 + 24;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  const CrtModuli cm = crt_moduli(r);
+  if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  if (from_host) {
+    if (cudaMemcpy2DAsync(const_cast<double*>(Bd), n * 8, B, static_cast<size_t>(ldb) * 8,
+                          static_cast<size_t>(n) * 8, k, h2d, cs) != cudaSuccess ||
+        cudaEventRecord(ev[evB], cs) != cudaSuccess || cudaStreamWaitEvent(stream, ev[evB], 0) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+  }
+  for (int c = 0; c < nch; ++c) {
+    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
+    if (from_host) {
+      if (cudaMemcpy2DAsync(const_cast<double*>(Ad) + static_cast<size_t>(row0) * k, k * 8,
+                            A + static_cast<size_t>(row0) * lda, static_cast<size_t>(lda) * 8,
+                            static_cast<size_t>(k) * 8, mc, h2d, cs) != cudaSuccess)
+        return OZEMU_ERR_CUDA;
+    } else {
+      uint8_t* ap = per_chunk + c * (szAp + szSa + szRes);
+      s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, reinterpret_cast<int32_t*>(ap + szAp), d, cs);
+      if (s != OZEMU_OK) return s;
+    }
+    if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
+  }
+  s = split_cols_f64(k, n, Bd, ldbd, pb_bits, r, bp, sbp, Bt, d, stream);
+  if (s != OZEMU_OK) return s;
+  for (int c = 0; c < nch; ++c) {
+    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
+    uint8_t* ap = per_chunk + c * (szAp + szSa + szRes);
+    int32_t* sap = reinterpret_cast<int32_t*>(ap + szAp);
+    uint8_t* res = ap + szAp + szSa;
+    if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
+    if (from_host) {
+      s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream);
+      if (s != OZEMU_OK) return s;
+    }
+    s = residue_gemm(mc, n, k, r, ap, bp, res, d, stream);
+    if (s != OZEMU_OK) return s;
+    if (cudaEventRecord(ev[evG + c], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG + c], 0) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (launch_crt_f64(mc, n, res, round_up(n, 16), sap, sbp, Cd + row0 * ldcd, ldcd, cm, xs) != cudaSuccess ||
+        cudaEventRecord(ev[evC + c], xs) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (from_host) {
+      if (cudaStreamWaitEvent(cs, ev[evC + c], 0) != cudaSuccess ||
+          cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc, static_cast<size_t>(ldc) * 8, Cd + row0 * ldcd,
+                            n * 8, static_cast<size_t>(n) * 8, mc, d2h, cs) != cudaSuccess)
+        return OZEMU_ERR_CUDA;
+    }
+  }
+  // The caller's stream completes only after the last CRT (or copy out).
+  cudaStream_t last = from_host ? cs : xs;
+  if (cudaEventRecord(ev[evD], last) != cudaSuccess || cudaStreamWaitEvent(stream, ev[evD], 0) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  return OZEMU_OK;
+}
+
 int limb_gemm_s32(int m, int n, int k, const uint8_t* ap, const uint8_t* bp, int32_t* C, long long ldc,
                   DeviceState* d, cudaStream_t st) {
   LimbGemmCall c;
@@ -645,6 +742,7 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
   if (n <= kNarrowMaxN && k <= kNarrowMaxK && pa_bits <= kNarrowMaxP && narrow_enabled())
     return dgemm_narrow(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, d, stream);
+  if (m >= 2048) return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, false, d, stream);
   const size_t pa = align256(plane_bytes(m, k, r)), pb = align256(plane_bytes(n, k, r));
   const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
   const size_t rb = align256(ozemu_residue_bytes(m, n, r));
@@ -738,73 +836,7 @@ int ozemu_dgemm_host(int m, int n, int k, const double* A, int lda, const double
         cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 8, Cd, n * 8, static_cast<size_t>(n) * 8, m, d2h, stream));
   }
 
-  // Row chunks of A, each an independent product A_c B, pipelined:
-  //   copy stream: B in, A_0 in, A_1 in, ..., then C_c out as each is ready;
-  //   caller's stream: split of B's columns, then per chunk split + limb GEMM;
-  //   CRT stream: per chunk CRT, beside the next chunk's GEMM.
-  const int chunk = m >= 4096 ? round_up((m + 7) / 8, 256) : (m >= 2048 ? round_up((m + 3) / 4, 256) : m);
-  const int nch = (m + chunk - 1) / chunk;
-  const size_t szBt = szB;
-  const size_t szBp = align256(plane_bytes(n, k, r)), szSb = align256(static_cast<size_t>(n) * 4);
-  const size_t szAp = align256(plane_bytes(chunk, k, r)), szSa = align256(static_cast<size_t>(chunk) * 4);
-  const size_t szRes = align256(ozemu_residue_bytes(chunk, n, r));
-  uint8_t* buf = nullptr;
-  s = workspace(d, szA + szB + szC + szBt + szBp + szSb + nch * (szAp + szSa + szRes), &buf);
-  if (s != OZEMU_OK) return s;
-  double* Ad = reinterpret_cast<double*>(buf);
-  double* Bd = reinterpret_cast<double*>(buf + szA);
-  double* Cd = reinterpret_cast<double*>(buf + szA + szB);
-  double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
-  uint8_t* bp = buf + szA + szB + szC + szBt;
-  int32_t* sbp = reinterpret_cast<int32_t*>(bp + szBp);
-  uint8_t* per_chunk = bp + szBp + szSb;
-  cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
-  cudaEvent_t* ev = d->ev;
-  const int evStart = 0, evB = 1, evA = 2, evG = 2 + 8, evC = 2 + 16, evD = 2 + 24;
-  const CrtModuli cm = crt_moduli(r);
-  // The helper streams start after everything the caller queued before.
-  if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
-      cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
-    return OZEMU_ERR_CUDA;
-  if (cudaMemcpy2DAsync(Bd, n * 8, B, static_cast<size_t>(ldb) * 8, static_cast<size_t>(n) * 8, k, h2d, cs) !=
-          cudaSuccess ||
-      cudaEventRecord(ev[evB], cs) != cudaSuccess)
-    return OZEMU_ERR_CUDA;
-  for (int c = 0; c < nch; ++c) {
-    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
-    if (cudaMemcpy2DAsync(Ad + static_cast<size_t>(row0) * k, k * 8, A + static_cast<size_t>(row0) * lda,
-                          static_cast<size_t>(lda) * 8, static_cast<size_t>(k) * 8, mc, h2d, cs) != cudaSuccess ||
-        cudaEventRecord(ev[evA + c], cs) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
-  }
-  if (cudaStreamWaitEvent(stream, ev[evB], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
-  s = split_cols_f64(k, n, Bd, n, pb_bits, r, bp, sbp, Bt, d, stream);
-  if (s != OZEMU_OK) return s;
-  for (int c = 0; c < nch; ++c) {
-    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
-    uint8_t* ap = per_chunk + c * (szAp + szSa + szRes);
-    int32_t* sap = reinterpret_cast<int32_t*>(ap + szAp);
-    uint8_t* res = ap + szAp + szSa;
-    if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
-    s = split_rows_f64(mc, k, Ad + static_cast<size_t>(row0) * k, k, pa_bits, r, ap, sap, d, stream);
-    if (s != OZEMU_OK) return s;
-    s = residue_gemm(mc, n, k, r, ap, bp, res, d, stream);
-    if (s != OZEMU_OK) return s;
-    if (cudaEventRecord(ev[evG + c], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG + c], 0) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
-    if (launch_crt_f64(mc, n, res, round_up(n, 16), sap, sbp, Cd + static_cast<size_t>(row0) * n, n, cm, xs) !=
-            cudaSuccess ||
-        cudaEventRecord(ev[evC + c], xs) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evC + c], 0) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
-    if (cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc, static_cast<size_t>(ldc) * 8,
-                          Cd + static_cast<size_t>(row0) * n, n * 8, static_cast<size_t>(n) * 8, mc, d2h, cs) !=
-        cudaSuccess)
-      return OZEMU_ERR_CUDA;
-  }
-  // The caller's stream completes only after the last copy out.
-  if (cudaEventRecord(ev[evD], cs) != cudaSuccess || cudaStreamWaitEvent(stream, ev[evD], 0) != cudaSuccess)
-    return OZEMU_ERR_CUDA;
-  return OZEMU_OK;
+  return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, true, d, stream);
 }
 
 int ozemu_get_status(cudaStream_t stream) {

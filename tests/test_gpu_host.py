@@ -75,3 +75,19 @@ def test_dgemm_host_k0_and_repeated_calls(oz):
     for (A_, B_, C_) in ((A1, B1, C1), (A2, B2, C2)):
         rows = np.array([0, 1, 1000, 2099])
         assert same_bits(C_.numpy()[rows], oracle.dgemm_block(A_, B_, 13, rows=rows))
+
+
+@pytest.mark.parametrize("m,n,k,r", [(2300, 130, 700, 13), (4100, 257, 300, 12)])
+def test_dgemm_device_chunked(oz, m, n, k, r):
+    # ozemu_dgemm pipelines row chunks of A on helper streams when m >= 2048;
+    # padded leading dimensions of A and C, rows checked against the oracle.
+    A, B = make_pair(m, n, k, seed=5 * m + n, dist="wide")
+    Ad = torch.zeros((m, k + 5), dtype=torch.float64, device="cuda")
+    Ad[:, :k] = torch.from_numpy(A).cuda()
+    Cd = torch.full((m, n + 3), 7.0, dtype=torch.float64, device="cuda")
+    oz.dgemm(Ad[:, :k], torch.from_numpy(B).cuda(), r, out=Cd[:, :n])
+    assert oz.get_status() == oz.OZEMU_OK
+    C = Cd.cpu().numpy()
+    assert (C[:, n:] == 7.0).all()
+    rows = np.unique(np.r_[0:3, m // 4 - 1: m // 4 + 2, m // 2, 3 * m // 4, m - 3:m])
+    assert same_bits(C[rows, :n], oracle.dgemm_block(A, B, r, rows=rows))
