@@ -63,9 +63,33 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* red) {
   return m;
 }
 
-__device__ __forceinline__ void load8_f64(const double* rowp, int k, int k0, bool vec_ok, uint64_t (&b)[8],
+// Widest vector load a row of X allows: 2 = 32 bytes (X 32-byte aligned,
+// ldx a multiple of 4), 1 = 16 bytes, 0 = single elements.
+__device__ __forceinline__ int row_vector_width(const double* X, long long ldx) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(X);
+  if ((a & 31u) == 0 && (ldx & 3) == 0) return 2;
+  if ((a & 15u) == 0 && (ldx & 1) == 0) return 1;
+  return 0;
+}
+
+// Elements k0 .. k0+7 of a row (zeros past k).  With 32-byte loads the
+// warp's two load instructions each fill whole 32-byte sectors (each lane's
+// eight elements are 64 bytes apart from its neighbour's).
+__device__ __forceinline__ void load8_f64(const double* rowp, int k, int k0, int vec, uint64_t (&b)[8],
                                           bool last_use) {
-  if (vec_ok && k0 + 8 <= k) {
+  if (vec == 2 && k0 + 8 <= k) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      unsigned long long x0, x1, x2, x3;
+      asm volatile("ld.global.nc.v4.u64 {%0, %1, %2, %3}, [%4];"
+                   : "=l"(x0), "=l"(x1), "=l"(x2), "=l"(x3)
+                   : "l"(rowp + k0 + 4 * q));
+      b[4 * q] = x0;
+      b[4 * q + 1] = x1;
+      b[4 * q + 2] = x2;
+      b[4 * q + 3] = x3;
+    }
+  } else if (vec >= 1 && k0 + 8 <= k) {
     const double2* p = reinterpret_cast<const double2*>(rowp + k0);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {

@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t dp2a_hi(uint32_t a, uint32_t b, uint32_t c) 
 // acc[c][l] += sum_k chunk_c(u_k) b_{l,k} with two-way 16 x 8-bit dot
 // products (dp2a), four elements per bres word.
 template <int R, int NCH, bool kFast, int kThreads>
-__device__ __forceinline__ void fused_pass2(const double* rowp, int k, int kbeg, int kend, bool vec_ok, int s, int d0,
+__device__ __forceinline__ void fused_pass2(const double* rowp, int k, int kbeg, int kend, int vec_ok, int s, int d0,
                                             uint64_t off, const uint8_t* __restrict__ bres, int kp,
                                             uint32_t (&acc)[NCH][R]) {
   for (int k0 = kbeg; k0 < kend; k0 += kThreads * 8) {
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kGroup, 3)
   __shared__ unsigned long long tot[V];
   const int tg = threadIdx.x, bar = 1;
   uint32_t* buf = reinterpret_cast<uint32_t*>(dsm);
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 1) == 0);
+  const int vec_ok = row_vector_width(A, lda);
   const uint64_t off = 1ull << p;
   const int row_step = gridDim.x;
 

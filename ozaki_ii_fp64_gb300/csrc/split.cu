@@ -76,7 +76,7 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
 // Pass 2 of the row split over the row's elements: integers, residues and
 // limb codes (or residue bytes), packed and stored.
 template <int R, bool kRes8, bool kFast>
-__device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, bool vec_ok, int s,
+__device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s,
                                             const SplitModuli& mods, const uint32_t* lut, uint8_t* out_row,
                                             long long plane_stride) {
   for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
   const long long row_bytes = kRes8 ? k_p : k_p / 2;
   const long long plane_stride = static_cast<long long>(rows_p) * row_bytes;
   constexpr int kPlanesPerModulus = kRes8 ? 1 : 3;
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0);
+  const int vec_ok = row_vector_width(X, ldx);
 
   for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
     uint8_t* out_row = planes + static_cast<long long>(row) * row_bytes;
