@@ -138,3 +138,39 @@ def test_product_path_has_no_fallback():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
+
+
+def test_header_and_library_usable_from_plain_c(oz, tmp_path):
+    # The boundary is a C ABI: a C99 program includes the header, links the
+    # library and calls host-side entry points (no device work).
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    lib = oz.library_path()
+    cuda_inc = "/usr/local/cuda/include"
+    src = tmp_path / "use.c"
+    src.write_text(
+        '#include "ozemu.h"\n'
+        "#include <stdio.h>\n"
+        "int main(void) {\n"
+        "  int pa = 0, pb = 0, m[16];\n"
+        "  if (ozemu_max_moduli() != 16) return 1;\n"
+        "  if (ozemu_moduli(3, m) != OZEMU_OK || m[0] != 256 || m[1] != 255 || m[2] != 253) return 2;\n"
+        "  if (ozemu_bit_budget(8192, 13, &pa, &pb) != OZEMU_OK) return 3;\n"
+        "  if (ozemu_dgemm(4, 4, 4, 0, 3, 0, 4, 0, 4, 13, 0) != OZEMU_ERR_INVALID_ARG) return 4;\n"
+        '  printf("%d %d\\n", pa, pb);\n'
+        "  return 0;\n"
+        "}\n")
+    exe = tmp_path / "use"
+    cmd = [gcc, "-std=c99", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe),
+           "-L", os.path.dirname(lib), "-lozemu", "-Wl,-rpath," + os.path.dirname(lib)]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0 and "cuda_runtime_api.h" in res.stderr:
+        pytest.skip("CUDA headers not found")
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, run.stdout + run.stderr
+    _, pa, pb = oracle.bit_budget(8192, 13)
+    assert run.stdout.split() == [str(pa), str(pb)]
