@@ -85,12 +85,8 @@ SplitModuli split_moduli(int r) {
   std::memset(&s, 0, sizeof(s));
   s.r = r;
   for (int l = 0; l < r; ++l) {
-    const uint32_t m = moduli().m[l];
-    s.m[l] = m;
-    s.c21x4[l] = 4u * pow_mod(2, 21, m);
-    s.c42x4[l] = 4u * pow_mod(2, 42, m);
-    s.magic4[l] = static_cast<uint32_t>((1ull << 32) / (4ull * m));
-    s.off[l] = pow_mod(2, 62, m);
+    s.m[l] = moduli().m[l];
+    if (s.m[l] != kModulusTable[l]) s.r = 0;  // table mismatch: the launch refuses r = 0
   }
   return s;
 }

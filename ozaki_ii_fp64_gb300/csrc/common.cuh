@@ -22,16 +22,18 @@ constexpr uint32_t kFlagTimeout = 2u;
 // Time limit of one pipeline wait before the kernel gives up (ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Per-modulus constants for the deconstruction kernel.  With the integer
-// offset u = x + 2^62 split in 21-bit chunks u = a2 2^42 + a1 2^21 + a0,
-// v = a2 (2^42 mod m) + a1 (2^21 mod m) + a0 < 2^30, and 4v < 2^32.
+// The moduli in the order they are taken: greedy pairwise-coprime integers
+// counting down from 256 (r moduli = the first r).  The deconstruction kernel
+// derives its per-modulus constants from this table at compile time; the host
+// checks its own construction against it before a launch.
+constexpr uint32_t kModulusTable[kMaxModuli] = {256, 255, 253, 251, 247, 241, 239, 233,
+                                                229, 227, 223, 217, 211, 199, 197, 193};
+
+// Moduli of a deconstruction launch (r = 0 if the host's moduli differ from
+// kModulusTable; the launch then refuses).
 struct SplitModuli {
   int r;
   uint32_t m[kMaxModuli];
-  uint32_t c21x4[kMaxModuli];   // 4 (2^21 mod m)
-  uint32_t c42x4[kMaxModuli];   // 4 (2^42 mod m)
-  uint32_t magic4[kMaxModuli];  // floor(2^32 / (4 m))
-  uint32_t off[kMaxModuli];     // 2^62 mod m
 };
 
 // Per-modulus constants for the fused narrow-N path.

@@ -105,16 +105,18 @@ __device__ __forceinline__ void load8_f64(const double* rowp, int k, int k0, int
 }
 
 // A' + off (mod 2^64) for the fp64 pattern `bits` of an element of a row
-// whose largest magnitude is a normal number, with p <= 52: |x 2^s| is then a right shift
-// of the 53-bit significand by d = (1075 - s) - max(E, 1) >= 1, rounded half
-// to even.  Non-finite elements give an unspecified value (they set the
+// whose largest magnitude is a normal number (or non-finite), with p <= 52:
+// |x 2^s| is then a right shift of the 53-bit significand M by
+// d = (d0 = 1075 - s) - max(E, 1) >= 1, rounded half to even as
+// (M + 2^(d-1) - 1 + bit_d(M)) >> d; d is capped at 54, where every M < 2^53
+// gives 0.  Non-finite elements give an unspecified value (they set the
 // non-finite flag elsewhere).
 __device__ __forceinline__ uint64_t offset_integer_fast(uint64_t bits, int d0, uint64_t off) {
   const uint32_t hi = static_cast<uint32_t>(bits >> 32), lo = static_cast<uint32_t>(bits);
-  const uint32_t E = (hi >> 20) & 0x7FFu;
-  const uint32_t mhi = (hi & 0xFFFFFu) | (E ? 0x100000u : 0u);
-  int d = d0 - static_cast<int>(E > 1u ? E : 1u);
-  d = d < 1 ? 1 : (d > 63 ? 63 : d);
+  const uint32_t ah = hi & 0x7FFFFFFFu;
+  const uint32_t e20 = max(ah & 0x7FF00000u, 0x00100000u);  // max(E, 1) << 20
+  const uint32_t mhi = ah + 0x00100000u - e20;              // M's high word: implicit bit for normals
+  const int d = min(d0 - static_cast<int>(e20 >> 20), 54);
   const uint64_t M = (static_cast<uint64_t>(mhi) << 32) | lo;
   const uint64_t q = (M + ((1ull << (d - 1)) - 1ull) + ((M >> d) & 1ull)) >> d;
   const uint64_t neg = static_cast<uint64_t>(static_cast<long long>(static_cast<int>(hi) >> 31));  // 0 or ~0

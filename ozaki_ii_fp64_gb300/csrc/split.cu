@@ -8,6 +8,7 @@
 //
 // All fp64 handling is integer bit manipulation: no fp64 arithmetic.
 #include <cstdint>
+#include <utility>
 
 #include "common.cuh"
 #include "deconstruct.cuh"
@@ -17,10 +18,15 @@ namespace ozemu {
 
 namespace {
 
-constexpr int kSplitThreads = 256;
+constexpr int kSplitThreads = 512;
 constexpr int kElemsPerThread = 8;
 constexpr int kChunk = kSplitThreads * kElemsPerThread;  // elements of a row per pass step
-constexpr int kLutStride = 512;                          // u32 entries per modulus (>= 2 m)
+// Code table: 256 rows (b + 128 for a balanced residue b) of 32 copies of the
+// code, word i of a row in bank i.
+constexpr int kTableRowShift = 7;
+constexpr int kTableRowBytes = 1 << kTableRowShift;
+constexpr int kTableWords = 256 * kTableRowBytes / 4;
+constexpr int kSplitBlocksPerSM = 2;  // 64 registers x 512 threads; 33 KiB of shared memory each
 
 // Smallest-magnitude member of S = {0,+-1,+-2,+-3,+-4,+-6,+-8,+-12} in the
 // class c mod 13 (c in [0, 13)).  Classes 1 and 12 take 1 and -1.
@@ -60,10 +66,9 @@ __device__ uint32_t limb_code(int x) {
 // Packs 8 limb codes (nibbles in bytes 0..2) into the three plane words:
 // word j holds limb j of elements 0..7, element e in nibble e.
 __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint32_t& w1, uint32_t& w2) {
-  uint32_t p01 = c[0] | (c[1] << 4);
-  uint32_t p23 = c[2] | (c[3] << 4);
-  uint32_t p45 = c[4] | (c[5] << 4);
-  uint32_t p67 = c[6] | (c[7] << 4);
+  // The nibbles of a pair never overlap: c + (c' << 4) is their bitwise or.
+  const uint32_t p01 = c[0] + (c[1] << 4), p23 = c[2] + (c[3] << 4);
+  const uint32_t p45 = c[4] + (c[5] << 4), p67 = c[6] + (c[7] << 4);
   uint32_t lo = __byte_perm(p01, p23, 0x5140);
   uint32_t hi = __byte_perm(p45, p67, 0x5140);
   w0 = __byte_perm(lo, hi, 0x5410);
@@ -73,73 +78,207 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
   w2 = __byte_perm(ulo, uhi, 0x5410);
 }
 
+// ---------------------------------------------------------------- residues
+// An element's integer A' goes in as u = A' + 2^63 (0 <= u < 2^64), taken as
+// its eight bytes: u = sum_i byte_i 2^(8i).  For modulus m, two 4-way byte dot
+// products with the weights 2^(8i) mod m (each < 256) and an accumulator
+// bias give v = u + bias < 2^20 with v = A' + h (mod m), h = floor(m/2).  The
+// quotient floor(v/m) comes from one fp32 fma rounded down: v and 2^23 are
+// exact in fp32, 1/m is taken rounded up (c = ceil(2^31/m) 2^-31), and
+// v c - v/m < 2^-11 < 1/m, so rd(v c + 2^23) = 2^23 + floor(v/m) exactly; its
+// bit pattern is 0x4B000000 + floor(v/m).  Then w = v - m floor(v/m) is
+// (A' + h) mod m and b = w - h is the balanced residue, in [-h, m - 1 - h] as
+// the method takes it.  The codes of b come from one table shared by every
+// modulus, indexed by b + 128.
+__host__ __device__ constexpr uint32_t pow2_mod(int e, uint32_t m) {
+  uint64_t r = 1 % m;
+  for (int i = 0; i < e; ++i) r = r * 2 % m;
+  return static_cast<uint32_t>(r);
+}
+
+struct ResidueStep {
+  uint32_t m, clo, chi, bias, row;
+  float inv_up;
+};
+
+__host__ __device__ constexpr ResidueStep residue_step(int l) {
+  const uint32_t m = kModulusTable[l], h = m >> 1;
+  ResidueStep st{m, 0u, 0u, 0u, 0u, 0.0f};
+  for (int i = 0; i < 4; ++i) {
+    st.clo |= pow2_mod(8 * i, m) << (8 * i);
+    st.chi |= pow2_mod(32 + 8 * i, m) << (8 * i);
+  }
+  st.bias = (h + m - pow2_mod(63, m)) % m;
+  st.row = 128u - h;  // table row of b = -h
+  // ceil(2^31 / m) < 2^24 for 128 < m < 256: exact in fp32.
+  st.inv_up = static_cast<float>((((1ull << 31) + m - 1) / m)) / 2147483648.0f;
+  return st;
+}
+
+// The per-modulus constants in the constant bank (operands of the dot
+// products and the fma), with the dot-product bias carrying 0x4B000000.
+__host__ __device__ constexpr ResidueStep residue_step_biased(int l) {
+  ResidueStep st = residue_step(l);
+  st.bias += 0x4B000000u;
+  return st;
+}
+__constant__ ResidueStep kSteps[kMaxModuli] = {
+    residue_step_biased(0),  residue_step_biased(1),  residue_step_biased(2),  residue_step_biased(3),
+    residue_step_biased(4),  residue_step_biased(5),  residue_step_biased(6),  residue_step_biased(7),
+    residue_step_biased(8),  residue_step_biased(9),  residue_step_biased(10), residue_step_biased(11),
+    residue_step_biased(12), residue_step_biased(13), residue_step_biased(14), residue_step_biased(15)};
+
+// Byte offset of this lane's table word for the balanced residue of A'
+// modulo modulus L, relative to the table row of b = -h.  A table row is 128
+// bytes: lane i's copy of the code at bytes 4i (bank i).  lane_hi =
+// (4 lane) << 25: the funnel shift puts w at bit 7 and the lane's word at bits
+// 2..6.  With the fp32 quotient,
+// vb - m (0x4B000000 + floor(v/m)) = w + 0x4B000000 (1 - m) (mod 2^32), and
+// for odd m, 0x4B000000 (1 - m) 2^7 = 0 (mod 2^32), so the shifted value is
+// w's (m = 256 takes the low byte directly).
+template <int L>
+__device__ __forceinline__ uint32_t residue_offset(uint32_t ulo, uint32_t uhi, uint32_t lane_hi) {
+  constexpr ResidueStep st = residue_step(L);
+  uint32_t w;
+  if constexpr (st.m == 256u) {
+    w = (ulo & 0xFFu) ^ 0x80u;  // 2^63 = 0 (mod 256): b is the low byte of A', signed
+  } else {
+    // vb = 0x4B000000 + v: the fp32 pattern of 2^23 + v (v < 2^23).
+    const uint32_t vb = __dp4a(ulo, kSteps[L].clo, __dp4a(uhi, kSteps[L].chi, kSteps[L].bias));
+    const float vf = __uint_as_float(vb) - 8388608.0f;
+    const uint32_t qb = __float_as_uint(__fmaf_rd(vf, kSteps[L].inv_up, 8388608.0f));
+    w = vb - qb * st.m;
+  }
+  return __funnelshift_l(lane_hi, w, kTableRowShift);
+}
+
+// Codes of 8 elements for modulus L, packed and stored.  Lane i reads bank i
+// only, so a warp's lookups never conflict.
+template <int L, bool kRes8>
+__device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const uint32_t (&uhi)[8], const char* tb,
+                                              uint32_t lane_hi, uint32_t* o, long long plane_words) {
+  constexpr uint32_t kRow0 = residue_step(L).row * kTableRowBytes;
+  const char* t0 = tb + kRow0;
+  uint32_t c[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    c[e] = *reinterpret_cast<const uint32_t*>(t0 + residue_offset<L>(ulo[e], uhi[e], lane_hi));
+  }
+  if constexpr (kRes8) {
+    uint2 w;
+    w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+    w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+    __stcs(reinterpret_cast<uint2*>(o + L * plane_words), w);
+  } else {
+    uint32_t w0, w1, w2;
+    pack8(c, w0, w1, w2);
+    uint32_t* p = o + 3 * L * plane_words;
+    __stcs(p, w0);
+    __stcs(p + plane_words, w1);
+    __stcs(p + 2 * plane_words, w2);
+  }
+}
+
+template <bool kRes8, int... Ls>
+__device__ __forceinline__ void all_moduli(std::integer_sequence<int, Ls...>, const uint32_t (&ulo)[8],
+                                           const uint32_t (&uhi)[8], const char* tb, uint32_t lane_hi, uint32_t* o,
+                                           long long plane_words) {
+  (modulus_codes<Ls, kRes8>(ulo, uhi, tb, lane_hi, o, plane_words), ...);
+}
+
 // Pass 2 of the row split over the row's elements: integers, residues and
 // limb codes (or residue bytes), packed and stored.
 template <int R, bool kRes8, bool kFast>
-__device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s,
-                                            const SplitModuli& mods, const uint32_t* lut, uint8_t* out_row,
-                                            long long plane_stride) {
+__device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s, const char* tb,
+                                            uint32_t lane_hi, uint8_t* out_row, long long plane_words) {
   for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
     uint64_t b[8];
     load8_f64(rowp, k, k0, vec_ok, b, true);
-    uint32_t a2[8], a1[8], a0x4[8];
+    uint32_t ulo[8], uhi[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const uint64_t u = kFast ? offset_integer_fast(b[e], 1075 - s, 1ull << 62) : scaled_offset(b[e], s);
-      a0x4[e] = (static_cast<uint32_t>(u) & 0x1FFFFFu) << 2;
-      a1[e] = static_cast<uint32_t>(u >> 21) & 0x1FFFFFu;
-      a2[e] = static_cast<uint32_t>(u >> 42);
+      const uint64_t u =
+          kFast ? offset_integer_fast(b[e], 1075 - s, 1ull << 63) : scaled_offset(b[e], s) + (1ull << 62);
+      ulo[e] = static_cast<uint32_t>(u);
+      uhi[e] = static_cast<uint32_t>(u >> 32);
     }
     uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : k0 / 2));
-#pragma unroll
-    for (int l = 0; l < R; ++l) {
-      const uint32_t c21 = mods.c21x4[l], c42 = mods.c42x4[l], mg = mods.magic4[l], m4 = mods.m[l] * 4u;
-      const char* lt = reinterpret_cast<const char*>(lut + l * kLutStride);
-      uint32_t c[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        uint32_t v4 = a2[e] * c42 + (a1[e] * c21 + a0x4[e]);
-        uint32_t q = __umulhi(v4, mg);
-        uint32_t off = v4 - q * m4;
-        c[e] = *reinterpret_cast<const uint32_t*>(lt + off);
-      }
-      if constexpr (kRes8) {
-        uint2 w;
-        w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-        w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-        __stcs(reinterpret_cast<uint2*>(o + static_cast<long long>(l) * plane_stride / 4), w);
-      } else {
-        uint32_t w0, w1, w2;
-        pack8(c, w0, w1, w2);
-        const long long pl = static_cast<long long>(l * 3) * plane_stride / 4;
-        __stcs(o + pl, w0);
-        __stcs(o + pl + plane_stride / 4, w1);
-        __stcs(o + pl + 2 * plane_stride / 4, w2);
-      }
-    }
+    all_moduli<kRes8>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, plane_words);
   }
+}
+
+// Largest (high word & 0x7FFFFFFF) over a row: the high word of the largest
+// magnitude.  With 32-byte rows each load instruction of a warp covers 1 KiB
+// of consecutive addresses, four of them in flight per thread.
+__device__ __forceinline__ uint32_t row_max_hi(const double* rowp, int k, int vec) {
+  uint32_t mh = 0;
+  if (vec == 2) {
+    constexpr int kStep = kSplitThreads * 4;
+    int k0 = threadIdx.x * 4;
+    for (; k0 + 3 * kStep + 4 <= k; k0 += 4 * kStep) {
+      uint32_t h[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        unsigned long long x0, x1, x2, x3;
+        asm volatile("ld.global.nc.v4.u64 {%0, %1, %2, %3}, [%4];"
+                     : "=l"(x0), "=l"(x1), "=l"(x2), "=l"(x3)
+                     : "l"(rowp + k0 + q * kStep));
+        h[4 * q] = static_cast<uint32_t>(x0 >> 32);
+        h[4 * q + 1] = static_cast<uint32_t>(x1 >> 32);
+        h[4 * q + 2] = static_cast<uint32_t>(x2 >> 32);
+        h[4 * q + 3] = static_cast<uint32_t>(x3 >> 32);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) mh = __vimax3_u32(mh, h[i] & 0x7FFFFFFFu, h[i + 1] & 0x7FFFFFFFu);
+    }
+    for (; k0 + 4 <= k; k0 += kStep) {
+      unsigned long long x0, x1, x2, x3;
+      asm volatile("ld.global.nc.v4.u64 {%0, %1, %2, %3}, [%4];"
+                   : "=l"(x0), "=l"(x1), "=l"(x2), "=l"(x3)
+                   : "l"(rowp + k0));
+      mh = __vimax3_u32(mh, static_cast<uint32_t>(x0 >> 32) & 0x7FFFFFFFu, static_cast<uint32_t>(x1 >> 32) & 0x7FFFFFFFu);
+      mh = __vimax3_u32(mh, static_cast<uint32_t>(x2 >> 32) & 0x7FFFFFFFu, static_cast<uint32_t>(x3 >> 32) & 0x7FFFFFFFu);
+    }
+    for (; k0 < k; ++k0) mh = max(mh, static_cast<uint32_t>(__double_as_longlong(rowp[k0]) >> 32) & 0x7FFFFFFFu);
+  } else {
+    for (int i = threadIdx.x; i < k; i += kSplitThreads)
+      mh = max(mh, static_cast<uint32_t>(__double_as_longlong(rowp[i]) >> 32) & 0x7FFFFFFFu);
+  }
+  return mh;
+}
+
+template <int kThreads>
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
+  v = __reduce_max_sync(0xFFFFFFFFu, v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t m = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) m = max(m, red[w]);
+  return m;
 }
 
 // kRes8 = false: FP4 limb planes [r][3][rows_p][k_p/2] (the FP4 path).
 // kRes8 = true: the balanced residues themselves as int8 [r][rows_p][k_p]
 // (input of the INT8 comparison GEMM).
 template <int R, bool kRes8>
-__global__ void __launch_bounds__(kSplitThreads, 3)
+__global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     split_rows_f64_kernel(const double* __restrict__ X, long long ldx, int rows, int k, int rows_p, int k_p, int p,
-                          SplitModuli mods, uint8_t* __restrict__ planes, int32_t* __restrict__ shifts,
-                          uint32_t* flags) {
-  extern __shared__ __align__(16) uint32_t lut[];  // [R][kLutStride]
-  __shared__ uint64_t red[kSplitThreads / 32];
-  constexpr int r = R;
-  for (int l = 0; l < r; ++l) {
-    const uint32_t m = mods.m[l];
-    for (uint32_t i = threadIdx.x; i < 2 * m; i += kSplitThreads) {
-      uint32_t res = (i + m - mods.off[l]) % m;  // residue of x' = u - 2^62
-      int bal = static_cast<int>(res) - (res > (m - 1) / 2 ? static_cast<int>(m) : 0);
-      lut[l * kLutStride + i] = kRes8 ? static_cast<uint32_t>(static_cast<uint8_t>(bal)) : limb_code(bal);
-    }
-  }
+                          uint8_t* __restrict__ planes, int32_t* __restrict__ shifts, uint32_t* flags) {
+  // Code table: row j = 32 copies of the codes (or residue byte) of
+  // b = j - 128, word i read by lane i; then 256 words of staging.
+  extern __shared__ __align__(16) uint32_t tbl[];
+  __shared__ uint32_t red[kSplitThreads / 32];
+  uint32_t* stage = tbl + kTableWords;
+  for (int i = threadIdx.x; i < 256; i += kSplitThreads)
+    stage[i] = kRes8 ? static_cast<uint32_t>(static_cast<uint8_t>(i - 128)) : limb_code(i - 128);
   __syncthreads();
+  for (int w = threadIdx.x; w < kTableWords; w += kSplitThreads)
+    tbl[w] = stage[w >> (kTableRowShift - 2)];
+  __syncthreads();
+  const char* tb = reinterpret_cast<const char*>(tbl);
+  const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);  // (4 lane) << 25
 
   const long long row_bytes = kRes8 ? k_p : k_p / 2;
   const long long plane_stride = static_cast<long long>(rows_p) * row_bytes;
@@ -149,7 +288,7 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
   for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
     uint8_t* out_row = planes + static_cast<long long>(row) * row_bytes;
     if (row >= rows) {  // padding row: digit (or residue) 0 everywhere
-      for (int l = 0; l < r; ++l)
+      for (int l = 0; l < R; ++l)
         for (int j = 0; j < kPlanesPerModulus; ++j) {
           uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (l * kPlanesPerModulus + j) * plane_stride);
           for (int w = threadIdx.x; w < row_bytes / 4; w += kSplitThreads) o[w] = 0u;
@@ -158,29 +297,38 @@ __global__ void __launch_bounds__(kSplitThreads, 3)
     }
     const double* rowp = X + static_cast<long long>(row) * ldx;
 
-    // Pass 1: largest magnitude of the row (as an ordered bit pattern).
-    uint64_t mx = 0;
-    for (int k0 = threadIdx.x * kElemsPerThread; k0 < k; k0 += kChunk) {
-      uint64_t b[8];
-      load8_f64(rowp, k, k0, vec_ok, b, false);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        uint64_t a = b[e] & 0x7FFFFFFFFFFFFFFFull;
-        mx = a > mx ? a : mx;
-      }
-    }
-    mx = block_max_u64<kSplitThreads>(mx, red);
+    // Pass 1: exponent of the largest magnitude of the row.  The high words
+    // decide it unless every high word is zero (magnitudes below 2^-1042),
+    // when the low words are scanned too.
+    const uint32_t mh = block_max_u32<kSplitThreads>(row_max_hi(rowp, k, vec_ok), red);
     int s = 0;
-    if (mx != 0) s = p - frexp_exp_bits(mx);
-    if (mx >= 0x7FF0000000000000ull && threadIdx.x == 0) atomicOr(flags, kFlagNonFinite);
+    if (mh >= 0x00100000u) {
+      s = p - (static_cast<int>(mh >> 20) - 1022);
+    } else if (mh != 0) {
+      s = p - ((64 - __clz(static_cast<int>(mh))) - 1074);
+    } else {
+      uint32_t ml = 0;
+      for (int i = threadIdx.x; i < k; i += kSplitThreads)
+        ml = max(ml, static_cast<uint32_t>(__double_as_longlong(rowp[i])));
+      ml = block_max_u32<kSplitThreads>(ml, red);
+      if (ml != 0) s = p - ((32 - __clz(static_cast<int>(ml))) - 1074);
+    }
+    if (mh >= 0x7FF00000u && threadIdx.x == 0) atomicOr(flags, kFlagNonFinite);
     if (threadIdx.x == 0) shifts[row] = s;
+
+    // Bring this CTA's next row into L2 while this one is split.
+    if (row + static_cast<int>(gridDim.x) < rows) {
+      const double* nrow = rowp + static_cast<long long>(gridDim.x) * ldx;
+      for (int k0 = threadIdx.x * 16; k0 < k; k0 += kSplitThreads * 16)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + k0));
+    }
 
     // Pass 2: integers, residues, limbs.  Rows whose largest magnitude is
     // normal (with p <= 52) take the right-shift rounding.
-    if ((mx >> 52) != 0 && p <= 52)
-      split_pass2<R, kRes8, true>(rowp, k, k_p, vec_ok, s, mods, lut, out_row, plane_stride);
+    if (mh >= 0x00100000u && p <= 52)
+      split_pass2<R, kRes8, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, plane_stride / 4);
     else
-      split_pass2<R, kRes8, false>(rowp, k, k_p, vec_ok, s, mods, lut, out_row, plane_stride);
+      split_pass2<R, kRes8, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, plane_stride / 4);
   }
 }
 
@@ -241,22 +389,22 @@ int split_grid(int rows_p) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int g = sms * 3;  // three CTAs per SM fit (80 registers x 256 threads)
+  int g = sms * kSplitBlocksPerSM;  // resident CTAs per SM (registers and shared memory)
   return rows_p < g ? rows_p : g;
 }
 
 }  // namespace
 
 template <int R, bool kRes8>
-cudaError_t launch_split_r(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
-                           uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+cudaError_t launch_split_r(const double* X, long long ldx, int rows, int k, int p, uint8_t* planes, int32_t* shifts,
+                           uint32_t* flags, cudaStream_t stream) {
   const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
-  const size_t smem = static_cast<size_t>(R) * kLutStride * sizeof(uint32_t);
+  const size_t smem = static_cast<size_t>(kTableWords + 256) * sizeof(uint32_t);
   cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R, kRes8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   split_rows_f64_kernel<R, kRes8><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p,
-                                                                                       p, mods, planes, shifts, flags);
+                                                                                       p, planes, shifts, flags);
   return cudaGetLastError();
 }
 
@@ -266,7 +414,7 @@ cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, i
   switch (mods.r) {
 #define OZEMU_SPLIT_CASE(R) \
   case R:                   \
-    return launch_split_r<R, kRes8>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream);
+    return launch_split_r<R, kRes8>(X, ldx, rows, k, p, planes, shifts, flags, stream);
     OZEMU_SPLIT_CASE(1) OZEMU_SPLIT_CASE(2) OZEMU_SPLIT_CASE(3) OZEMU_SPLIT_CASE(4) OZEMU_SPLIT_CASE(5)
     OZEMU_SPLIT_CASE(6) OZEMU_SPLIT_CASE(7) OZEMU_SPLIT_CASE(8) OZEMU_SPLIT_CASE(9) OZEMU_SPLIT_CASE(10)
     OZEMU_SPLIT_CASE(11) OZEMU_SPLIT_CASE(12) OZEMU_SPLIT_CASE(13) OZEMU_SPLIT_CASE(14) OZEMU_SPLIT_CASE(15)
