@@ -366,15 +366,19 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   const int chunk = from_host ? (m >= 4096 ? round_up((m + 7) / 8, 256) : (m >= 2048 ? round_up((m + 3) / 4, 256) : m))
                               : (m >= 2048 ? round_up((m + 3) / 4, 256) : m);
   const int nch = (m + chunk - 1) / chunk;
+  // With host operands B comes over in blocks of columns, so that the first
+  // products start once its first block is in and split.
+  const int bcols = (from_host && n >= 4096) ? round_up((n + 1) / 2, 256) : n;
+  const int nbc = (n + bcols - 1) / bcols;
   const size_t szA = from_host ? align256(static_cast<size_t>(m) * k * 8) : 0;
   const size_t szB = from_host ? align256(static_cast<size_t>(k) * n * 8) : 0;
   const size_t szC = from_host ? align256(static_cast<size_t>(m) * n * 8) : 0;
-  const size_t szBt = align256(static_cast<size_t>(k) * n * 8);
-  const size_t szBp = align256(plane_bytes(n, k, r)), szSb = align256(static_cast<size_t>(n) * 4);
+  const size_t szBt = align256(static_cast<size_t>(k) * bcols * 8);
+  const size_t szBp = align256(plane_bytes(bcols, k, r)), szSb = align256(static_cast<size_t>(bcols) * 4);
   const size_t szAp = align256(plane_bytes(chunk, k, r)), szSa = align256(static_cast<size_t>(chunk) * 4);
-  const size_t szRes = align256(ozemu_residue_bytes(chunk, n, r));
+  const size_t szRes = align256(ozemu_residue_bytes(chunk, bcols, r));
   uint8_t* buf = nullptr;
-  s = workspace(d, szA + szB + szC + szBt + szBp + szSb + nch * (szAp + szSa + szRes), &buf);
+  s = workspace(d, szA + szB + szC + szBt + nbc * (szBp + szSb) + nch * (szAp + szSa + nbc * szRes), &buf);
   if (s != OZEMU_OK) return s;
   // Operands on the device: copies in the workspace, or the caller's buffers.
   const double* Ad = from_host ? reinterpret_cast<const double*>(buf) : A;
@@ -382,23 +386,33 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   double* Cd = from_host ? reinterpret_cast<double*>(buf + szA + szB) : C;
   const long long ldad = from_host ? k : lda, ldbd = from_host ? n : ldb, ldcd = from_host ? n : ldc;
   double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
-  uint8_t* bp = buf + szA + szB + szC + szBt;
-  int32_t* sbp = reinterpret_cast<int32_t*>(bp + szBp);
-  uint8_t* per_chunk = bp + szBp + szSb;
+  uint8_t* per_bblock = buf + szA + szB + szC + szBt;           // [nbc] planes + shifts of B's column blocks
+  uint8_t* per_chunk = per_bblock + nbc * (szBp + szSb);       // [nch] planes + shifts of A's rows, residues
   cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
   cudaEvent_t* ev = d->ev;
-  const int evStart = 0, evB = 1, evA = 2, evG = 2 + 8, evC = 2 + 16, evD = 2 + 24;
+  constexpr int evStart = 0, evB = 1, evA = 3, evG = 11, evC = 12, evD = 13;  // nbc <= 2, nch <= 8
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   const CrtModuli cm = crt_moduli(r);
+  auto bcol0 = [&](int j) { return j * bcols; };
+  auto bwidth = [&](int j) { return n - j * bcols < bcols ? n - j * bcols : bcols; };
+  auto bplanes = [&](int j) { return per_bblock + j * (szBp + szSb); };
+  auto bshifts = [&](int j) { return reinterpret_cast<int32_t*>(per_bblock + j * (szBp + szSb) + szBp); };
+  auto copy_b = [&](int j) {
+    return cudaMemcpy2DAsync(const_cast<double*>(Bd) + bcol0(j), static_cast<size_t>(n) * 8, B + bcol0(j),
+                             static_cast<size_t>(ldb) * 8, static_cast<size_t>(bwidth(j)) * 8, k, h2d, cs) ==
+                   cudaSuccess &&
+           cudaEventRecord(ev[evB + j], cs) == cudaSuccess;
+  };
+  auto split_b = [&](int j) -> int {
+    if (from_host && cudaStreamWaitEvent(stream, ev[evB + j], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
+    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), Bt, d, stream);
+  };
   if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
       cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
     return OZEMU_ERR_CUDA;
-  if (from_host) {
-    if (cudaMemcpy2DAsync(const_cast<double*>(Bd), n * 8, B, static_cast<size_t>(ldb) * 8,
-                          static_cast<size_t>(n) * 8, k, h2d, cs) != cudaSuccess ||
-        cudaEventRecord(ev[evB], cs) != cudaSuccess || cudaStreamWaitEvent(stream, ev[evB], 0) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
-  }
+  // Copy stream: B's first block, A's first rows, B's other blocks, A's other
+  // rows (device operands: the splits of A's rows).
+  if (from_host && !copy_b(0)) return OZEMU_ERR_CUDA;
   for (int c = 0; c < nch; ++c) {
     const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
     if (from_host) {
@@ -407,36 +421,50 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
                             static_cast<size_t>(k) * 8, mc, h2d, cs) != cudaSuccess)
         return OZEMU_ERR_CUDA;
     } else {
-      uint8_t* ap = per_chunk + c * (szAp + szSa + szRes);
+      uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
       s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, reinterpret_cast<int32_t*>(ap + szAp), d, cs);
       if (s != OZEMU_OK) return s;
     }
     if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
+    if (c == 0 && from_host)
+      for (int j = 1; j < nbc; ++j)
+        if (!copy_b(j)) return OZEMU_ERR_CUDA;
   }
-  s = split_cols_f64(k, n, Bd, ldbd, pb_bits, r, bp, sbp, Bt, d, stream);
+  s = split_b(0);
   if (s != OZEMU_OK) return s;
   for (int c = 0; c < nch; ++c) {
     const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
-    uint8_t* ap = per_chunk + c * (szAp + szSa + szRes);
+    uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
     int32_t* sap = reinterpret_cast<int32_t*>(ap + szAp);
-    uint8_t* res = ap + szAp + szSa;
     if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
     if (from_host) {
       s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream);
       if (s != OZEMU_OK) return s;
     }
-    s = residue_gemm(mc, n, k, r, ap, bp, res, d, stream);
-    if (s != OZEMU_OK) return s;
-    if (cudaEventRecord(ev[evG + c], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG + c], 0) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
-    if (launch_crt_f64(mc, n, res, round_up(n, 16), sap, sbp, Cd + row0 * ldcd, ldcd, cm, xs) != cudaSuccess ||
-        cudaEventRecord(ev[evC + c], xs) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
-    if (from_host) {
-      if (cudaStreamWaitEvent(cs, ev[evC + c], 0) != cudaSuccess ||
-          cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc, static_cast<size_t>(ldc) * 8, Cd + row0 * ldcd,
-                            n * 8, static_cast<size_t>(n) * 8, mc, d2h, cs) != cudaSuccess)
+    for (int j = 0; j < nbc; ++j) {
+      if (c == 0 && j > 0) {
+        s = split_b(j);
+        if (s != OZEMU_OK) return s;
+      }
+      const int col0 = bcol0(j), nc = bwidth(j);
+      uint8_t* res = ap + szAp + szSa + j * szRes;
+      s = residue_gemm(mc, nc, k, r, ap, bplanes(j), res, d, stream);
+      if (s != OZEMU_OK) return s;
+      // One event each for the product -> CRT and CRT -> copy hand-offs: each
+      // record is waited on before the next one.
+      if (cudaEventRecord(ev[evG], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG], 0) != cudaSuccess)
         return OZEMU_ERR_CUDA;
+      if (launch_crt_f64(mc, nc, res, round_up(nc, 16), sap, bshifts(j), Cd + row0 * ldcd + col0, ldcd, cm, xs) !=
+              cudaSuccess ||
+          cudaEventRecord(ev[evC], xs) != cudaSuccess)
+        return OZEMU_ERR_CUDA;
+      if (from_host) {
+        if (cudaStreamWaitEvent(cs, ev[evC], 0) != cudaSuccess ||
+            cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc + col0, static_cast<size_t>(ldc) * 8,
+                              Cd + row0 * ldcd + col0, static_cast<size_t>(ldcd) * 8, static_cast<size_t>(nc) * 8, mc,
+                              d2h, cs) != cudaSuccess)
+          return OZEMU_ERR_CUDA;
+      }
     }
   }
   // The caller's stream completes only after the last CRT (or copy out).

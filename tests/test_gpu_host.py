@@ -2,9 +2,9 @@
 
 The result must equal the oracle's bit for bit (and ozemu_dgemm's) for
 pinned and pageable buffers, padded leading dimensions, row counts that
-split into ragged chunks, narrow B (the fused path), k = 0, and two calls in
-a row on one stream (the second must not overwrite the first's workspace
-while it is in use).
+split into ragged chunks, B wide enough to come over in column blocks,
+narrow B (the fused path), k = 0, and two calls in a row on one stream (the
+second must not overwrite the first's workspace while it is in use).
 """
 
 import numpy as np
@@ -43,6 +43,8 @@ def same_bits(x, y):
     (300, 250, 1000, 13, True),   # one chunk
     (700, 2, 900, 12, True),      # narrow B: the fused path
     (3000, 70, 9000, 12, True),   # chunked K inside each row chunk
+    (2100, 4500, 300, 13, True),  # B in two column blocks (ragged second block)
+    (4100, 4200, 200, 12, False), # eight row chunks x two column blocks, pageable
 ])
 def test_dgemm_host_matches_oracle(oz, m, n, k, r, pinned):
     A, B = make_pair(m, n, k, seed=m + 3 * n + k, dist="wide")
