@@ -441,6 +441,39 @@ def run_gpu(args):
             "stage_ms": {kk: round(v, 3) for kk, v in stage_ms.items()},
             "gpu_launches": launches_per_step * args.steps, "clocks": clk}
 
+    # The memory-bound stages alone (limb-plane path): median of repeated
+    # launches, each after a write of 256 MiB (more than L2), against the
+    # algorithmic bytes.  Deconstruction reads 8 B and writes 1.5 r B per input
+    # element (B's transpose is extra traffic of this implementation, not in
+    # the count); the CRT reads r B and writes 8 B per output.
+    if not narrow:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def median_ms(fn, reps=9):
+            ts = []
+            for _ in range(reps):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            return statistics.median(ts)
+
+        def mem_entry(name, fn, nbytes):
+            t = median_ms(fn)
+            gbs = nbytes / (t / 1e3) / 1e9
+            return {"kernel": name, "ms": round(t, 4), "algorithmic_bytes": int(nbytes), "achieved": round(gbs, 1),
+                    "peak": round(pk["hbm_gbs"], 1), "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4)}
+
+        line["memory_stages"] = {
+            "deconstruct_A": mem_entry("split_rows_f64_kernel", split_a, (8.0 + 1.5 * r) * m * k),
+            "deconstruct_B": mem_entry("transpose + split_rows_f64_kernel", split_b, (8.0 + 1.5 * r) * k * n),
+            "reconstruct": mem_entry("crt_kernel", crt, (r + 8.0) * m * n)}
+        del flush
+
     # The limb-plane path on the same narrow problem, for comparison.
     plane_stages = [("split_A", split_a), ("split_B", split_b), ("limb_gemm", limb_gemm), ("crt", crt)]
     if narrow:
