@@ -252,22 +252,25 @@ bool rows_ok(int rows, int r) {  // plane-row coordinates fit in int
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? OZEMU_OK : OZEMU_ERR_CUDA; }
 
 // ---------------------------------------------------------------- stages
+// plane_rows (0: the rows' own padded count) and b_rows_p below let a block
+// of rows (columns of B) live inside a taller plane stack.
 int split_rows_f64(int rows, int k, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, DeviceState* d, cudaStream_t st) {
-  return cuda_status(launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r), planes, shifts, d->flags, st));
+                   int32_t* shifts, DeviceState* d, cudaStream_t st, int plane_rows = 0) {
+  return cuda_status(
+      launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r), planes, shifts, d->flags, st, plane_rows));
 }
 
 int split_cols_f64(int k, int cols, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st) {
+                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st, int plane_rows = 0) {
   if (k > 0) {
     cudaError_t e = launch_transpose_f64(X, ldx, k, cols, scratch, k, st);
     if (e != cudaSuccess) return OZEMU_ERR_CUDA;
   }
-  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st);
+  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st, plane_rows);
 }
 
 int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* bp, uint8_t* res, DeviceState* d,
-                 cudaStream_t st) {
+                 cudaStream_t st, int b_rows_p = 0) {
   LimbGemmCall c;
   c.residue_mode = true;
   c.m = m;
@@ -281,6 +284,7 @@ int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* b
   c.c32 = nullptr;
   c.ldc = 0;
   c.kc_blocks = kchunk_blocks();
+  c.b_rows_p = b_rows_p;
   c.em = epi_moduli(r);
   c.flags = d->flags;
   return cuda_status(launch_limb_gemm(c, st));
@@ -359,13 +363,27 @@ int pipeline_state(DeviceState* d) {
 // instead.  The caller's stream completes after the last CRT (device) or
 // copy out (host); the helper streams start after everything the caller
 // queued before.
+constexpr int kMaxChunks = 8;
+
 int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc, int r,
                   int pa_bits, int pb_bits, bool from_host, DeviceState* d, cudaStream_t stream) {
   int s = pipeline_state(d);
   if (s != OZEMU_OK) return s;
-  const int chunk = from_host ? (m >= 4096 ? round_up((m + 7) / 8, 256) : (m >= 2048 ? round_up((m + 3) / 4, 256) : m))
-                              : (m >= 2048 ? round_up((m + 3) / 4, 256) : m);
-  const int nch = (m + chunk - 1) / chunk;
+  // Row chunks of A: up to four equal chunks; with host operands and
+  // m >= 4096 the first two are half as tall (m/8), so that the first
+  // products start early and the later ones run at full size.
+  int row0s[kMaxChunks + 1];
+  int nch = 0;
+  if (from_host && m >= 4096) {
+    const int base = round_up((m + 7) / 8, 256);
+    for (int row = 0; row < m; row += (nch < 2 ? base : 2 * base)) row0s[nch++] = row;
+  } else {
+    const int step = m >= 2048 ? round_up((m + 3) / 4, 256) : m;
+    for (int row = 0; row < m; row += step) row0s[nch++] = row;
+  }
+  row0s[nch] = m;
+  int chunk = 0;  // tallest chunk (sizes the per-chunk buffers)
+  for (int c = 0; c < nch; ++c) chunk = row0s[c + 1] - row0s[c] > chunk ? row0s[c + 1] - row0s[c] : chunk;
   // With host operands B comes over in blocks of columns, so that the first
   // products start once its first block is in and split.
   const int bcols = (from_host && n >= 4096) ? round_up((n + 1) / 2, 256) : n;
@@ -390,7 +408,7 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   uint8_t* per_chunk = per_bblock + nbc * (szBp + szSb);       // [nch] planes + shifts of A's rows, residues
   cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
   cudaEvent_t* ev = d->ev;
-  constexpr int evStart = 0, evB = 1, evA = 3, evG = 11, evC = 12, evD = 13;  // nbc <= 2, nch <= 8
+  constexpr int evStart = 0, evB = 1, evA = 3, evG = 3 + kMaxChunks, evC = evG + 1, evD = evC + 1;  // nbc <= 2
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   const CrtModuli cm = crt_moduli(r);
   auto bcol0 = [&](int j) { return j * bcols; };
@@ -410,11 +428,17 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
       cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
     return OZEMU_ERR_CUDA;
-  // Copy stream: B's first block, A's first rows, B's other blocks, A's other
-  // rows (device operands: the splits of A's rows).
+  // Copy stream: B's first block, the first nfirst row chunks of A, B's other
+  // block, A's other rows (device operands: the splits of A's rows).  The
+  // products of the first chunks with B's first block keep the GPU busy
+  // while B's second block comes over.
+  int nfirst = nch;  // chunks that cover at least half of A's rows
+  if (nbc > 1)
+    for (nfirst = 1; nfirst < nch && 2 * row0s[nfirst] < m; ++nfirst) {
+    }
   if (from_host && !copy_b(0)) return OZEMU_ERR_CUDA;
   for (int c = 0; c < nch; ++c) {
-    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
+    const int row0 = row0s[c], mc = row0s[c + 1] - row0;
     if (from_host) {
       if (cudaMemcpy2DAsync(const_cast<double*>(Ad) + static_cast<size_t>(row0) * k, k * 8,
                             A + static_cast<size_t>(row0) * lda, static_cast<size_t>(lda) * 8,
@@ -426,47 +450,58 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
       if (s != OZEMU_OK) return s;
     }
     if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
-    if (c == 0 && from_host)
+    if (c == nfirst - 1 && from_host)
       for (int j = 1; j < nbc; ++j)
         if (!copy_b(j)) return OZEMU_ERR_CUDA;
   }
-  s = split_b(0);
-  if (s != OZEMU_OK) return s;
-  for (int c = 0; c < nch; ++c) {
-    const int row0 = c * chunk, mc = m - row0 < chunk ? m - row0 : chunk;
+  // One (row chunk, column block) product, its CRT and its copy out.  A
+  // chunk's rows are split before its first product (block 0).
+  auto block = [&](int c, int j) -> int {
+    const int row0 = row0s[c], mc = row0s[c + 1] - row0;
     uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
     int32_t* sap = reinterpret_cast<int32_t*>(ap + szAp);
-    if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
-    if (from_host) {
-      s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream);
-      if (s != OZEMU_OK) return s;
-    }
-    for (int j = 0; j < nbc; ++j) {
-      if (c == 0 && j > 0) {
-        s = split_b(j);
-        if (s != OZEMU_OK) return s;
-      }
-      const int col0 = bcol0(j), nc = bwidth(j);
-      uint8_t* res = ap + szAp + szSa + j * szRes;
-      s = residue_gemm(mc, nc, k, r, ap, bplanes(j), res, d, stream);
-      if (s != OZEMU_OK) return s;
-      // One event each for the product -> CRT and CRT -> copy hand-offs: each
-      // record is waited on before the next one.
-      if (cudaEventRecord(ev[evG], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG], 0) != cudaSuccess)
-        return OZEMU_ERR_CUDA;
-      if (launch_crt_f64(mc, nc, res, round_up(nc, 16), sap, bshifts(j), Cd + row0 * ldcd + col0, ldcd, cm, xs) !=
-              cudaSuccess ||
-          cudaEventRecord(ev[evC], xs) != cudaSuccess)
-        return OZEMU_ERR_CUDA;
+    if (j == 0) {
+      if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
       if (from_host) {
-        if (cudaStreamWaitEvent(cs, ev[evC], 0) != cudaSuccess ||
-            cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc + col0, static_cast<size_t>(ldc) * 8,
-                              Cd + row0 * ldcd + col0, static_cast<size_t>(ldcd) * 8, static_cast<size_t>(nc) * 8, mc,
-                              d2h, cs) != cudaSuccess)
-          return OZEMU_ERR_CUDA;
+        const int st = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream);
+        if (st != OZEMU_OK) return st;
       }
     }
+    const int col0 = bcol0(j), nc = bwidth(j);
+    uint8_t* res = ap + szAp + szSa + j * szRes;
+    const int st = residue_gemm(mc, nc, k, r, ap, bplanes(j), res, d, stream);
+    if (st != OZEMU_OK) return st;
+    // One event each for the product -> CRT and CRT -> copy hand-offs: each
+    // record is waited on before the next one.
+    if (cudaEventRecord(ev[evG], stream) != cudaSuccess || cudaStreamWaitEvent(xs, ev[evG], 0) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (launch_crt_f64(mc, nc, res, round_up(nc, 16), sap, bshifts(j), Cd + row0 * ldcd + col0, ldcd, cm, xs) !=
+            cudaSuccess ||
+        cudaEventRecord(ev[evC], xs) != cudaSuccess)
+      return OZEMU_ERR_CUDA;
+    if (from_host) {
+      if (cudaStreamWaitEvent(cs, ev[evC], 0) != cudaSuccess ||
+          cudaMemcpy2DAsync(C + static_cast<size_t>(row0) * ldc + col0, static_cast<size_t>(ldc) * 8,
+                            Cd + row0 * ldcd + col0, static_cast<size_t>(ldcd) * 8, static_cast<size_t>(nc) * 8, mc,
+                            d2h, cs) != cudaSuccess)
+        return OZEMU_ERR_CUDA;
+    }
+    return OZEMU_OK;
+  };
+  // Products: the first chunks with B's first block, then with its other
+  // block, then the remaining chunks with both.
+  s = split_b(0);
+  if (s != OZEMU_OK) return s;
+  for (int c = 0; c < nfirst; ++c)
+    if ((s = block(c, 0)) != OZEMU_OK) return s;
+  for (int j = 1; j < nbc; ++j) {
+    if ((s = split_b(j)) != OZEMU_OK) return s;
+    for (int c = 0; c < nfirst; ++c)
+      if ((s = block(c, j)) != OZEMU_OK) return s;
   }
+  for (int c = nfirst; c < nch; ++c)
+    for (int j = 0; j < nbc; ++j)
+      if ((s = block(c, j)) != OZEMU_OK) return s;
   // The caller's stream completes only after the last CRT (or copy out).
   cudaStream_t last = from_host ? cs : xs;
   if (cudaEventRecord(ev[evD], last) != cudaSuccess || cudaStreamWaitEvent(stream, ev[evD], 0) != cudaSuccess)

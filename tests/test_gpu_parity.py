@@ -51,10 +51,16 @@ def special_matrix(rows, k, seed):
 
 # ---------------------------------------------------------------- splits
 
-@pytest.mark.parametrize("rows,k,p,r", [(300, 1000, 44, 13), (1, 1, 62, 16), (129, 257, 30, 5), (64, 8192, 44, 13)])
-def test_split_rows_f64_parity(oz, rows, k, p, r):
+# pad: extra columns of the device buffer, so that the row stride is k + pad
+# (k = 1000, pad = 2 gives 16-byte but not 32-byte row loads; pad = 1 single
+# elements).
+@pytest.mark.parametrize("rows,k,p,r,pad", [(300, 1000, 44, 13, 0), (1, 1, 62, 16, 0), (129, 257, 30, 5, 0),
+                                           (64, 8192, 44, 13, 0), (77, 1000, 44, 13, 2), (50, 3000, 40, 12, 1)])
+def test_split_rows_f64_parity(oz, rows, k, p, r, pad):
     A = special_matrix(rows, k, seed=rows + k)
-    planes, shifts = oz.split_rows_f64(to_dev(A), p, r)
+    Ad = torch.zeros((rows, k + pad), dtype=torch.float64, device=DEV)
+    Ad[:, :k] = to_dev(A)
+    planes, shifts = oz.split_rows_f64(Ad[:, :k], p, r)
     status_ok(oz)
     ref = oracle.deconstruct(A, p, r)
     assert (shifts.cpu().numpy() == ref["shift"]).all()
