@@ -252,25 +252,22 @@ bool rows_ok(int rows, int r) {  // plane-row coordinates fit in int
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? OZEMU_OK : OZEMU_ERR_CUDA; }
 
 // ---------------------------------------------------------------- stages
-// plane_rows (0: the rows' own padded count) and b_rows_p below let a block
-// of rows (columns of B) live inside a taller plane stack.
 int split_rows_f64(int rows, int k, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, DeviceState* d, cudaStream_t st, int plane_rows = 0) {
-  return cuda_status(
-      launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r), planes, shifts, d->flags, st, plane_rows));
+                   int32_t* shifts, DeviceState* d, cudaStream_t st) {
+  return cuda_status(launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r), planes, shifts, d->flags, st));
 }
 
 int split_cols_f64(int k, int cols, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st, int plane_rows = 0) {
+                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st) {
   if (k > 0) {
     cudaError_t e = launch_transpose_f64(X, ldx, k, cols, scratch, k, st);
     if (e != cudaSuccess) return OZEMU_ERR_CUDA;
   }
-  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st, plane_rows);
+  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st);
 }
 
 int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* bp, uint8_t* res, DeviceState* d,
-                 cudaStream_t st, int b_rows_p = 0) {
+                 cudaStream_t st) {
   LimbGemmCall c;
   c.residue_mode = true;
   c.m = m;
@@ -284,7 +281,6 @@ int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* b
   c.c32 = nullptr;
   c.ldc = 0;
   c.kc_blocks = kchunk_blocks();
-  c.b_rows_p = b_rows_p;
   c.em = epi_moduli(r);
   c.flags = d->flags;
   return cuda_status(launch_limb_gemm(c, st));

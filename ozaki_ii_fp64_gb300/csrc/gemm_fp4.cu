@@ -788,8 +788,7 @@ bool make_plane_map(CUtensorMap* map, const uint8_t* base, int k_p, long long to
 template <int BN, bool kResidue>
 cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   using Cf = Cfg<BN>;
-  const int rows_a_p = round_up(c.m, kRowAlign);
-  const int rows_b_p = c.b_rows_p > 0 ? c.b_rows_p : round_up(c.n, kRowAlign);
+  const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
   const int k_p = round_up(c.k, kKAlign);
   const int r = c.residue_mode ? c.r : 1;
   CUtensorMap ma, mb;
@@ -824,8 +823,7 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
 
 template <bool kInt>
 cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
-  const int rows_a_p = round_up(c.m, kRowAlign);
-  const int rows_b_p = c.b_rows_p > 0 ? c.b_rows_p : round_up(c.n, kRowAlign);
+  const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
   const int k_p = round_up(c.k, kKAlign);
   CUtensorMap ma, mb;
   if (!make_plane_map(&ma, c.a_planes, k_p, 3LL * c.r * rows_a_p, kBM)) return cudaErrorInvalidValue;

@@ -10,12 +10,9 @@ namespace ozemu {
 
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Deconstruction of the rows of X into limb planes (split.cu).  plane_rows:
-// rows between consecutive planes (0: round_up(rows, kRowAlign)); a larger
-// value writes these rows into a block of a taller plane stack.
+// Deconstruction of the rows of X into limb planes (split.cu).
 cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
-                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream,
-                                  int plane_rows = 0);
+                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream);
 cudaError_t launch_split_rows_f64_res8(const double* X, long long ldx, int rows, int k, int p,
                                        const SplitModuli& mods, int8_t* res8, int32_t* shifts, uint32_t* flags,
                                        cudaStream_t stream);
@@ -28,9 +25,7 @@ cudaError_t launch_transpose_s8(const int8_t* in, long long ldin, int rows, int 
 
 // FP4 limb GEMM (gemm_fp4.cu).  Residue mode writes uint8 [r][m][ldr]
 // residues; int mode (r = 1) writes int32 C32 with leading dimension ldc.
-// kc_blocks: 128-wide K blocks per exactly accumulated chunk.  b_rows_p:
-// rows between consecutive B planes (0: round_up(n, kRowAlign)), so that B
-// may be a block of columns inside a wider plane stack.
+// kc_blocks: 128-wide K blocks per exactly accumulated chunk.
 struct LimbGemmCall {
   bool residue_mode;
   int m, n, k, r;
@@ -41,7 +36,6 @@ struct LimbGemmCall {
   int32_t* c32;
   long long ldc;
   int kc_blocks;
-  int b_rows_p = 0;
   EpiModuli em;
   uint32_t* flags;
 };

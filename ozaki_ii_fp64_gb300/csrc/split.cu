@@ -265,8 +265,7 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
 template <int R, bool kRes8>
 __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     split_rows_f64_kernel(const double* __restrict__ X, long long ldx, int rows, int k, int rows_p, int k_p, int p,
-                          int plane_rows, uint8_t* __restrict__ planes, int32_t* __restrict__ shifts,
-                          uint32_t* flags) {
+                          uint8_t* __restrict__ planes, int32_t* __restrict__ shifts, uint32_t* flags) {
   // Code table: row j = 32 copies of the codes (or residue byte) of
   // b = j - 128, word i read by lane i; then 256 words of staging.
   extern __shared__ __align__(16) uint32_t tbl[];
@@ -282,7 +281,7 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
   const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);  // (4 lane) << 25
 
   const long long row_bytes = kRes8 ? k_p : k_p / 2;
-  const long long plane_stride = static_cast<long long>(plane_rows) * row_bytes;
+  const long long plane_stride = static_cast<long long>(rows_p) * row_bytes;
   constexpr int kPlanesPerModulus = kRes8 ? 1 : 3;
   const int vec_ok = row_vector_width(X, ldx);
 
@@ -398,27 +397,24 @@ int split_grid(int rows_p) {
 
 template <int R, bool kRes8>
 cudaError_t launch_split_r(const double* X, long long ldx, int rows, int k, int p, uint8_t* planes, int32_t* shifts,
-                           uint32_t* flags, cudaStream_t stream, int plane_rows) {
+                           uint32_t* flags, cudaStream_t stream) {
   const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
-  if (plane_rows <= 0) plane_rows = rows_p;
-  if (plane_rows < rows_p) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(kTableWords + 256) * sizeof(uint32_t);
   cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R, kRes8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  split_rows_f64_kernel<R, kRes8><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(
-      X, ldx, rows, k, rows_p, k_p, p, plane_rows, planes, shifts, flags);
+  split_rows_f64_kernel<R, kRes8><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p,
+                                                                                       p, planes, shifts, flags);
   return cudaGetLastError();
 }
 
 template <bool kRes8>
 cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
-                              uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream,
-                              int plane_rows) {
+                              uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
   switch (mods.r) {
 #define OZEMU_SPLIT_CASE(R) \
   case R:                   \
-    return launch_split_r<R, kRes8>(X, ldx, rows, k, p, planes, shifts, flags, stream, plane_rows);
+    return launch_split_r<R, kRes8>(X, ldx, rows, k, p, planes, shifts, flags, stream);
     OZEMU_SPLIT_CASE(1) OZEMU_SPLIT_CASE(2) OZEMU_SPLIT_CASE(3) OZEMU_SPLIT_CASE(4) OZEMU_SPLIT_CASE(5)
     OZEMU_SPLIT_CASE(6) OZEMU_SPLIT_CASE(7) OZEMU_SPLIT_CASE(8) OZEMU_SPLIT_CASE(9) OZEMU_SPLIT_CASE(10)
     OZEMU_SPLIT_CASE(11) OZEMU_SPLIT_CASE(12) OZEMU_SPLIT_CASE(13) OZEMU_SPLIT_CASE(14) OZEMU_SPLIT_CASE(15)
@@ -430,16 +426,14 @@ cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, i
 }
 
 cudaError_t launch_split_rows_f64(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
-                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream,
-                                  int plane_rows) {
-  return launch_split_mode<false>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream, plane_rows);
+                                  uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+  return launch_split_mode<false>(X, ldx, rows, k, p, mods, planes, shifts, flags, stream);
 }
 
 cudaError_t launch_split_rows_f64_res8(const double* X, long long ldx, int rows, int k, int p,
                                        const SplitModuli& mods, int8_t* res8, int32_t* shifts, uint32_t* flags,
                                        cudaStream_t stream) {
-  return launch_split_mode<true>(X, ldx, rows, k, p, mods, reinterpret_cast<uint8_t*>(res8), shifts, flags, stream,
-                                 0);
+  return launch_split_mode<true>(X, ldx, rows, k, p, mods, reinterpret_cast<uint8_t*>(res8), shifts, flags, stream);
 }
 
 cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k, uint8_t* planes,
