@@ -152,6 +152,8 @@ CrtModuli crt_moduli(int r) {
     const u128 Ml = M / m;
     const u128 W = Ml * inv_mod(static_cast<uint32_t>(Ml % m), m);  // < M
     for (int w = 0; w < 16; ++w) c.wb[l / 4][w] |= static_cast<uint32_t>((W >> (8 * w)) & 0xFF) << (8 * (l % 4));
+    if (l == r - 1)
+      for (int t = 0; t < 8; ++t) c.wl16[t] = static_cast<uint32_t>((W >> (16 * t)) & 0xFFFF);
   }
   for (int t = 0; t < 9; ++t) c.m16[t] = t < 8 ? static_cast<uint32_t>((M >> (16 * t)) & 0xFFFF) : 0u;
   int bits = 0;

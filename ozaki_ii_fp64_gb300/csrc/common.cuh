@@ -68,6 +68,7 @@ struct CrtModuli {
   uint32_t prefix[kMaxModuli][4];         // m_0 ... m_{l-1} as 128-bit little-endian words
   // Direct form: C' = sum_l c_l W_l - q M with W_l = (M/m_l) ((M/m_l)^-1 mod m_l).
   uint32_t wb[4][16];                     // byte w of W_{4q+i} at byte i of wb[q][w]
+  uint32_t wl16[8];                       // W_{r-1} in 16-bit limbs (a lone last modulus, r = 1 mod 4)
   uint32_t m16[9];                        // M in 16-bit limbs
   float gt[9];                            // 2^(16 t) / M
 };

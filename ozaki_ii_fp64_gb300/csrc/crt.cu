@@ -90,8 +90,7 @@ __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const ui
         T[t] = s0 + (s1 << 8);
         if (kLastByMad) {
           const uint32_t c_last = (word[R - 1] >> (8 * e)) & 0xFFu;
-          const uint32_t wl = (cm.wb[R / 4][2 * t] & 0xFFu) | ((2 * t + 1 < NL ? cm.wb[R / 4][2 * t + 1] & 0xFFu : 0u) << 8);
-          T[t] += c_last * wl;
+          T[t] += c_last * cm.wl16[t];
         }
       }
       // q = round(Y / M) from the three top partial sums.
