@@ -39,7 +39,7 @@ template <int R>
 __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const uint8_t* __restrict__ res,
                                                           long long ldr, const int32_t* __restrict__ sa,
                                                           const int32_t* __restrict__ sb, double* __restrict__ C,
-                                                          long long ldc, const CrtModuli cm) {
+                                                          long long ldc, const __grid_constant__ CrtModuli cm) {
   constexpr bool kLastByMad = (R % 4) == 1;   // a lone last modulus: multiply-adds, not dp4a
   constexpr int NQ = kLastByMad ? R / 4 : (R + 3) / 4;  // words of four residues through dp4a
   constexpr int BM = kCrtBits[R];             // bit length of M

@@ -27,8 +27,9 @@ __device__ __forceinline__ int clz128(u128 x) {
   return hi ? __clzll(static_cast<long long>(hi)) : 64 + __clzll(static_cast<long long>(lo));
 }
 
-// Bits of RN(X 2^-S) as an IEEE binary64.
-__device__ inline uint64_t round_scaled(i128 X, int S) {
+// Bits of RN(X 2^-S) as an IEEE binary64 (the rare subnormal-range path:
+// not inlined, so it does not widen the common path).
+__device__ __noinline__ uint64_t round_scaled(i128 X, int S) {
   if (X == 0) return 0ull;
   const bool neg = X < 0;
   u128 mag = neg ? static_cast<u128>(-X) : static_cast<u128>(X);
@@ -122,9 +123,10 @@ __device__ __forceinline__ void horner_step(uint32_t (&x)[L], uint32_t m, int v)
   }
 }
 
-// Bits of RN(C' 2^-S) for the residues c[0..R) (each in [0, m_l)).
+// Bits of RN(C' 2^-S) for the residues c[0..R) (each in [0, m_l)); the
+// CRT kernel's fallback, not inlined.
 template <int R>
-__device__ __forceinline__ uint64_t crt_round(const uint32_t (&c)[R], int S, const CrtModuli& cm) {
+__device__ __noinline__ uint64_t crt_round(const uint32_t (&c)[R], int S, const CrtModuli& cm) {
   constexpr int L = Limbs<R>::value;
   int v[R];
 #pragma unroll
