@@ -33,12 +33,13 @@
  *     low digits are the smallest-magnitude member of S in x's class mod 13.
  *
  * Limb-plane layout (written by the split calls, read by the GEMM calls)
- *   rows_p = round_up(rows, 128), k_p = round_up(k, 128), row_bytes = k_p/2.
- *   Plane (l, j) for modulus l (0-based) and limb j in {0,1,2} starts at byte
- *   ((l*3 + j) * rows_p) * row_bytes; row i of it at + i*row_bytes.  Element
- *   k of a row is the 4-bit FP4 e2m1 code of d/2 in byte k/2, low nibble for
- *   even k.  Padding rows and columns hold digit 0 (code 0).  INT8 planes are
- *   the same with a single "modulus" (3 planes).
+ *   rows_p = round_up(rows, 128), k_p = round_up(k, 128), row_bytes =
+ *   3 k_p/2.  Row i of modulus l (0-based) starts at byte
+ *   (l*rows_p + i) * row_bytes.  A row holds, for each 128-element K block
+ *   kb, the 64 bytes of limb 0, then of limb 1, then of limb 2: limb j of
+ *   element k is at row byte (3*(k/128) + j)*64 + (k%128)/2, the 4-bit FP4
+ *   e2m1 code of d_j/2, low nibble for even k.  Padding rows and columns hold
+ *   digit 0 (code 0).  INT8 planes are the same with a single "modulus".
  *   Total bytes: ozemu_plane_bytes(rows, k, r).
  *
  * Residue layout (written by ozemu_residue_gemm, read by ozemu_crt_f64)

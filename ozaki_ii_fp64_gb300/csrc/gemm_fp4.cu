@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < args.total_tiles && ok; t += gridDim.x) {
         int l, tm, tn;
         tile_coords(t, args, l, tm, tn);
-        const int a_row = l * 3 * args.rows_a_p + tm * kBM;
-        const int b_row = l * 3 * args.rows_b_p + tn * BN;
+        const int a_row = l * args.rows_a_p + tm * kBM;
+        const int b_row = l * args.rows_b_p + tn * BN;
         for (int kb = 0; kb < kb_total; ++kb, ++it) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
@@ -224,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], C::kStage);
 #pragma unroll
           for (int j = 0; j < 3; ++j)
-            tma_load_2d(st + j * kATile, &tmA, &full[s], kb * kBKBytes, a_row + j * args.rows_a_p);
+            tma_load_2d(st + j * kATile, &tmA, &full[s], (3 * kb + j) * kBKBytes, a_row);
 #pragma unroll
           for (int j = 0; j < 3; ++j)
-            tma_load_2d(st + 3 * kATile + j * C::kBTile, &tmB, &full[s], kb * kBKBytes, b_row + j * args.rows_b_p);
+            tma_load_2d(st + 3 * kATile + j * C::kBTile, &tmB, &full[s], (3 * kb + j) * kBKBytes, b_row);
         }
       }
       if (!ok) {
@@ -553,8 +553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int t = pair; t < args.total_tiles && ok; t += npairs) {
         int l, tm2, tn;
         pair_tile_coords(t, args, l, tm2, tn);
-        const int a_row = l * 3 * args.rows_a_p + tm2 * 256 + static_cast<int>(rank) * kBM;
-        const int b_row = l * 3 * args.rows_b_p + tn * kBN2 + static_cast<int>(rank) * kBHalf;
+        const int a_row = l * args.rows_a_p + tm2 * 256 + static_cast<int>(rank) * kBM;
+        const int b_row = l * args.rows_b_p + tn * kBN2 + static_cast<int>(rank) * kBHalf;
         for (int kb = 0; kb < kb_total; ++kb, ++it) {
           const int s = it % kStages2;
           const uint32_t ph = (it / kStages2) & 1;
@@ -572,11 +572,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStage2);
 #pragma unroll
           for (int j = 0; j < 3; ++j)
-            tma_load_2d_pair(st + j * kATile, &tmA, full_leader, kb * kBKBytes, a_row + j * args.rows_a_p);
+            tma_load_2d_pair(st + j * kATile, &tmA, full_leader, (3 * kb + j) * kBKBytes, a_row);
 #pragma unroll
           for (int j = 0; j < 3; ++j)
-            tma_load_2d_pair(st + 3 * kATile + j * kBTile2, &tmB, full_leader, kb * kBKBytes,
-                             b_row + j * args.rows_b_p);
+            tma_load_2d_pair(st + 3 * kATile + j * kBTile2, &tmB, full_leader, (3 * kb + j) * kBKBytes, b_row);
         }
       }
       if (!ok) settle_after_abort();
@@ -771,12 +770,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over a stack of limb planes: x = byte within a row, y = plane row.
+// 2-D map over the limb planes of r moduli: y = modulus l rows_p + row;
+// x = byte within the row, where the three limbs of 128-element K block kb
+// lie at x = (3 kb + j) 64.
 bool make_plane_map(CUtensorMap* map, const uint8_t* base, int k_p, long long total_rows, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_p / 2), static_cast<cuuint64_t>(total_rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(k_p / 2)};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(3LL * k_p / 2), static_cast<cuuint64_t>(total_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(3LL * k_p / 2)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
@@ -792,8 +793,8 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   const int k_p = round_up(c.k, kKAlign);
   const int r = c.residue_mode ? c.r : 1;
   CUtensorMap ma, mb;
-  if (!make_plane_map(&ma, c.a_planes, k_p, 3LL * r * rows_a_p, kBM)) return cudaErrorInvalidValue;
-  if (!make_plane_map(&mb, c.b_planes, k_p, 3LL * r * rows_b_p, BN)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&ma, c.a_planes, k_p, 1LL * r * rows_a_p, kBM)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&mb, c.b_planes, k_p, 1LL * r * rows_b_p, BN)) return cudaErrorInvalidValue;
   GemmArgs a;
   a.m = c.m;
   a.n = c.n;
@@ -826,8 +827,8 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
   const int k_p = round_up(c.k, kKAlign);
   CUtensorMap ma, mb;
-  if (!make_plane_map(&ma, c.a_planes, k_p, 3LL * c.r * rows_a_p, kBM)) return cudaErrorInvalidValue;
-  if (!make_plane_map(&mb, c.b_planes, k_p, 3LL * c.r * rows_b_p, kBHalf)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&ma, c.a_planes, k_p, 1LL * c.r * rows_a_p, kBM)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&mb, c.b_planes, k_p, 1LL * c.r * rows_b_p, kBHalf)) return cudaErrorInvalidValue;
   PairArgs a;
   a.m = c.m;
   a.n = c.n;

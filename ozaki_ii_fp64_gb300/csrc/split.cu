@@ -156,7 +156,7 @@ __device__ __forceinline__ uint32_t residue_offset(uint32_t ulo, uint32_t uhi, u
 // only, so a warp's lookups never conflict.
 template <int L, bool kRes8>
 __device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const uint32_t (&uhi)[8], const char* tb,
-                                              uint32_t lane_hi, uint32_t* o, long long plane_words) {
+                                              uint32_t lane_hi, uint32_t* o, long long modulus_words) {
   constexpr uint32_t kRow0 = residue_step(L).row * kTableRowBytes;
   const char* t0 = tb + kRow0;
   uint32_t c[8];
@@ -168,29 +168,30 @@ __device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const ui
     uint2 w;
     w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
     w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-    __stcs(reinterpret_cast<uint2*>(o + L * plane_words), w);
+    __stcs(reinterpret_cast<uint2*>(o + L * modulus_words), w);
   } else {
     uint32_t w0, w1, w2;
     pack8(c, w0, w1, w2);
-    uint32_t* p = o + 3 * L * plane_words;
+    // Limb j of a 128-element K block sits 64 j bytes after limb 0.
+    uint32_t* p = o + L * modulus_words;
     __stcs(p, w0);
-    __stcs(p + plane_words, w1);
-    __stcs(p + 2 * plane_words, w2);
+    __stcs(p + 16, w1);
+    __stcs(p + 32, w2);
   }
 }
 
 template <bool kRes8, int... Ls>
 __device__ __forceinline__ void all_moduli(std::integer_sequence<int, Ls...>, const uint32_t (&ulo)[8],
                                            const uint32_t (&uhi)[8], const char* tb, uint32_t lane_hi, uint32_t* o,
-                                           long long plane_words) {
-  (modulus_codes<Ls, kRes8>(ulo, uhi, tb, lane_hi, o, plane_words), ...);
+                                           long long modulus_words) {
+  (modulus_codes<Ls, kRes8>(ulo, uhi, tb, lane_hi, o, modulus_words), ...);
 }
 
 // Pass 2 of the row split over the row's elements: integers, residues and
 // limb codes (or residue bytes), packed and stored.
 template <int R, bool kRes8, bool kFast>
 __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s, const char* tb,
-                                            uint32_t lane_hi, uint8_t* out_row, long long plane_words) {
+                                            uint32_t lane_hi, uint8_t* out_row, long long modulus_words) {
   for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
     uint64_t b[8];
     load8_f64(rowp, k, k0, vec_ok, b, true);
@@ -202,8 +203,8 @@ __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, 
       ulo[e] = static_cast<uint32_t>(u);
       uhi[e] = static_cast<uint32_t>(u >> 32);
     }
-    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : k0 / 2));
-    all_moduli<kRes8>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, plane_words);
+    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : (k0 >> 7) * 192 + (k0 & 127) / 2));
+    all_moduli<kRes8>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_words);
   }
 }
 
@@ -280,17 +281,18 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
   const char* tb = reinterpret_cast<const char*>(tbl);
   const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);  // (4 lane) << 25
 
-  const long long row_bytes = kRes8 ? k_p : k_p / 2;
-  const long long plane_stride = static_cast<long long>(rows_p) * row_bytes;
-  constexpr int kPlanesPerModulus = kRes8 ? 1 : 3;
+  // FP4 planes: a row holds the three limbs of each 128-element K block
+  // side by side (3 x 64 bytes); moduli follow one another.
+  const long long row_bytes = kRes8 ? k_p : 3LL * k_p / 2;
+  const long long modulus_stride = static_cast<long long>(rows_p) * row_bytes;
   const int vec_ok = row_vector_width(X, ldx);
 
   for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
     uint8_t* out_row = planes + static_cast<long long>(row) * row_bytes;
     if (row >= rows) {  // padding row: digit (or residue) 0 everywhere
       for (int l = 0; l < R; ++l)
-        for (int j = 0; j < kPlanesPerModulus; ++j) {
-          uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (l * kPlanesPerModulus + j) * plane_stride);
+        {
+          uint32_t* o = reinterpret_cast<uint32_t*>(out_row + l * modulus_stride);
           for (int w = threadIdx.x; w < row_bytes / 4; w += kSplitThreads) o[w] = 0u;
         }
       continue;
@@ -326,9 +328,9 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     // Pass 2: integers, residues, limbs.  Rows whose largest magnitude is
     // normal (with p <= 52) take the right-shift rounding.
     if (mh >= 0x00100000u && p <= 52)
-      split_pass2<R, kRes8, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, plane_stride / 4);
+      split_pass2<R, kRes8, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
     else
-      split_pass2<R, kRes8, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, plane_stride / 4);
+      split_pass2<R, kRes8, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
   }
 }
 
@@ -338,8 +340,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_rows_s8_kernel(const int8
   __shared__ uint32_t lut[256];
   for (int i = threadIdx.x; i < 256; i += kSplitThreads) lut[i] = limb_code(i - 128);
   __syncthreads();
-  const long long row_bytes = k_p / 2;
-  const long long plane_words = static_cast<long long>(rows_p) * row_bytes / 4;
+  const long long row_bytes = 3LL * k_p / 2;  // the three limbs of each 128-element K block side by side
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(X) & 7u) == 0) && ((ldx & 7) == 0);
   for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
     uint32_t* o_row = reinterpret_cast<uint32_t*>(planes + static_cast<long long>(row) * row_bytes);
@@ -360,10 +361,10 @@ __global__ void __launch_bounds__(kSplitThreads) split_rows_s8_kernel(const int8
       for (int e = 0; e < 8; ++e) c[e] = lut[static_cast<int>(v[e]) + 128];
       uint32_t w0, w1, w2;
       pack8(c, w0, w1, w2);
-      uint32_t* o = o_row + k0 / 8;
+      uint32_t* o = o_row + (k0 >> 7) * 48 + (k0 & 127) / 8;
       o[0] = w0;
-      o[plane_words] = w1;
-      o[2 * plane_words] = w2;
+      o[16] = w1;
+      o[32] = w2;
     }
   }
 }

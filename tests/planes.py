@@ -17,7 +17,10 @@ def decode_planes(planes, rows, k, r):
     """uint8 plane bytes -> digits (r, 3, rows_p, k_p) as int64."""
     rows_p = (rows + 127) // 128 * 128
     k_p = (k + 127) // 128 * 128
-    b = np.asarray(planes, dtype=np.uint8).reshape(r, 3, rows_p, k_p // 2)
+    # [r][rows_p][k_p/128][3][64]: the three limbs of each 128-element K
+    # block side by side in a row.
+    b = np.asarray(planes, dtype=np.uint8).reshape(r, rows_p, k_p // 128, 3, 64)
+    b = b.transpose(0, 3, 1, 2, 4).reshape(r, 3, rows_p, k_p // 2)
     codes = np.empty((r, 3, rows_p, k_p), dtype=np.uint8)
     codes[..., 0::2] = b & 0xF
     codes[..., 1::2] = b >> 4
