@@ -22,7 +22,7 @@ with no independent pin say "parity unpinned".
 """
 
 from .ozaki2 import (  # noqa: F401
-    S, BASE, LIMB_WEIGHTS, N_LIMBS, MODULUS_CEILING,
+    S, BASE, LIMB_WEIGHTS, N_LIMBS, MODULUS_CEILING, MODULUS_CEILING_2LIMB,
     moduli, modulus_product, bit_budget, frexp_exponent, row_shifts,
     scale_round_scalar, scale_round, balanced_residue, balanced_residue_array,
     digit_of_class, limb_split, limb_table_int8, limb_digits,

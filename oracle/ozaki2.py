@@ -48,22 +48,27 @@ LIMB_WEIGHTS = (1, 13, 169)
 N_LIMBS = 3
 #: Largest modulus: keeps every balanced residue inside int8 (reading).
 MODULUS_CEILING = 256
+# Two-limb reading ([AWE] abstract: base-13 limbs from S; residues of moduli
+# up to 113 lie in [-56, 56], where the 3-limb split's top digit is always 0,
+# so 2 limbs and 2 x 2 = 4 FP4 products per modulus suffice).
+MODULUS_CEILING_2LIMB = 113
 
 
 # ----------------------------------------------------------------------------
 # Stage 0: moduli and bit budget (reading of [TME4] abstract; configs)
 # ----------------------------------------------------------------------------
 
-def moduli(r):
-    """First ``r`` greedy pairwise-coprime integers counting down from 256.
+def moduli(r, ceiling=MODULUS_CEILING):
+    """First ``r`` greedy pairwise-coprime integers counting down from
+    ``ceiling`` (256; 113 for the two-limb reading).
 
-    The sources name no moduli.  Reading: take each integer from 256 down
-    that is coprime to every modulus already taken.
+    The sources name no moduli.  Reading: take each integer from the ceiling
+    down that is coprime to every modulus already taken.
     """
     if r < 1:
         raise ValueError("r must be >= 1")
     out = []
-    m = MODULUS_CEILING
+    m = ceiling
     while len(out) < r:
         if m < 2:
             raise ValueError("ran out of moduli")
@@ -73,15 +78,15 @@ def moduli(r):
     return out
 
 
-def modulus_product(r):
+def modulus_product(r, ceiling=MODULUS_CEILING):
     """Product of the first ``r`` moduli, as a Python int."""
     prod = 1
-    for m in moduli(r):
+    for m in moduli(r, ceiling):
         prod *= m
     return prod
 
 
-def bit_budget(k, r):
+def bit_budget(k, r, ceiling=MODULUS_CEILING):
     """Return (P, p_A, p_B): P is the largest integer with 2 k 2^P < M.
 
     |A'| <= 2^p_A and |B'| <= 2^p_B then give |sum_k A'B'| <= k 2^P < M/2,
@@ -90,7 +95,7 @@ def bit_budget(k, r):
     """
     if k < 1:
         raise ValueError("k must be >= 1")
-    M = modulus_product(r)
+    M = modulus_product(r, ceiling)
     if not (2 * k * 1 < M):
         raise ValueError("modulus product too small for this k")
     P = 0
@@ -353,25 +358,26 @@ def scale_back_array(Cp, sA, sB):
 # Pipelines
 # ----------------------------------------------------------------------------
 
-def deconstruct(X, p, r):
+def deconstruct(X, p, r, ceiling=MODULUS_CEILING):
     """Stage 1 + 2 for the rows of X: shifts, integers, residues, limb digits.
 
     Returns dict(shift=(rows,), xint=(rows, k), res=(r, rows, k),
-    digits=(r, 3, rows, k)).
+    digits=(r, 3, rows, k)); with ceiling 113 the top digit is 0 throughout.
     """
     s = row_shifts(X, p)
     xi = scale_round(X, s)
-    mods = moduli(r)
+    mods = moduli(r, ceiling)
     res = np.stack([balanced_residue_array(xi, m) for m in mods]) if r else None
     digits = np.stack([limb_digits(res[l]) for l in range(r)])
     return dict(shift=s, xint=xi, res=res, digits=digits)
 
 
-def dgemm_block(A, B, r, rows=None, cols=None, stages=False):
+def dgemm_block(A, B, r, rows=None, cols=None, stages=False, ceiling=MODULUS_CEILING):
     """Emulated C[rows][:, cols] = A @ B by the four stages.
 
     ``rows`` / ``cols`` select a sub-block (default: all).  Row and column
-    exponents always see the full row / column.
+    exponents always see the full row / column.  ``ceiling`` 113 takes the
+    two-limb moduli (the same stages; the third limb is 0).
     """
     A = np.asarray(A, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
@@ -381,10 +387,10 @@ def dgemm_block(A, B, r, rows=None, cols=None, stages=False):
         raise ValueError("inner dimensions differ")
     rows = np.arange(M) if rows is None else np.asarray(rows)
     cols = np.arange(N) if cols is None else np.asarray(cols)
-    mods = moduli(r)
-    _, pA, pB = bit_budget(K, r)
-    da = deconstruct(A[rows], pA, r)
-    db = deconstruct(B[:, cols].T, pB, r)  # columns of B as rows
+    mods = moduli(r, ceiling)
+    _, pA, pB = bit_budget(K, r, ceiling)
+    da = deconstruct(A[rows], pA, r, ceiling)
+    db = deconstruct(B[:, cols].T, pB, r, ceiling)  # columns of B as rows
     res = np.zeros((r, len(rows), len(cols)), dtype=np.int64)
     for l, m in enumerate(mods):
         Ad = da["digits"][l]                       # (3, rows, K)
@@ -397,9 +403,9 @@ def dgemm_block(A, B, r, rows=None, cols=None, stages=False):
     return C
 
 
-def dgemm(A, B, r, stages=False):
+def dgemm(A, B, r, stages=False, ceiling=MODULUS_CEILING):
     """Emulated fp64 C = A @ B with r moduli (whole matrix)."""
-    return dgemm_block(A, B, r, stages=stages)
+    return dgemm_block(A, B, r, stages=stages, ceiling=ceiling)
 
 
 def igemm_s8(A, B):

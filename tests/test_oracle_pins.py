@@ -429,3 +429,56 @@ def test_scale_back_overflow_rounds_to_signed_inf():
     assert oracle.scale_back(-big, 0) == -math.inf
     assert oracle.scale_back(3, -1100) == math.inf
     assert oracle.scale_back(3, 1100) == 0.0
+
+
+# --------------------------------------------------------------------------
+# Two-limb reading: moduli up to 113, residues in [-56, 56], top digit 0
+# --------------------------------------------------------------------------
+
+def test_two_limb_range_is_pm56():
+    # Every integer of [-56, 56] splits with d2 = 0 (two limbs in S); 57 and
+    # -57 are the first that need the third limb.
+    for x in range(-56, 57):
+        d0, d1, d2 = oracle.limb_split(x)
+        assert d2 == 0 and d0 in oracle.S and d1 in oracle.S and d0 + 13 * d1 == x
+    assert oracle.limb_split(57)[2] != 0 and oracle.limb_split(-57)[2] != 0
+    # Brute force over all pairs of S: no wider symmetric interval is reachable.
+    reach = {a + 13 * b for a in oracle.S for b in oracle.S}
+    assert all(x in reach for x in range(-56, 57)) and 57 not in reach
+
+
+def test_two_limb_moduli_greedy_and_residue_range():
+    mods = oracle.moduli(16, oracle.MODULUS_CEILING_2LIMB)
+    assert mods[0] == 113 and 2 * (113 // 2) + 1 == 113
+    for i, m in enumerate(mods):
+        for j in range(i):
+            assert math.gcd(m, mods[j]) == 1
+        lo, hi = m + 1, (mods[i - 1] - 1 if i else 113)
+        for c in range(lo, hi + 1):
+            assert any(math.gcd(c, mods[j]) != 1 for j in range(i))
+        bal = oracle.balanced_residue_array(np.arange(-3 * m, 3 * m), m)
+        assert bal.min() >= -56 and bal.max() <= 56
+        assert ((bal - np.arange(-3 * m, 3 * m)) % m == 0).all()
+
+
+def test_two_limb_deconstruct_has_zero_top_digit():
+    A, _ = make_pair(9, 1, 200, seed=38, dist="wide")
+    _, pA, _ = oracle.bit_budget(200, 16, oracle.MODULUS_CEILING_2LIMB)
+    d = oracle.deconstruct(A, pA, 16, oracle.MODULUS_CEILING_2LIMB)
+    assert (d["digits"][:, 2] == 0).all()
+    assert (d["digits"][:, 0] + 13 * d["digits"][:, 1] == d["res"]).all()
+
+
+def test_two_limb_crt_recovers_integer_product_and_bound():
+    A, B = make_pair(6, 5, 33, seed=39, dist="uniform")
+    C, st = oracle.dgemm(A, B, 16, stages=True, ceiling=oracle.MODULUS_CEILING_2LIMB)
+    exact_int = st["a"]["xint"].astype(object) @ st["b"]["xint"].T.astype(object)
+    assert (st["Cp"] == exact_int).all()
+    # Bits per modulus are fewer (6.8 against 8): at K = 256 on wide-range
+    # data 17 two-limb moduli (P = 100) meet the bound as 14 of the 3-limb
+    # list (P = 101) do; 16 (P = 94) do not, like 13 of the 3-limb list.
+    A, B = make_pair(24, 20, 256, seed=35, dist="wide")
+    C = oracle.dgemm(A, B, 17, ceiling=oracle.MODULUS_CEILING_2LIMB)
+    assert oracle.error_bound_ratio(A, B, C) <= 1.0
+    C = oracle.dgemm(A, B, 16, ceiling=oracle.MODULUS_CEILING_2LIMB)
+    assert oracle.error_bound_ratio(A, B, C) > 1.0
