@@ -55,9 +55,33 @@ def parse():
     ap.add_argument("--no-native", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the INT8 residue-GEMM comparison")
     ap.add_argument("--no-igemm", action="store_true", help="skip the exact INT8 product leg (4096^3)")
+    ap.add_argument("--no-two-limb", action="store_true", help="skip the two-limb moduli leg")
     ap.add_argument("--chunks", type=int, default=4,
                     help="row chunks of A in the timed step (1: the stages one after another)")
     return ap.parse_args()
+
+
+ACC_SAMPLE = 24  # sampled entries of C for the exact error measurement
+
+
+def bound_ratios(A_h, B_h, rows, cols, results):
+    """max over sampled entries (i, j) of |C_ij - (AB)_ij| / (2 K 2^-53 (|A||B|)_ij)
+    for each named result (arrays of the sampled entries), with the exact
+    product (AB)_ij summed in rationals (every fp64 value is a dyadic
+    rational, so the sum is exact)."""
+    from fractions import Fraction
+    k = A_h.shape[1]
+    out = {name: 0.0 for name in results}
+    for e, (i, j) in enumerate(zip(rows, cols)):
+        a = A_h[i]
+        b = B_h[:, j]
+        exact = sum((Fraction(float(x)) * Fraction(float(y)) for x, y in zip(a, b)), Fraction(0))
+        scale = 2.0 * k * 2.0 ** -53 * float(np.abs(a) @ np.abs(b))
+        for name, vals in results.items():
+            err = abs(Fraction(float(vals[e])) - exact)
+            if scale > 0:
+                out[name] = max(out[name], float(err) / scale)
+    return out
 
 
 def peaks():
@@ -537,13 +561,26 @@ def run_gpu(args):
             n0 = torch.cuda.Event(enable_timing=True)
             n1 = torch.cuda.Event(enable_timing=True)
             n0.record(stream)
-            torch.matmul(A, B)
+            C_native = torch.matmul(A, B)
             n1.record(stream)
             torch.cuda.synchronize(dev)
             times.append(n0.elapsed_time(n1))
         nat_ms = statistics.median(times)
         line["native_dgemm"] = {"tflops": round(flop / (nat_ms / 1e3) / 1e12, 3), "ms": round(nat_ms, 3),
                                 "calls": len(times), "speedup_of_emulation": round(nat_ms / ms_per_step, 2)}
+
+    # Accuracy on sampled entries against the exact product (rationals on the
+    # host): the emulated result, native cuBLAS DGEMM and, below, the
+    # two-limb result, each as a fraction of the 2 K 2^-53 |A||B| bound.
+    acc_rng = np.random.default_rng(7)
+    acc_rows = acc_rng.integers(0, m, size=ACC_SAMPLE)
+    acc_cols = acc_rng.integers(0, n, size=ACC_SAMPLE)
+    ri = torch.from_numpy(acc_rows).to(dev)
+    ci = torch.from_numpy(acc_cols).to(dev)
+    acc_results = {"emulated": C[ri, ci].cpu().numpy()}
+    if not args.no_native:
+        acc_results["native_dgemm"] = C_native[ri, ci].cpu().numpy()
+        del C_native
 
     if not args.no_compare:
         # Comparison: the residue products as one INT8 GEMM per modulus on the
@@ -634,6 +671,59 @@ def run_gpu(args):
             leg["cublaslt_int8_ms"] = round(i0.elapsed_time(i1), 3)
         line["igemm_s8_4096"] = leg
         del Ai, Bi, Ci
+
+    if not args.no_two_limb and not narrow:
+        # The same product with the two-limb moduli (<= 113, 4 FP4 GEMMs per
+        # modulus) through ozemu_dgemm_2limb, at the smallest r whose bit
+        # budget reaches the three-limb run's.
+        P3 = sum(oz.ozemu_bit_budget(k, r))
+        r2 = None
+        for cand in range(1, oz.ozemu_max_moduli() + 1):
+            try:
+                if sum(oz.ozemu_bit_budget_2limb(k, cand)) >= P3:
+                    r2 = cand
+                    break
+            except oz.OzemuError:
+                continue
+        if r2 is not None:
+            C2 = torch.empty((m, n), dtype=torch.float64, device=dev)
+
+            def two_limb():
+                check(oz.ozemu_dgemm_2limb(m, n, k, A.data_ptr(), k, B.data_ptr(), n, C2.data_ptr(), n, r2, sh),
+                      "dgemm_2limb")
+
+            for _ in range(2):
+                two_limb()
+            torch.cuda.synchronize(dev)
+            times = []
+            for _ in range(5):
+                t0 = torch.cuda.Event(enable_timing=True)
+                t1 = torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                two_limb()
+                t1.record(stream)
+                torch.cuda.synchronize(dev)
+                times.append(t0.elapsed_time(t1))
+            st2 = oz.ozemu_get_status(sh)
+            t2 = statistics.median(times)
+            acc_results["two_limb"] = C2[ri, ci].cpu().numpy()
+            line["two_limb"] = {
+                "r": r2, "bit_budget": sum(oz.ozemu_bit_budget_2limb(k, r2)), "three_limb_bit_budget": P3,
+                "fp4_gemms": 4 * r2, "three_limb_fp4_gemms": 9 * r, "ms": round(t2, 3),
+                "tflops": round(flop / (t2 / 1e3) / 1e12, 2), "status": int(st2),
+                "same_bits_as_three_limb_frac": round(float((C2.view(torch.int64) == C.view(torch.int64))
+                                                            .double().mean()), 4)}
+            del C2
+
+    if rank == 0:
+        t_acc = time.time()
+        ratios = bound_ratios(A_h, B_h, acc_rows, acc_cols, acc_results)
+        line["accuracy"] = {"sample": "%d random entries of C, exact products summed in rationals on the host"
+                                      % ACC_SAMPLE,
+                            "max_err_over_bound": {kk: round(v, 6) for kk, v in ratios.items()},
+                            "bound": "2 K 2^-53 (|A||B|)_ij", "seconds": round(time.time() - t_acc, 1)}
+        if "two_limb" in ratios:
+            line["accuracy"]["two_limb_r"] = line["two_limb"]["r"]
 
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_oracle(args.workload, r, CPU_MIN_SECONDS, shape={"m": m, "n": n, "k": k})

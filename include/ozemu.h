@@ -280,6 +280,55 @@ void ozemu_release(void);
 int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const double* B,
                         int ldb, double* C, int ldc, int r, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Two-limb moduli                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* A variant of the same scheme with smaller moduli, so that each balanced
+ * residue needs only two base-13 limbs.  [AWE] abstract: limbs in S with
+ * weights (1, 13, 169) and 9 FP4 products per modulus.  Two limbs d0 + 13 d1
+ * with d_i in S cover every integer of [-56, 56] (-56 = -4 + 13 (-4),
+ * 56 = 4 + 13 * 4, and each class mod 13 has a member of S of magnitude
+ * <= 6), so a modulus m <= 113 needs no third limb.  The product of two such
+ * residues then takes 4 FP4 GEMMs instead of 9:
+ *   D1 = A0 B0 + 13 (A0 B1 + A1 B0),   D2 = A1 B1,   residue = D1 + 169 D2 mod m.
+ * Each modulus carries about 6.7 bits instead of 8, so about 16/13 as many
+ * moduli reach the same accuracy: r = 16 two-limb moduli (64 products) give
+ * about the bit budget of r = 13 three-limb moduli (117 products).  The
+ * pages give the three-limb form; this one is a reading of the same limb
+ * algebra with the top limb fixed at zero.
+ *
+ *   - Moduli: the greedy pairwise-coprime integers counting down from 113
+ *     (113, 112, 111, 109, 107, 103, 101, 97, 95, 89, 83, 79, 73, 71, 67, 61).
+ *   - Bit budget: as above with these moduli (2k 2^P < m_1...m_r).
+ *   - Limb planes: row_bytes = 2 k_p/2; a row holds, for each 128-element K
+ *     block, the 64 bytes of limb 0, then of limb 1: limb j of element k is
+ *     at row byte (2*(k/128) + j)*64 + (k%128)/2.  Row i of modulus l starts
+ *     at byte (l*rows_p + i) * row_bytes.  Total: ozemu_plane_bytes_2limb.
+ *   - Residue layout: the same as the three-limb calls, with these moduli.
+ * Planes and residues of one family are not valid input to the other's
+ * calls.  Arguments, ownership and errors are those of the three-limb call of
+ * the same name. */
+int ozemu_moduli_2limb(int r, int32_t* out);
+int ozemu_bit_budget_2limb(int k, int r, int* p_a, int* p_b);
+size_t ozemu_plane_bytes_2limb(int rows, int k, int r);
+int ozemu_split_rows_f64_2limb(int rows, int k, const double* X, int ldx, int p, int r,
+                               uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+int ozemu_split_cols_f64_2limb(int k, int cols, const double* X, int ldx, int p, int r,
+                               uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+int ozemu_residue_gemm_2limb(int m, int n, int k, int r, const uint8_t* a_planes,
+                             const uint8_t* b_planes, uint8_t* residues, cudaStream_t stream);
+int ozemu_crt_f64_2limb(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a,
+                        const int32_t* shifts_b, double* C, int ldc, cudaStream_t stream);
+
+/* C = A B (device buffers, as ozemu_dgemm) through the two-limb stages:
+ * split, 4 FP4 GEMMs per modulus, CRT, one correct rounding per entry.
+ * Requires 2k < m_1...m_r of the two-limb moduli.  There is no narrow path;
+ * m >= 2048 pipelines the stages over row chunks like ozemu_dgemm.  Uses the
+ * cached workspace. */
+int ozemu_dgemm_2limb(int m, int n, int k, const double* A, int lda, const double* B,
+                      int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

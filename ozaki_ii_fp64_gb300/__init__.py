@@ -67,6 +67,14 @@ _SIGNATURES = {
     "ozemu_narrow_max_n": (_I, []),
     "ozemu_dgemm_host": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
     "ozemu_residues_narrow_f64": (_I, [_I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P]),
+    "ozemu_moduli_2limb": (_I, [_I, _P]),
+    "ozemu_bit_budget_2limb": (_I, [_I, _I, _P, _P]),
+    "ozemu_plane_bytes_2limb": (_S, [_I, _I, _I]),
+    "ozemu_split_rows_f64_2limb": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "ozemu_split_cols_f64_2limb": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "ozemu_residue_gemm_2limb": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
+    "ozemu_crt_f64_2limb": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P]),
+    "ozemu_dgemm_2limb": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
 }
 
 
@@ -200,6 +208,46 @@ def ozemu_release():
 
 def ozemu_dgemm_noalloc(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
     return _call("ozemu_dgemm_noalloc", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
+
+
+def ozemu_moduli_2limb(r):
+    buf = (ctypes.c_int32 * max(r, 1))()
+    st = _call("ozemu_moduli_2limb", r, ctypes.cast(buf, ctypes.c_void_p))
+    if st != OZEMU_OK:
+        raise OzemuError(st, "ozemu_moduli_2limb")
+    return [int(x) for x in buf[:r]]
+
+
+def ozemu_bit_budget_2limb(k, r):
+    pa, pb = ctypes.c_int(0), ctypes.c_int(0)
+    st = _call("ozemu_bit_budget_2limb", k, r, ctypes.byref(pa), ctypes.byref(pb))
+    if st != OZEMU_OK:
+        raise OzemuError(st, "ozemu_bit_budget_2limb")
+    return pa.value, pb.value
+
+
+def ozemu_plane_bytes_2limb(rows, k, r):
+    return _call("ozemu_plane_bytes_2limb", rows, k, r)
+
+
+def ozemu_split_rows_f64_2limb(rows, k, X, ldx, p, r, planes, shifts, stream):
+    return _call("ozemu_split_rows_f64_2limb", rows, k, X, ldx, p, r, planes, shifts, stream)
+
+
+def ozemu_split_cols_f64_2limb(k, cols, X, ldx, p, r, planes, shifts, stream):
+    return _call("ozemu_split_cols_f64_2limb", k, cols, X, ldx, p, r, planes, shifts, stream)
+
+
+def ozemu_residue_gemm_2limb(m, n, k, r, a_planes, b_planes, residues, stream):
+    return _call("ozemu_residue_gemm_2limb", m, n, k, r, a_planes, b_planes, residues, stream)
+
+
+def ozemu_crt_f64_2limb(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream):
+    return _call("ozemu_crt_f64_2limb", m, n, r, residues, shifts_a, shifts_b, C, ldc, stream)
+
+
+def ozemu_dgemm_2limb(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
+    return _call("ozemu_dgemm_2limb", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
 
 
 # ------------------------------------------------------- torch marshalling
@@ -396,3 +444,58 @@ def crt_f64(m, n, r, residues, shifts_a, shifts_b, out=None, stream=None):
 
 def get_status(stream=None):
     return ozemu_get_status(_stream(stream))
+
+
+# ------------------------------------------------------ two-limb moduli
+
+def dgemm_2limb(A, B, r, out=None, stream=None):
+    """Emulated fp64 A @ B with r two-limb moduli (4 FP4 products each)."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2:
+        raise ValueError("inner dimensions differ")
+    C = torch.empty((m, n), dtype=torch.float64, device=A.device) if out is None else out
+    _check(ozemu_dgemm_2limb(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
+                             _stream(stream)), "ozemu_dgemm_2limb")
+    return C
+
+
+def split_rows_f64_2limb(X, p, r, stream=None):
+    """(planes, shifts) of the rows of a cuda float64 matrix, two limbs."""
+    torch = _torch()
+    rows, k = X.shape
+    planes = torch.empty(ozemu_plane_bytes_2limb(rows, k, r), dtype=torch.uint8, device=X.device)
+    shifts = torch.empty(rows, dtype=torch.int32, device=X.device)
+    _check(ozemu_split_rows_f64_2limb(rows, k, X.data_ptr(), _ld(X), p, r, planes.data_ptr(), shifts.data_ptr(),
+                                      _stream(stream)), "ozemu_split_rows_f64_2limb")
+    return planes, shifts
+
+
+def split_cols_f64_2limb(X, p, r, stream=None):
+    """(planes, shifts) of the columns of a cuda float64 matrix, two limbs."""
+    torch = _torch()
+    k, cols = X.shape
+    planes = torch.empty(ozemu_plane_bytes_2limb(cols, k, r), dtype=torch.uint8, device=X.device)
+    shifts = torch.empty(cols, dtype=torch.int32, device=X.device)
+    _check(ozemu_split_cols_f64_2limb(k, cols, X.data_ptr(), _ld(X), p, r, planes.data_ptr(), shifts.data_ptr(),
+                                      _stream(stream)), "ozemu_split_cols_f64_2limb")
+    return planes, shifts
+
+
+def residue_gemm_2limb(m, n, k, r, a_planes, b_planes, out=None, stream=None):
+    """uint8 residues [r][m][round_up(n, 16)] of the two-limb product."""
+    torch = _torch()
+    ldr = (n + 15) // 16 * 16
+    res = torch.empty((r, m, ldr), dtype=torch.uint8, device=a_planes.device) if out is None else out
+    _check(ozemu_residue_gemm_2limb(m, n, k, r, a_planes.data_ptr(), b_planes.data_ptr(), res.data_ptr(),
+                                    _stream(stream)), "ozemu_residue_gemm_2limb")
+    return res
+
+
+def crt_f64_2limb(m, n, r, residues, shifts_a, shifts_b, out=None, stream=None):
+    torch = _torch()
+    C = torch.empty((m, n), dtype=torch.float64, device=residues.device) if out is None else out
+    _check(ozemu_crt_f64_2limb(m, n, r, residues.data_ptr(), shifts_a.data_ptr(), shifts_b.data_ptr(),
+                               C.data_ptr(), _ld(C), _stream(stream)), "ozemu_crt_f64_2limb")
+    return C

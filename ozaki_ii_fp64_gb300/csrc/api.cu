@@ -15,12 +15,13 @@ namespace {
 typedef unsigned __int128 u128;
 
 // ------------------------------------------------------------------ moduli
-// Greedy pairwise-coprime integers counting down from 256.
+// Greedy pairwise-coprime integers counting down from the ceiling: 256 for
+// the 3-limb moduli, 113 for the two-limb moduli.
 struct ModuliTable {
   uint32_t m[kMaxModuli];
-  ModuliTable() {
+  explicit ModuliTable(uint32_t ceiling) {
     int n = 0;
-    for (uint32_t c = 256; n < kMaxModuli && c >= 2; --c) {
+    for (uint32_t c = ceiling; n < kMaxModuli && c >= 2; --c) {
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
         uint32_t a = c, b = m[j];
@@ -35,20 +36,20 @@ struct ModuliTable {
     }
   }
 };
-const ModuliTable& moduli() {
-  static const ModuliTable t;
-  return t;
+const ModuliTable& moduli(int limbs = 3) {
+  static const ModuliTable t3(256), t2(113);
+  return limbs == 2 ? t2 : t3;
 }
 
-u128 modulus_product(int r) {
+u128 modulus_product(int r, int limbs = 3) {
   u128 p = 1;
-  for (int l = 0; l < r; ++l) p *= moduli().m[l];
+  for (int l = 0; l < r; ++l) p *= moduli(limbs).m[l];
   return p;
 }
 
 // Largest P with 2 k 2^P < M; -1 if none.
-int budget_P(long long k, int r) {
-  const u128 M = modulus_product(r);
+int budget_P(long long k, int r, int limbs = 3) {
+  const u128 M = modulus_product(r, limbs);
   const u128 two_k = static_cast<u128>(2) * static_cast<u128>(k);
   if (!(two_k < M)) return -1;
   int P = 0;
@@ -80,13 +81,14 @@ uint32_t inv_mod(uint32_t a, uint32_t m) {  // a coprime to m
   return static_cast<uint32_t>(t < 0 ? t + m : t);
 }
 
-SplitModuli split_moduli(int r) {
+SplitModuli split_moduli(int r, int limbs = 3) {
   SplitModuli s;
   std::memset(&s, 0, sizeof(s));
   s.r = r;
+  s.limbs = limbs;
   for (int l = 0; l < r; ++l) {
-    s.m[l] = moduli().m[l];
-    if (s.m[l] != kModulusTable[l]) s.r = 0;  // table mismatch: the launch refuses r = 0
+    s.m[l] = moduli(limbs).m[l];
+    if (s.m[l] != (limbs == 2 ? kModulusTable2[l] : kModulusTable[l])) s.r = 0;  // mismatch: the launch refuses
   }
   return s;
 }
@@ -113,11 +115,11 @@ bool narrow_enabled() {
   return !(s && s[0] == '0');
 }
 
-EpiModuli epi_moduli(int r) {
+EpiModuli epi_moduli(int r, int limbs = 3) {
   EpiModuli e;
   std::memset(&e, 0, sizeof(e));
   for (int l = 0; l < r; ++l) {
-    const uint32_t m = moduli().m[l];
+    const uint32_t m = moduli(limbs).m[l];
     e.m[l] = static_cast<float>(m);
     e.inv_m[l] = 1.0f / static_cast<float>(m);
     const int w = static_cast<int>(169u % m);
@@ -126,13 +128,14 @@ EpiModuli epi_moduli(int r) {
   return e;
 }
 
-CrtModuli crt_moduli(int r) {
+CrtModuli crt_moduli(int r, int limbs = 3) {
   CrtModuli c;
   std::memset(&c, 0, sizeof(c));
   c.r = r;
+  c.limbs = limbs;
   u128 pref = 1;
   for (int l = 0; l < r; ++l) {
-    const uint32_t m = moduli().m[l];
+    const uint32_t m = moduli(limbs).m[l];
     c.m[l] = m;
     c.magic[l] = static_cast<uint32_t>((1ull << 32) / m);
     const uint32_t inv = inv_mod(static_cast<uint32_t>(pref % m), m);
@@ -140,7 +143,7 @@ CrtModuli crt_moduli(int r) {
     u128 pj = 1;
     for (int j = 0; j < l; ++j) {
       c.g[l][j] = static_cast<uint32_t>((static_cast<uint64_t>(pj % m) * inv) % m);
-      pj *= moduli().m[j];
+      pj *= moduli(limbs).m[j];
     }
     for (int w = 0; w < 4; ++w) c.prefix[l][w] = static_cast<uint32_t>(pref >> (32 * w));
     pref *= m;
@@ -148,7 +151,7 @@ CrtModuli crt_moduli(int r) {
   // Direct form.  pref is now M (< 2^126).
   const u128 M = pref;
   for (int l = 0; l < r; ++l) {
-    const uint32_t m = moduli().m[l];
+    const uint32_t m = moduli(limbs).m[l];
     const u128 Ml = M / m;
     const u128 W = Ml * inv_mod(static_cast<uint32_t>(Ml % m), m);  // < M
     for (int w = 0; w < 16; ++w) c.wb[l / 4][w] |= static_cast<uint32_t>((W >> (8 * w)) & 0xFF) << (8 * (l % 4));
@@ -158,7 +161,7 @@ CrtModuli crt_moduli(int r) {
   for (int t = 0; t < 9; ++t) c.m16[t] = t < 8 ? static_cast<uint32_t>((M >> (16 * t)) & 0xFFFF) : 0u;
   int bits = 0;
   while (bits < 128 && (M >> bits) != 0) ++bits;
-  if (bits != kCrtBits[r]) c.r = 0;  // table mismatch: the launch refuses r = 0
+  if (bits != (limbs == 2 ? kCrtBits2[r] : kCrtBits[r])) c.r = 0;  // table mismatch: the launch refuses r = 0
   const long double Md = static_cast<long double>(M);
   for (int t = 0; t < 9; ++t) c.gt[t] = static_cast<float>(std::ldexp(1.0L, 16 * t) / Md);
   return c;
@@ -242,8 +245,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t plane_bytes(long long rows, long long k, int r) {
-  return static_cast<size_t>(3LL * r * round_up(static_cast<int>(rows), kRowAlign)) *
+size_t plane_bytes(long long rows, long long k, int r, int limbs = 3) {
+  return static_cast<size_t>(static_cast<long long>(limbs) * r * round_up(static_cast<int>(rows), kRowAlign)) *
          static_cast<size_t>(round_up(static_cast<int>(k), kKAlign) / 2);
 }
 
@@ -255,21 +258,22 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? OZEMU_OK : OZEMU_ERR_
 
 // ---------------------------------------------------------------- stages
 int split_rows_f64(int rows, int k, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, DeviceState* d, cudaStream_t st) {
-  return cuda_status(launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r), planes, shifts, d->flags, st));
+                   int32_t* shifts, DeviceState* d, cudaStream_t st, int limbs = 3) {
+  return cuda_status(
+      launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r, limbs), planes, shifts, d->flags, st));
 }
 
 int split_cols_f64(int k, int cols, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st) {
+                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st, int limbs = 3) {
   if (k > 0) {
     cudaError_t e = launch_transpose_f64(X, ldx, k, cols, scratch, k, st);
     if (e != cudaSuccess) return OZEMU_ERR_CUDA;
   }
-  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st);
+  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st, limbs);
 }
 
 int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* bp, uint8_t* res, DeviceState* d,
-                 cudaStream_t st) {
+                 cudaStream_t st, int limbs = 3) {
   LimbGemmCall c;
   c.residue_mode = true;
   c.m = m;
@@ -283,7 +287,8 @@ int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* b
   c.c32 = nullptr;
   c.ldc = 0;
   c.kc_blocks = kchunk_blocks();
-  c.em = epi_moduli(r);
+  c.limbs = limbs;
+  c.em = epi_moduli(r, limbs);
   c.flags = d->flags;
   return cuda_status(launch_limb_gemm(c, st));
 }
@@ -364,7 +369,7 @@ int pipeline_state(DeviceState* d) {
 constexpr int kMaxChunks = 8;
 
 int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc, int r,
-                  int pa_bits, int pb_bits, bool from_host, DeviceState* d, cudaStream_t stream) {
+                  int pa_bits, int pb_bits, bool from_host, DeviceState* d, cudaStream_t stream, int limbs = 3) {
   int s = pipeline_state(d);
   if (s != OZEMU_OK) return s;
   // Row chunks of A: up to four equal chunks; with host operands and
@@ -390,8 +395,8 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   const size_t szB = from_host ? align256(static_cast<size_t>(k) * n * 8) : 0;
   const size_t szC = from_host ? align256(static_cast<size_t>(m) * n * 8) : 0;
   const size_t szBt = align256(static_cast<size_t>(k) * bcols * 8);
-  const size_t szBp = align256(plane_bytes(bcols, k, r)), szSb = align256(static_cast<size_t>(bcols) * 4);
-  const size_t szAp = align256(plane_bytes(chunk, k, r)), szSa = align256(static_cast<size_t>(chunk) * 4);
+  const size_t szBp = align256(plane_bytes(bcols, k, r, limbs)), szSb = align256(static_cast<size_t>(bcols) * 4);
+  const size_t szAp = align256(plane_bytes(chunk, k, r, limbs)), szSa = align256(static_cast<size_t>(chunk) * 4);
   const size_t szRes = align256(ozemu_residue_bytes(chunk, bcols, r));
   uint8_t* buf = nullptr;
   s = workspace(d, szA + szB + szC + szBt + nbc * (szBp + szSb) + nch * (szAp + szSa + nbc * szRes), &buf);
@@ -408,7 +413,7 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   cudaEvent_t* ev = d->ev;
   constexpr int evStart = 0, evB = 1, evA = 3, evG = 3 + kMaxChunks, evC = evG + 1, evD = evC + 1;  // nbc <= 2
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-  const CrtModuli cm = crt_moduli(r);
+  const CrtModuli cm = crt_moduli(r, limbs);
   auto bcol0 = [&](int j) { return j * bcols; };
   auto bwidth = [&](int j) { return n - j * bcols < bcols ? n - j * bcols : bcols; };
   auto bplanes = [&](int j) { return per_bblock + j * (szBp + szSb); };
@@ -421,7 +426,8 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   };
   auto split_b = [&](int j) -> int {
     if (from_host && cudaStreamWaitEvent(stream, ev[evB + j], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
-    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), Bt, d, stream);
+    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), Bt, d, stream,
+                          limbs);
   };
   if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
       cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
@@ -444,7 +450,8 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
         return OZEMU_ERR_CUDA;
     } else {
       uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
-      s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, reinterpret_cast<int32_t*>(ap + szAp), d, cs);
+      s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, reinterpret_cast<int32_t*>(ap + szAp), d, cs,
+                         limbs);
       if (s != OZEMU_OK) return s;
     }
     if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
@@ -461,13 +468,13 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
     if (j == 0) {
       if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
       if (from_host) {
-        const int st = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream);
+        const int st = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream, limbs);
         if (st != OZEMU_OK) return st;
       }
     }
     const int col0 = bcol0(j), nc = bwidth(j);
     uint8_t* res = ap + szAp + szSa + j * szRes;
-    const int st = residue_gemm(mc, nc, k, r, ap, bplanes(j), res, d, stream);
+    const int st = residue_gemm(mc, nc, k, r, ap, bplanes(j), res, d, stream, limbs);
     if (st != OZEMU_OK) return st;
     // One event each for the product -> CRT and CRT -> copy hand-offs: each
     // record is waited on before the next one.
@@ -612,8 +619,8 @@ int ozemu_split_rows_f64(int rows, int k, const double* X, int ldx, int p, int r
   return split_rows_f64(rows, k, X, ldx, p, r, planes, shifts, d, stream);
 }
 
-int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
-                         int32_t* shifts, cudaStream_t stream) {
+static int split_cols_entry(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
+                            int32_t* shifts, cudaStream_t stream, int limbs) {
   if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
     return OZEMU_ERR_INVALID_ARG;
   if (cols == 0) return OZEMU_OK;
@@ -624,7 +631,12 @@ int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r
   uint8_t* ws = nullptr;
   s = workspace(d, align256(static_cast<size_t>(k > 0 ? k : 1) * cols * sizeof(double)), &ws);
   if (s != OZEMU_OK) return s;
-  return split_cols_f64(k, cols, X, ldx, p, r, planes, shifts, reinterpret_cast<double*>(ws), d, stream);
+  return split_cols_f64(k, cols, X, ldx, p, r, planes, shifts, reinterpret_cast<double*>(ws), d, stream, limbs);
+}
+
+int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
+                         int32_t* shifts, cudaStream_t stream) {
+  return split_cols_entry(k, cols, X, ldx, p, r, planes, shifts, stream, 3);
 }
 
 int ozemu_split_rows_s8(int rows, int k, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream) {
@@ -702,8 +714,8 @@ int ozemu_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8, cons
                                             stream));
 }
 
-int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
-                       uint8_t* residues, cudaStream_t stream) {
+static int residue_gemm_entry(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
+                              uint8_t* residues, cudaStream_t stream, int limbs) {
   if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
   if (m == 0 || n == 0) return OZEMU_OK;
   if (!residues || !aligned16(residues) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
@@ -714,7 +726,12 @@ int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes, cons
   if (s != OZEMU_OK) return s;
   if (k == 0)
     return cuda_status(cudaMemsetAsync(residues, 0, ozemu_residue_bytes(m, n, r), stream));
-  return residue_gemm(m, n, k, r, a_planes, b_planes, residues, d, stream);
+  return residue_gemm(m, n, k, r, a_planes, b_planes, residues, d, stream, limbs);
+}
+
+int ozemu_residue_gemm(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
+                       uint8_t* residues, cudaStream_t stream) {
+  return residue_gemm_entry(m, n, k, r, a_planes, b_planes, residues, stream, 3);
 }
 
 int ozemu_limb_gemm_s32(int m, int n, int k, const uint8_t* a_planes, const uint8_t* b_planes, int32_t* C32,
@@ -750,8 +767,8 @@ int ozemu_residues_narrow_f64(int m, int n, int k, int r, const double* A, int l
   return narrow_residues(m, n, k, A, lda, B, ldb, r, pa_bits, pb_bits, residues, shifts_a, shifts_b, d, stream);
 }
 
-int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a, const int32_t* shifts_b,
-                  double* C, int ldc, cudaStream_t stream) {
+static int crt_entry(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a, const int32_t* shifts_b,
+                     double* C, int ldc, cudaStream_t stream, int limbs) {
   if (m < 0 || n < 0 || r < 1 || r > kMaxModuli || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
   if (m == 0 || n == 0) return OZEMU_OK;
   if (!residues || !aligned16(residues) || !shifts_a || !shifts_b || !C) return OZEMU_ERR_INVALID_ARG;
@@ -759,7 +776,12 @@ int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* s
   int s = device_state(&d);
   if (s != OZEMU_OK) return s;
   return cuda_status(
-      launch_crt_f64(m, n, residues, round_up(n, 16), shifts_a, shifts_b, C, ldc, crt_moduli(r), stream));
+      launch_crt_f64(m, n, residues, round_up(n, 16), shifts_a, shifts_b, C, ldc, crt_moduli(r, limbs), stream));
+}
+
+int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a, const int32_t* shifts_b,
+                  double* C, int ldc, cudaStream_t stream) {
+  return crt_entry(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream, 3);
 }
 
 int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B, int32_t* C32, cudaStream_t stream) {
@@ -820,6 +842,89 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   s = residue_gemm(m, n, k, r, ap, bp, res, d, stream);
   if (s != OZEMU_OK) return s;
   return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), stream));
+}
+
+// ---------------------------------------------------------- two-limb moduli
+int ozemu_moduli_2limb(int r, int32_t* out) {
+  if (r < 1 || r > kMaxModuli || !out) return OZEMU_ERR_INVALID_ARG;
+  for (int l = 0; l < r; ++l) out[l] = static_cast<int32_t>(moduli(2).m[l]);
+  return OZEMU_OK;
+}
+
+int ozemu_bit_budget_2limb(int k, int r, int* p_a, int* p_b) {
+  if (k < 1 || r < 1 || r > kMaxModuli || !p_a || !p_b) return OZEMU_ERR_INVALID_ARG;
+  const int P = budget_P(k, r, 2);
+  if (P < 0) return OZEMU_ERR_INVALID_ARG;
+  *p_a = (P + 1) / 2;
+  *p_b = P / 2;
+  return OZEMU_OK;
+}
+
+size_t ozemu_plane_bytes_2limb(int rows, int k, int r) {
+  if (rows < 0 || k < 0 || r < 1 || r > kMaxModuli) return 0;
+  return plane_bytes(rows, k, r, 2);
+}
+
+int ozemu_split_rows_f64_2limb(int rows, int k, const double* X, int ldx, int p, int r, uint8_t* planes,
+                               int32_t* shifts, cudaStream_t stream) {
+  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+    return OZEMU_ERR_INVALID_ARG;
+  if (rows == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !shifts || !aligned16(planes) || !rows_ok(rows, r)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  return split_rows_f64(rows, k, X, ldx, p, r, planes, shifts, d, stream, 2);
+}
+
+int ozemu_split_cols_f64_2limb(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
+                               int32_t* shifts, cudaStream_t stream) {
+  return split_cols_entry(k, cols, X, ldx, p, r, planes, shifts, stream, 2);
+}
+
+int ozemu_residue_gemm_2limb(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
+                             uint8_t* residues, cudaStream_t stream) {
+  return residue_gemm_entry(m, n, k, r, a_planes, b_planes, residues, stream, 2);
+}
+
+int ozemu_crt_f64_2limb(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a,
+                        const int32_t* shifts_b, double* C, int ldc, cudaStream_t stream) {
+  return crt_entry(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream, 2);
+}
+
+int ozemu_dgemm_2limb(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                      int r, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (k > 0 && ozemu_bit_budget_2limb(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
+  if (m >= 2048) return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, false, d, stream, 2);
+  const size_t pa = align256(plane_bytes(m, k, r, 2)), pb = align256(plane_bytes(n, k, r, 2));
+  const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
+  const size_t rb = align256(ozemu_residue_bytes(m, n, r));
+  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  uint8_t* ws = nullptr;
+  s = workspace(d, pa + pb + sa + sb + rb + bt, &ws);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ap = ws;
+  uint8_t* bp = ap + pa;
+  int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
+  int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
+  uint8_t* res = bp + pb + sa + sb;
+  double* btr = reinterpret_cast<double*>(res + rb);
+  s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, d, stream, 2);
+  if (s != OZEMU_OK) return s;
+  s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, d, stream, 2);
+  if (s != OZEMU_OK) return s;
+  s = residue_gemm(m, n, k, r, ap, bp, res, d, stream, 2);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r, 2), stream));
 }
 
 int ozemu_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,

@@ -29,10 +29,18 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kModulusTable[kMaxModuli] = {256, 255, 253, 251, 247, 241, 239, 233,
                                                 229, 227, 223, 217, 211, 199, 197, 193};
 
-// Moduli of a deconstruction launch (r = 0 if the host's moduli differ from
-// kModulusTable; the launch then refuses).
+// The two-limb moduli: greedy pairwise-coprime integers counting down from
+// 113.  Their balanced residues lie in [-56, 56], where the base-13 split's
+// third limb is always 0, so two limbs (4 FP4 products per modulus) suffice.
+constexpr uint32_t kModulusTable2[kMaxModuli] = {113, 112, 111, 109, 107, 103, 101, 97,
+                                                 95,  89,  83,  79,  73,  71,  67,  61};
+
+// Moduli of a deconstruction launch: limbs 3 takes kModulusTable, limbs 2
+// kModulusTable2 (r = 0 if the host's moduli differ from the table; the
+// launch then refuses).
 struct SplitModuli {
   int r;
+  int limbs;
   uint32_t m[kMaxModuli];
 };
 
@@ -58,9 +66,12 @@ struct EpiModuli {
 // Bit length of M = m_1 ... m_r for the moduli table (greedy pairwise-coprime
 // integers from 256 down), r = 0..16; the host checks it against the table.
 constexpr int kCrtBits[kMaxModuli + 1] = {0, 9, 16, 24, 32, 40, 48, 56, 64, 72, 80, 88, 95, 103, 111, 118, 126};
+// The same for the two-limb moduli (kModulusTable2).
+constexpr int kCrtBits2[kMaxModuli + 1] = {0, 7, 14, 21, 28, 34, 41, 48, 54, 61, 67, 74, 80, 86, 92, 99, 104};
 
 struct CrtModuli {
   int r;
+  int limbs;                              // 3: kModulusTable, 2: kModulusTable2
   uint32_t m[kMaxModuli];
   uint32_t magic[kMaxModuli];             // floor(2^32 / m)
   uint32_t inv[kMaxModuli];               // (m_0 ... m_{l-1})^-1 mod m_l

@@ -35,14 +35,16 @@ __device__ __forceinline__ uint32_t dp4a_u8(uint32_t a, uint32_t b, uint32_t c) 
 // 2^(16 NX) (|C'| < M/2 fits).  When Y/M lies within 2^-8 of a half-integer
 // the estimate may be off by one: that output takes the mixed-radix digits
 // instead (crt_round), which are exact for any input.
-template <int R>
+// NLimb = 2: the two-limb moduli (kModulusTable2), whose products have the
+// bit lengths kCrtBits2.
+template <int R, int NLimb>
 __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const uint8_t* __restrict__ res,
                                                           long long ldr, const int32_t* __restrict__ sa,
                                                           const int32_t* __restrict__ sb, double* __restrict__ C,
                                                           long long ldc, const __grid_constant__ CrtModuli cm) {
   constexpr bool kLastByMad = (R % 4) == 1;   // a lone last modulus: multiply-adds, not dp4a
   constexpr int NQ = kLastByMad ? R / 4 : (R + 3) / 4;  // words of four residues through dp4a
-  constexpr int BM = kCrtBits[R];             // bit length of M
+  constexpr int BM = NLimb == 2 ? kCrtBits2[R] : kCrtBits[R];  // bit length of M
   constexpr int NL = (BM + 7) / 8;            // bytes of W_l
   constexpr int NT = (NL + 1) / 2;            // 16-bit positions of Y's partial sums
   constexpr int NX = (BM + 15) / 16;          // 16-bit limbs of C' (two's complement)
@@ -152,12 +154,12 @@ int grid_for(long long work, int threads) {
 
 }  // namespace
 
-template <int R>
+template <int R, int NL>
 cudaError_t launch_crt_r(int m, int n, const uint8_t* residues, long long ldr, const int32_t* sa, const int32_t* sb,
                          double* C, long long ldc, const CrtModuli& cm, cudaStream_t stream) {
   if (cm.r != R) return cudaErrorInvalidValue;
   const long long work = static_cast<long long>(m) * ((n + 3) / 4);
-  crt_kernel<R><<<grid_for(work, kCrtThreads), kCrtThreads, 0, stream>>>(m, n, residues, ldr, sa, sb, C, ldc, cm);
+  crt_kernel<R, NL><<<grid_for(work, kCrtThreads), kCrtThreads, 0, stream>>>(m, n, residues, ldr, sa, sb, C, ldc, cm);
   return cudaGetLastError();
 }
 
@@ -166,7 +168,8 @@ cudaError_t launch_crt_f64(int m, int n, const uint8_t* residues, long long ldr,
   switch (cm.r) {
 #define OZEMU_CRT_CASE(R) \
   case R:                 \
-    return launch_crt_r<R>(m, n, residues, ldr, sa, sb, C, ldc, cm, stream);
+    return cm.limbs == 2 ? launch_crt_r<R, 2>(m, n, residues, ldr, sa, sb, C, ldc, cm, stream) \
+                         : launch_crt_r<R, 3>(m, n, residues, ldr, sa, sb, C, ldc, cm, stream);
     OZEMU_CRT_CASE(1) OZEMU_CRT_CASE(2) OZEMU_CRT_CASE(3) OZEMU_CRT_CASE(4) OZEMU_CRT_CASE(5) OZEMU_CRT_CASE(6)
     OZEMU_CRT_CASE(7) OZEMU_CRT_CASE(8) OZEMU_CRT_CASE(9) OZEMU_CRT_CASE(10) OZEMU_CRT_CASE(11)
     OZEMU_CRT_CASE(12) OZEMU_CRT_CASE(13) OZEMU_CRT_CASE(14) OZEMU_CRT_CASE(15) OZEMU_CRT_CASE(16)

@@ -134,7 +134,9 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)
   for (int c = 0; c < CW; c += 8) tmem_st8(taddr + c, v + c);
 }
 
-template <int BN, bool kResidue>
+// NL: limbs per modulus (3; 2 for the two-limb moduli, whose third limb is 0:
+// 4 products, the third limb neither loaded nor multiplied).
+template <int BN, bool kResidue, int NL>
 __global__ void __launch_bounds__(kThreads, 1)
     limb_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs args) {
@@ -221,13 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = smem + s * C::kStage;
-          mbar_arrive_expect_tx(&full[s], C::kStage);
+          mbar_arrive_expect_tx(&full[s], NL * (kATile + C::kBTile));
 #pragma unroll
-          for (int j = 0; j < 3; ++j)
-            tma_load_2d(st + j * kATile, &tmA, &full[s], (3 * kb + j) * kBKBytes, a_row);
+          for (int j = 0; j < NL; ++j)
+            tma_load_2d(st + j * kATile, &tmA, &full[s], (NL * kb + j) * kBKBytes, a_row);
 #pragma unroll
-          for (int j = 0; j < 3; ++j)
-            tma_load_2d(st + 3 * kATile + j * C::kBTile, &tmB, &full[s], (3 * kb + j) * kBKBytes, b_row);
+          for (int j = 0; j < NL; ++j)
+            tma_load_2d(st + 3 * kATile + j * C::kBTile, &tmB, &full[s], (NL * kb + j) * kBKBytes, b_row);
         }
       }
       if (!ok) {
@@ -286,15 +288,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               // (collector buffer), with one A scale per group: the factor
               // 13 sits on B's scale; A2 B2 (weight 169 = 26 * 26 / 4) needs
               // the other A scale and is issued on its own.
-              mma_fp4_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
-              mma_fp4_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
-              mma_fp4_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
-              mma_fp4_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
-              mma_fp4_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
-              mma_fp4_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
-              mma_fp4_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
-              mma_fp4_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
-              mma_fp4(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+              if constexpr (NL == 3) {
+                mma_fp4_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+                mma_fp4_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
+                mma_fp4_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
+                mma_fp4_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+                mma_fp4_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
+                mma_fp4_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
+                mma_fp4_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
+                mma_fp4_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
+                mma_fp4(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+              } else {
+                // D1 = A0B0 + 13 (A0B1 + A1B0), D2 = A1B1 (weight 169 at the drain).
+                mma_fp4_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+                mma_fp4_lastuse(d1, a0, b1, idesc, s2, s26, 1u);   // 13
+                mma_fp4_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+                mma_fp4_lastuse(d2, a1, b1, idesc, s2, s2, acc);   // 1 (in D2)
+              }
               if (ks == 0)
                 known_full = mbar_test_wait(&full[(it + 1) % C::kStages], ((it + 1) / C::kStages) & 1);
             }
@@ -485,7 +495,7 @@ __device__ __forceinline__ void settle_after_abort() {
 
 // kInt: the INT8 product (r = 1, one exact K chunk): the epilogue writes the
 // int32 sums D1 + 169 D2 slice by slice instead of residues.
-template <bool kInt>
+template <bool kInt, int NL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     limb_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const PairArgs args) {
@@ -569,13 +579,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // earlier bulk copies and serialise the stages.  The phase cannot
           // complete before it is armed, and the second CTA cannot fill a
           // stage of the next phase before the pair's MMAs freed it.
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStage2);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * NL * (kATile + kBTile2));
 #pragma unroll
-          for (int j = 0; j < 3; ++j)
-            tma_load_2d_pair(st + j * kATile, &tmA, full_leader, (3 * kb + j) * kBKBytes, a_row);
+          for (int j = 0; j < NL; ++j)
+            tma_load_2d_pair(st + j * kATile, &tmA, full_leader, (NL * kb + j) * kBKBytes, a_row);
 #pragma unroll
-          for (int j = 0; j < 3; ++j)
-            tma_load_2d_pair(st + 3 * kATile + j * kBTile2, &tmB, full_leader, (3 * kb + j) * kBKBytes, b_row);
+          for (int j = 0; j < NL; ++j)
+            tma_load_2d_pair(st + 3 * kATile + j * kBTile2, &tmB, full_leader, (NL * kb + j) * kBKBytes, b_row);
         }
       }
       if (!ok) settle_after_abort();
@@ -620,15 +630,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * kBTile2 + ks * 32);
               const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * kBTile2 + ks * 32);
               const uint32_t acc = (kb == kc0 && ks == 0) ? 0u : 1u;
-              mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
-              mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
-              mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
-              mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
-              mma_fp4_pair_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
-              mma_fp4_pair_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
-              mma_fp4_pair_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
-              mma_fp4_pair_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
-              mma_fp4_pair(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+              if constexpr (NL == 3) {
+                mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+                mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
+                mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
+                mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+                mma_fp4_pair_use(d2, a1, b1, idesc, s2, s2, 1u);        // 1 (in D2)
+                mma_fp4_pair_lastuse(d2, a1, b2, idesc, s2, s26, 1u);   // 13 (in D2)
+                mma_fp4_pair_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
+                mma_fp4_pair_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
+                mma_fp4_pair(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
+              } else {
+                // D1 = A0B0 + 13 (A0B1 + A1B0), D2 = A1B1 (weight 169 at the drain).
+                mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
+                mma_fp4_pair_lastuse(d1, a0, b1, idesc, s2, s26, 1u);   // 13
+                mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
+                mma_fp4_pair_lastuse(d2, a1, b1, idesc, s2, s2, acc);   // 1 (in D2)
+              }
               if (ks == 0)
                 known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
             }
@@ -772,12 +790,13 @@ EncodeTiledFn encode_fn() {
 
 // 2-D map over the limb planes of r moduli: y = modulus l rows_p + row;
 // x = byte within the row, where the three limbs of 128-element K block kb
-// lie at x = (3 kb + j) 64.
-bool make_plane_map(CUtensorMap* map, const uint8_t* base, int k_p, long long total_rows, int box_rows) {
+// lie at x = (3 kb + j) 64 (two-limb moduli: (2 kb + j) 64).
+bool make_plane_map(CUtensorMap* map, const uint8_t* base, int k_p, int limbs, long long total_rows, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(3LL * k_p / 2), static_cast<cuuint64_t>(total_rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(3LL * k_p / 2)};
+  const long long row_bytes = static_cast<long long>(limbs) * k_p / 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(total_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
@@ -786,15 +805,15 @@ bool make_plane_map(CUtensorMap* map, const uint8_t* base, int k_p, long long to
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool kResidue>
+template <int BN, bool kResidue, int NL>
 cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   using Cf = Cfg<BN>;
   const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
   const int k_p = round_up(c.k, kKAlign);
   const int r = c.residue_mode ? c.r : 1;
   CUtensorMap ma, mb;
-  if (!make_plane_map(&ma, c.a_planes, k_p, 1LL * r * rows_a_p, kBM)) return cudaErrorInvalidValue;
-  if (!make_plane_map(&mb, c.b_planes, k_p, 1LL * r * rows_b_p, BN)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&ma, c.a_planes, k_p, NL, 1LL * r * rows_a_p, kBM)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&mb, c.b_planes, k_p, NL, 1LL * r * rows_b_p, BN)) return cudaErrorInvalidValue;
   GemmArgs a;
   a.m = c.m;
   a.n = c.n;
@@ -811,7 +830,7 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   a.c32 = c.c32;
   a.ldc = c.ldc;
   a.flags = c.flags;
-  auto kern = limb_gemm_kernel<BN, kResidue>;
+  auto kern = limb_gemm_kernel<BN, kResidue, NL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
@@ -822,13 +841,13 @@ cudaError_t launch_bn(const LimbGemmCall& c, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <bool kInt>
+template <bool kInt, int NL>
 cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   const int rows_a_p = round_up(c.m, kRowAlign), rows_b_p = round_up(c.n, kRowAlign);
   const int k_p = round_up(c.k, kKAlign);
   CUtensorMap ma, mb;
-  if (!make_plane_map(&ma, c.a_planes, k_p, 1LL * c.r * rows_a_p, kBM)) return cudaErrorInvalidValue;
-  if (!make_plane_map(&mb, c.b_planes, k_p, 1LL * c.r * rows_b_p, kBHalf)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&ma, c.a_planes, k_p, NL, 1LL * c.r * rows_a_p, kBM)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&mb, c.b_planes, k_p, NL, 1LL * c.r * rows_b_p, kBHalf)) return cudaErrorInvalidValue;
   PairArgs a;
   a.m = c.m;
   a.n = c.n;
@@ -846,11 +865,11 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   a.ldc = c.ldc;
   a.flags = c.flags;
   cudaError_t e =
-      cudaFuncSetAttribute(limb_gemm_pair_kernel<kInt>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2);
+      cudaFuncSetAttribute(limb_gemm_pair_kernel<kInt, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2);
   if (e != cudaSuccess) return e;
   // A persistent grid must not exceed the clusters that can be resident at
   // once, or the excess clusters start only when others finish.
-  static int max_pairs[64] = {0};  // the two instantiations have the same resources
+  static int max_pairs[64] = {0};  // every instantiation has the same resources
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -867,7 +886,7 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, limb_gemm_pair_kernel<kInt>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, limb_gemm_pair_kernel<kInt, NL>, &cfg);
     if (e != cudaSuccess || n < 1) {
       cudaGetLastError();
       int sms = 148;
@@ -877,7 +896,7 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
     max_pairs[dev] = n;
   }
   const int pairs = a.total_tiles < max_pairs[dev] ? a.total_tiles : max_pairs[dev];
-  limb_gemm_pair_kernel<kInt><<<2 * pairs, kThreads, kSmem2, stream>>>(ma, mb, a);
+  limb_gemm_pair_kernel<kInt, NL><<<2 * pairs, kThreads, kSmem2, stream>>>(ma, mb, a);
   return cudaGetLastError();
 }
 
@@ -889,19 +908,25 @@ bool use_pair(const LimbGemmCall& c) {
   return true;
 }
 
-template <bool kResidue>
+template <bool kResidue, int NL>
 cudaError_t launch_mode(const LimbGemmCall& c, cudaStream_t stream) {
-  if (c.n <= 16) return launch_bn<16, kResidue>(c, stream);
-  if (c.n <= 32) return launch_bn<32, kResidue>(c, stream);
-  if (c.n <= 64) return launch_bn<64, kResidue>(c, stream);
-  return launch_bn<128, kResidue>(c, stream);
+  if (c.n <= 16) return launch_bn<16, kResidue, NL>(c, stream);
+  if (c.n <= 32) return launch_bn<32, kResidue, NL>(c, stream);
+  if (c.n <= 64) return launch_bn<64, kResidue, NL>(c, stream);
+  return launch_bn<128, kResidue, NL>(c, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream) {
-  if (use_pair(call)) return call.residue_mode ? launch_pair<false>(call, stream) : launch_pair<true>(call, stream);
-  return call.residue_mode ? launch_mode<true>(call, stream) : launch_mode<false>(call, stream);
+  if (call.limbs == 2) {  // two-limb moduli: residue products only
+    if (!call.residue_mode) return cudaErrorInvalidValue;
+    return use_pair(call) ? launch_pair<false, 2>(call, stream) : launch_mode<true, 2>(call, stream);
+  }
+  if (call.limbs != 3) return cudaErrorInvalidValue;
+  if (use_pair(call))
+    return call.residue_mode ? launch_pair<false, 3>(call, stream) : launch_pair<true, 3>(call, stream);
+  return call.residue_mode ? launch_mode<true, 3>(call, stream) : launch_mode<false, 3>(call, stream);
 }
 
 }  // namespace ozemu

@@ -36,6 +36,7 @@ struct LimbGemmCall {
   int32_t* c32;
   long long ldc;
   int kc_blocks;
+  int limbs = 3;  // limbs per modulus: 3, or 2 for the two-limb moduli (residue mode only)
   EpiModuli em;
   uint32_t* flags;
 };

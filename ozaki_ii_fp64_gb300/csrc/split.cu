@@ -84,9 +84,12 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
 // products with the weights 2^(8i) mod m (each < 256) and an accumulator
 // bias give v = u + bias < 2^20 with v = A' + h (mod m), h = floor(m/2).  The
 // quotient floor(v/m) comes from one fp32 fma rounded down: v and 2^23 are
-// exact in fp32, 1/m is taken rounded up (c = ceil(2^31/m) 2^-31), and
-// v c - v/m < 2^-11 < 1/m, so rd(v c + 2^23) = 2^23 + floor(v/m) exactly; its
-// bit pattern is 0x4B000000 + floor(v/m).  Then w = v - m floor(v/m) is
+// exact in fp32, 1/m is taken rounded up (c = ceil(2^e/m) 2^-e with
+// e = 23 + ceil(log2 m), a 24-bit integer times a power of two), and
+// v c - v/m < 2^(20-e) <= 2^-9 < 1/m, so rd(v c + 2^23) = 2^23 + floor(v/m)
+// exactly; its bit pattern is 0x4B000000 + floor(v/m).  (An even modulus
+// other than 256, 112 in the two-limb list, takes an exact Barrett step with
+// ceil(2^32/m) instead, v m < 2^32.)  Then w = v - m floor(v/m) is
 // (A' + h) mod m and b = w - h is the balanced residue, in [-h, m - 1 - h] as
 // the method takes it.  The codes of b come from one table shared by every
 // modulus, indexed by b + 128.
@@ -101,8 +104,9 @@ struct ResidueStep {
   float inv_up;
 };
 
-__host__ __device__ constexpr ResidueStep residue_step(int l) {
-  const uint32_t m = kModulusTable[l], h = m >> 1;
+// Modulus l of the 3-limb (nl = 3) or two-limb (nl = 2) list.
+__host__ __device__ constexpr ResidueStep residue_step(int l, int nl) {
+  const uint32_t m = nl == 2 ? kModulusTable2[l] : kModulusTable[l], h = m >> 1;
   ResidueStep st{m, 0u, 0u, 0u, 0u, 0.0f};
   for (int i = 0; i < 4; ++i) {
     st.clo |= pow2_mod(8 * i, m) << (8 * i);
@@ -110,23 +114,31 @@ __host__ __device__ constexpr ResidueStep residue_step(int l) {
   }
   st.bias = (h + m - pow2_mod(63, m)) % m;
   st.row = 128u - h;  // table row of b = -h
-  // ceil(2^31 / m) < 2^24 for 128 < m < 256: exact in fp32.
-  st.inv_up = static_cast<float>((((1ull << 31) + m - 1) / m)) / 2147483648.0f;
+  int lg = 0;
+  while ((1u << lg) < m) ++lg;
+  const int e = 23 + lg;  // ceil(2^e / m) lies in [2^23, 2^24): exact in fp32
+  st.inv_up = static_cast<float>(((1ull << e) + m - 1) / m) / static_cast<float>(1ull << e);
   return st;
 }
 
 // The per-modulus constants in the constant bank (operands of the dot
-// products and the fma), with the dot-product bias carrying 0x4B000000.
-__host__ __device__ constexpr ResidueStep residue_step_biased(int l) {
-  ResidueStep st = residue_step(l);
-  st.bias += 0x4B000000u;
+// products and the fma), with the dot-product bias carrying 0x4B000000 for
+// the odd moduli (the fp32 quotient).
+__host__ __device__ constexpr ResidueStep residue_step_biased(int l, int nl) {
+  ResidueStep st = residue_step(l, nl);
+  if (st.m % 2 == 1) st.bias += 0x4B000000u;
   return st;
 }
-__constant__ ResidueStep kSteps[kMaxModuli] = {
-    residue_step_biased(0),  residue_step_biased(1),  residue_step_biased(2),  residue_step_biased(3),
-    residue_step_biased(4),  residue_step_biased(5),  residue_step_biased(6),  residue_step_biased(7),
-    residue_step_biased(8),  residue_step_biased(9),  residue_step_biased(10), residue_step_biased(11),
-    residue_step_biased(12), residue_step_biased(13), residue_step_biased(14), residue_step_biased(15)};
+#define OZEMU_STEPS(NL)                                                                                      \
+  {residue_step_biased(0, NL),  residue_step_biased(1, NL),  residue_step_biased(2, NL),                    \
+   residue_step_biased(3, NL),  residue_step_biased(4, NL),  residue_step_biased(5, NL),                    \
+   residue_step_biased(6, NL),  residue_step_biased(7, NL),  residue_step_biased(8, NL),                    \
+   residue_step_biased(9, NL),  residue_step_biased(10, NL), residue_step_biased(11, NL),                   \
+   residue_step_biased(12, NL), residue_step_biased(13, NL), residue_step_biased(14, NL),                   \
+   residue_step_biased(15, NL)}
+__constant__ ResidueStep kSteps3[kMaxModuli] = OZEMU_STEPS(3);
+__constant__ ResidueStep kSteps2[kMaxModuli] = OZEMU_STEPS(2);
+#undef OZEMU_STEPS
 
 // Byte offset of this lane's table word for the balanced residue of A'
 // modulo modulus L, relative to the table row of b = -h.  A table row is 128
@@ -136,17 +148,22 @@ __constant__ ResidueStep kSteps[kMaxModuli] = {
 // vb - m (0x4B000000 + floor(v/m)) = w + 0x4B000000 (1 - m) (mod 2^32), and
 // for odd m, 0x4B000000 (1 - m) 2^7 = 0 (mod 2^32), so the shifted value is
 // w's (m = 256 takes the low byte directly).
-template <int L>
+template <int L, int NL>
 __device__ __forceinline__ uint32_t residue_offset(uint32_t ulo, uint32_t uhi, uint32_t lane_hi) {
-  constexpr ResidueStep st = residue_step(L);
+  constexpr ResidueStep st = residue_step(L, NL);
+  const ResidueStep& ks = NL == 2 ? kSteps2[L] : kSteps3[L];
   uint32_t w;
   if constexpr (st.m == 256u) {
     w = (ulo & 0xFFu) ^ 0x80u;  // 2^63 = 0 (mod 256): b is the low byte of A', signed
+  } else if constexpr (st.m % 2 == 0) {
+    const uint32_t v = __dp4a(ulo, ks.clo, __dp4a(uhi, ks.chi, ks.bias));
+    constexpr uint32_t kMagic = static_cast<uint32_t>(((1ull << 32) + st.m - 1) / st.m);
+    w = v - __umulhi(v, kMagic) * st.m;
   } else {
     // vb = 0x4B000000 + v: the fp32 pattern of 2^23 + v (v < 2^23).
-    const uint32_t vb = __dp4a(ulo, kSteps[L].clo, __dp4a(uhi, kSteps[L].chi, kSteps[L].bias));
+    const uint32_t vb = __dp4a(ulo, ks.clo, __dp4a(uhi, ks.chi, ks.bias));
     const float vf = __uint_as_float(vb) - 8388608.0f;
-    const uint32_t qb = __float_as_uint(__fmaf_rd(vf, kSteps[L].inv_up, 8388608.0f));
+    const uint32_t qb = __float_as_uint(__fmaf_rd(vf, ks.inv_up, 8388608.0f));
     w = vb - qb * st.m;
   }
   return __funnelshift_l(lane_hi, w, kTableRowShift);
@@ -154,15 +171,15 @@ __device__ __forceinline__ uint32_t residue_offset(uint32_t ulo, uint32_t uhi, u
 
 // Codes of 8 elements for modulus L, packed and stored.  Lane i reads bank i
 // only, so a warp's lookups never conflict.
-template <int L, bool kRes8>
+template <int L, bool kRes8, int NL>
 __device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const uint32_t (&uhi)[8], const char* tb,
                                               uint32_t lane_hi, uint32_t* o, long long modulus_words) {
-  constexpr uint32_t kRow0 = residue_step(L).row * kTableRowBytes;
+  constexpr uint32_t kRow0 = residue_step(L, NL).row * kTableRowBytes;
   const char* t0 = tb + kRow0;
   uint32_t c[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    c[e] = *reinterpret_cast<const uint32_t*>(t0 + residue_offset<L>(ulo[e], uhi[e], lane_hi));
+    c[e] = *reinterpret_cast<const uint32_t*>(t0 + residue_offset<L, NL>(ulo[e], uhi[e], lane_hi));
   }
   if constexpr (kRes8) {
     uint2 w;
@@ -172,24 +189,25 @@ __device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const ui
   } else {
     uint32_t w0, w1, w2;
     pack8(c, w0, w1, w2);
-    // Limb j of a 128-element K block sits 64 j bytes after limb 0.
+    // Limb j of a 128-element K block sits 64 j bytes after limb 0 (two-limb
+    // moduli: the third limb is 0 and not stored).
     uint32_t* p = o + L * modulus_words;
     __stcs(p, w0);
     __stcs(p + 16, w1);
-    __stcs(p + 32, w2);
+    if constexpr (NL == 3) __stcs(p + 32, w2);
   }
 }
 
-template <bool kRes8, int... Ls>
+template <bool kRes8, int NL, int... Ls>
 __device__ __forceinline__ void all_moduli(std::integer_sequence<int, Ls...>, const uint32_t (&ulo)[8],
                                            const uint32_t (&uhi)[8], const char* tb, uint32_t lane_hi, uint32_t* o,
                                            long long modulus_words) {
-  (modulus_codes<Ls, kRes8>(ulo, uhi, tb, lane_hi, o, modulus_words), ...);
+  (modulus_codes<Ls, kRes8, NL>(ulo, uhi, tb, lane_hi, o, modulus_words), ...);
 }
 
 // Pass 2 of the row split over the row's elements: integers, residues and
 // limb codes (or residue bytes), packed and stored.
-template <int R, bool kRes8, bool kFast>
+template <int R, bool kRes8, int NL, bool kFast>
 __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s, const char* tb,
                                             uint32_t lane_hi, uint8_t* out_row, long long modulus_words) {
   for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
@@ -203,8 +221,8 @@ __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, 
       ulo[e] = static_cast<uint32_t>(u);
       uhi[e] = static_cast<uint32_t>(u >> 32);
     }
-    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : (k0 >> 7) * 192 + (k0 & 127) / 2));
-    all_moduli<kRes8>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_words);
+    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : (k0 >> 7) * (64 * NL) + (k0 & 127) / 2));
+    all_moduli<kRes8, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_words);
   }
 }
 
@@ -263,7 +281,7 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
 // kRes8 = false: FP4 limb planes [r][3][rows_p][k_p/2] (the FP4 path).
 // kRes8 = true: the balanced residues themselves as int8 [r][rows_p][k_p]
 // (input of the INT8 comparison GEMM).
-template <int R, bool kRes8>
+template <int R, bool kRes8, int NL>
 __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     split_rows_f64_kernel(const double* __restrict__ X, long long ldx, int rows, int k, int rows_p, int k_p, int p,
                           uint8_t* __restrict__ planes, int32_t* __restrict__ shifts, uint32_t* flags) {
@@ -283,7 +301,7 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
 
   // FP4 planes: a row holds the three limbs of each 128-element K block
   // side by side (3 x 64 bytes); moduli follow one another.
-  const long long row_bytes = kRes8 ? k_p : 3LL * k_p / 2;
+  const long long row_bytes = kRes8 ? k_p : static_cast<long long>(NL) * k_p / 2;
   const long long modulus_stride = static_cast<long long>(rows_p) * row_bytes;
   const int vec_ok = row_vector_width(X, ldx);
 
@@ -328,9 +346,9 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     // Pass 2: integers, residues, limbs.  Rows whose largest magnitude is
     // normal (with p <= 52) take the right-shift rounding.
     if (mh >= 0x00100000u && p <= 52)
-      split_pass2<R, kRes8, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
+      split_pass2<R, kRes8, NL, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
     else
-      split_pass2<R, kRes8, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
+      split_pass2<R, kRes8, NL, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
   }
 }
 
@@ -396,17 +414,29 @@ int split_grid(int rows_p) {
 
 }  // namespace
 
-template <int R, bool kRes8>
+template <int R, bool kRes8, int NL>
 cudaError_t launch_split_r(const double* X, long long ldx, int rows, int k, int p, uint8_t* planes, int32_t* shifts,
                            uint32_t* flags, cudaStream_t stream) {
   const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
   const size_t smem = static_cast<size_t>(kTableWords + 256) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R, kRes8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(split_rows_f64_kernel<R, kRes8, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  split_rows_f64_kernel<R, kRes8><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p,
+  split_rows_f64_kernel<R, kRes8, NL><<<split_grid(rows_p), kSplitThreads, smem, stream>>>(X, ldx, rows, k, rows_p, k_p,
                                                                                        p, planes, shifts, flags);
   return cudaGetLastError();
+}
+
+// Two-limb moduli only for FP4 planes (the INT8 comparison path takes the
+// 3-limb list).
+template <int R, bool kRes8>
+cudaError_t launch_split_limbs(const double* X, long long ldx, int rows, int k, int p, int limbs, uint8_t* planes,
+                               int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+  if (limbs == 3) return launch_split_r<R, kRes8, 3>(X, ldx, rows, k, p, planes, shifts, flags, stream);
+  if constexpr (!kRes8) {
+    if (limbs == 2) return launch_split_r<R, false, 2>(X, ldx, rows, k, p, planes, shifts, flags, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <bool kRes8>
@@ -415,7 +445,7 @@ cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, i
   switch (mods.r) {
 #define OZEMU_SPLIT_CASE(R) \
   case R:                   \
-    return launch_split_r<R, kRes8>(X, ldx, rows, k, p, planes, shifts, flags, stream);
+    return launch_split_limbs<R, kRes8>(X, ldx, rows, k, p, mods.limbs, planes, shifts, flags, stream);
     OZEMU_SPLIT_CASE(1) OZEMU_SPLIT_CASE(2) OZEMU_SPLIT_CASE(3) OZEMU_SPLIT_CASE(4) OZEMU_SPLIT_CASE(5)
     OZEMU_SPLIT_CASE(6) OZEMU_SPLIT_CASE(7) OZEMU_SPLIT_CASE(8) OZEMU_SPLIT_CASE(9) OZEMU_SPLIT_CASE(10)
     OZEMU_SPLIT_CASE(11) OZEMU_SPLIT_CASE(12) OZEMU_SPLIT_CASE(13) OZEMU_SPLIT_CASE(14) OZEMU_SPLIT_CASE(15)

@@ -72,6 +72,28 @@ def test_layout_sizes(oz):
     assert oz.ozemu_residue_bytes(1, 1, 17) == 0
 
 
+def test_two_limb_moduli_match_oracle(oz):
+    assert oz.ozemu_moduli_2limb(16) == oracle.moduli(16, oracle.MODULUS_CEILING_2LIMB)
+
+
+@pytest.mark.parametrize("k", [1, 2, 255, 256, 4096, 8192, 65536, 131071])
+@pytest.mark.parametrize("r", [1, 3, 8, 13, 16])
+def test_two_limb_bit_budget_matches_oracle(oz, k, r):
+    try:
+        _, pa, pb = oracle.bit_budget(k, r, oracle.MODULUS_CEILING_2LIMB)
+    except ValueError:
+        with pytest.raises(oz.OzemuError):
+            oz.ozemu_bit_budget_2limb(k, r)
+        return
+    assert oz.ozemu_bit_budget_2limb(k, r) == (pa, pb)
+
+
+def test_two_limb_layout_sizes(oz):
+    assert oz.ozemu_plane_bytes_2limb(1, 1, 1) == 2 * 128 * 64
+    assert oz.ozemu_plane_bytes_2limb(129, 300, 16) == 2 * 16 * 256 * 192
+    assert oz.ozemu_plane_bytes_2limb(1, 1, 17) == 0
+
+
 NULL = None
 FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
 
@@ -107,6 +129,14 @@ FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
     lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 4, 13, FAKE, 4, FAKE, 1, FAKE + 8, FAKE, FAKE, NULL),
     lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 200, 1, FAKE, 200, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # 2k >= M
     lambda oz: oz.ozemu_residues_narrow_f64(4, 1, 5, 16, FAKE, 5, FAKE, 1, FAKE, FAKE, FAKE, NULL),  # p_A > 52
+    lambda oz: oz.ozemu_dgemm_2limb(4, 4, 4, FAKE, 3, FAKE, 4, FAKE, 4, 16, NULL),  # lda < k
+    lambda oz: oz.ozemu_dgemm_2limb(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 17, NULL),  # r > 16
+    lambda oz: oz.ozemu_dgemm_2limb(4, 4, 4, FAKE, 4, FAKE, 4, NULL, 4, 16, NULL),  # null C
+    lambda oz: oz.ozemu_dgemm_2limb(4, 4, 60, FAKE, 60, FAKE, 4, FAKE, 4, 1, NULL),  # 2k >= 113
+    lambda oz: oz.ozemu_split_rows_f64_2limb(4, 4, FAKE, 4, 63, 16, FAKE, FAKE, NULL),  # p > 62
+    lambda oz: oz.ozemu_split_cols_f64_2limb(4, 4, FAKE, 3, 40, 16, FAKE, FAKE, NULL),  # ldx < cols
+    lambda oz: oz.ozemu_residue_gemm_2limb(4, 4, 4, 16, FAKE, FAKE, FAKE + 4, NULL),  # unaligned residues
+    lambda oz: oz.ozemu_crt_f64_2limb(4, 4, 0, FAKE, FAKE, FAKE, FAKE, 4, NULL),  # r < 1
 ])
 def test_invalid_arguments_rejected_on_host(oz, call):
     assert call(oz) == oz.OZEMU_ERR_INVALID_ARG
