@@ -27,6 +27,7 @@ constexpr int kTableRowShift = 7;
 constexpr int kTableRowBytes = 1 << kTableRowShift;
 constexpr int kTableWords = 256 * kTableRowBytes / 4;
 constexpr int kSplitBlocksPerSM = 2;  // 64 registers x 512 threads; 33 KiB of shared memory each
+constexpr int kPrefetchMaxK = 16384;  // longest row whose successor is prefetched into L2
 
 // Smallest-magnitude member of S = {0,+-1,+-2,+-3,+-4,+-6,+-8,+-12} in the
 // class c mod 13 (c in [0, 13)).  Classes 1 and 12 take 1 and -1.
@@ -210,7 +211,11 @@ __device__ __forceinline__ void all_moduli(std::integer_sequence<int, Ls...>, co
 template <int R, bool kRes8, int NL, bool kFast>
 __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s, const char* tb,
                                             uint32_t lane_hi, uint8_t* out_row, long long modulus_words) {
-  for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
+  // Backwards over the row: pass 1 read it forwards, so the most recently
+  // read part (the likeliest still in L2) comes first.
+  const int kfirst = threadIdx.x * kElemsPerThread;
+  const int klast = kfirst < k_p ? kfirst + ((k_p - 1 - kfirst) / kChunk) * kChunk : -1;
+  for (int k0 = klast; k0 >= kfirst; k0 -= kChunk) {
     uint64_t b[8];
     load8_f64(rowp, k, k0, vec_ok, b, true);
     uint32_t ulo[8], uhi[8];
@@ -336,8 +341,11 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     if (mh >= 0x7FF00000u && threadIdx.x == 0) atomicOr(flags, kFlagNonFinite);
     if (threadIdx.x == 0) shifts[row] = s;
 
-    // Bring this CTA's next row into L2 while this one is split.
-    if (row + static_cast<int>(gridDim.x) < rows) {
+    // Bring this CTA's next row into L2 while this one is split, when the
+    // current and next rows of every resident CTA fit in L2 together
+    // (2 x 304 CTAs x 16384 x 8 B = 80 MB); longer rows would evict the
+    // current row before pass 2 re-reads it.
+    if (k <= kPrefetchMaxK && row + static_cast<int>(gridDim.x) < rows) {
       const double* nrow = rowp + static_cast<long long>(gridDim.x) * ldx;
       for (int k0 = threadIdx.x * 16; k0 < k; k0 += kSplitThreads * 16)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + k0));
