@@ -214,10 +214,10 @@ def cpu_oracle(name, r, min_seconds, max_steps=0, sample=CPU_SAMPLE, shape=None)
 
 # ------------------------------------------------------------------ GPU arm
 
-def kernel_traffic(workload):
+def kernel_traffic(workload, chunks):
     """DRAM bytes per launch of the limb GEMM from the committed ncu record,
-    used only for the workload it was captured on and only while the kernel
-    sources are unchanged since the capture."""
+    used only for the workload and row chunking it was captured on and only
+    while the kernel sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "limb_gemm_traffic.json")
     if not os.path.exists(path):
         return None
@@ -227,7 +227,7 @@ def kernel_traffic(workload):
     for fn in ("gemm_fp4.cu", "common.cuh"):
         with open(os.path.join(ROOT, "ozaki_ii_fp64_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
-    if d.get("source_sha256") != h.hexdigest() or d.get("workload") != workload:
+    if d.get("source_sha256") != h.hexdigest() or d.get("workload") != workload or d.get("chunks") != chunks:
         return None
     return d
 
@@ -439,7 +439,7 @@ def run_gpu(args):
         t_roof = bytes_alg / (pk["hbm_gbs"] * 1e9)
     else:
         achieved = fp4_flop / (dom_ms / 1e3) / 1e12
-        tr = kernel_traffic(workload_name(args, spec))
+        tr = kernel_traffic(workload_name(args, spec), nch)
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
                     "traffic": (int(tr["bytes_per_launch"]) if tr else None),
@@ -657,7 +657,7 @@ def run_gpu(args):
         iflop = 2.0 * 4096 ** 3
         leg = {"ms": round(ig_ms, 3), "tops": round(iflop / (ig_ms / 1e3) / 1e12, 1),
                "fp4_frac": round(9 * iflop / (ig_ms / 1e3) / 1e12 / fp4_peak, 4),
-               "launches": "split A, transpose B, split B^T, limb GEMM (int32 epilogue)"}
+               "launches": "split A rows, split B columns, limb GEMM (int32 epilogue)"}
         if hasattr(torch, "_int_mm"):
             ref = torch._int_mm(Ai, Bi)
             torch.cuda.synchronize(dev)

@@ -656,12 +656,8 @@ int ozemu_split_cols_s8(int k, int cols, const int8_t* X, int ldx, uint8_t* plan
   DeviceState* d = nullptr;
   int s = device_state(&d);
   if (s != OZEMU_OK) return s;
-  uint8_t* ws = nullptr;
-  s = workspace(d, align256(static_cast<size_t>(k > 0 ? k : 1) * cols), &ws);
-  if (s != OZEMU_OK) return s;
-  int8_t* t = reinterpret_cast<int8_t*>(ws);
-  if (k > 0 && launch_transpose_s8(X, ldx, k, cols, t, k, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
-  return cuda_status(launch_split_rows_s8(t, k > 0 ? k : 1, cols, k, planes, stream));
+  if (k == 0) return cuda_status(cudaMemsetAsync(planes, 0, plane_bytes(cols, 0, 1), stream));
+  return cuda_status(launch_split_cols_s8(X, ldx, k, cols, planes, stream));
 }
 
 size_t ozemu_res8_bytes(int rows, int k, int r) {
@@ -794,16 +790,22 @@ int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B, int32_
   if (s != OZEMU_OK) return s;
   if (k == 0) return cuda_status(launch_zero_s32(C32, m, n, n, stream));
   const size_t pa = align256(plane_bytes(m, k, 1)), pb = align256(plane_bytes(n, k, 1));
-  const size_t bt = align256(static_cast<size_t>(k) * n);
   uint8_t* ws = nullptr;
-  s = workspace(d, pa + pb + bt, &ws);
+  s = workspace(d, pa + pb, &ws);
   if (s != OZEMU_OK) return s;
   uint8_t* ap = ws;
   uint8_t* bp = ws + pa;
-  int8_t* btr = reinterpret_cast<int8_t*>(ws + pa + pb);
-  if (launch_split_rows_s8(A, k, m, k, ap, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
-  if (launch_transpose_s8(B, n, k, n, btr, k, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
-  if (launch_split_rows_s8(btr, k, n, k, bp, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  // The two splits are small and latency-bound: A's rows on a helper stream
+  // beside B's columns on the caller's stream.
+  s = pipeline_state(d);
+  if (s != OZEMU_OK) return s;
+  cudaStream_t xs = d->copy_stream;
+  if (cudaEventRecord(d->ev[0], stream) != cudaSuccess || cudaStreamWaitEvent(xs, d->ev[0], 0) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  if (launch_split_rows_s8(A, k, m, k, ap, xs) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (cudaEventRecord(d->ev[1], xs) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (launch_split_cols_s8(B, n, k, n, bp, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (cudaStreamWaitEvent(stream, d->ev[1], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
   return limb_gemm_s32(m, n, k, ap, bp, C32, n, d, stream);
 }
 

@@ -20,8 +20,10 @@ cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k
                                  cudaStream_t stream);
 cudaError_t launch_transpose_f64(const double* in, long long ldin, int rows, int cols, double* out,
                                  long long ldout, cudaStream_t stream);
-cudaError_t launch_transpose_s8(const int8_t* in, long long ldin, int rows, int cols, int8_t* out, long long ldout,
-                                cudaStream_t stream);
+// INT8 limb planes of the columns of X (k x cols, row-major, k >= 1): plane
+// row j holds column j.
+cudaError_t launch_split_cols_s8(const int8_t* X, long long ldx, int k, int cols, uint8_t* planes,
+                                 cudaStream_t stream);
 
 // FP4 limb GEMM (gemm_fp4.cu).  Residue mode writes uint8 [r][m][ldr]
 // residues; int mode (r = 1) writes int32 C32 with leading dimension ldc.

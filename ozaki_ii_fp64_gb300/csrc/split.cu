@@ -395,6 +395,59 @@ __global__ void __launch_bounds__(kSplitThreads) split_rows_s8_kernel(const int8
   }
 }
 
+// INT8 limb planes of the columns of X (k x cols, row-major): column j
+// becomes plane row j, without a transposed copy.  One CTA per (128-element
+// K block, 64 columns): the block is staged in shared memory as it lies in
+// X (coalesced 4-byte loads along the rows), each thread forms the codes of
+// 32 consecutive K elements of one column, and the 4 lanes of a column write
+// its 64-byte run of each limb with one 16-byte store each.  Padding columns
+// (cols <= j < cols_p) and K elements (k <= e < k_p) get code 0.
+constexpr int kColTile = 64;
+constexpr int kColPitch = kColTile + 4;  // bytes per staged K row
+
+__global__ void __launch_bounds__(256) split_cols_s8_kernel(const int8_t* __restrict__ X, long long ldx, int k,
+                                                            int cols, int k_p, uint8_t* __restrict__ planes) {
+  __shared__ uint32_t lut[256];
+  __shared__ __align__(16) uint8_t tile[128 * kColPitch];
+  lut[threadIdx.x] = limb_code(static_cast<int>(threadIdx.x) - 128);
+  const int c0 = blockIdx.x * kColTile;
+  const int kb = blockIdx.y;
+  const bool vec = ((reinterpret_cast<uintptr_t>(X) & 3u) == 0) && ((ldx & 3) == 0) && (c0 + kColTile <= cols);
+  for (int w = threadIdx.x; w < 128 * (kColTile / 4); w += 256) {
+    const int i = w / (kColTile / 4), q = w % (kColTile / 4);
+    const int kr = kb * 128 + i;
+    uint32_t v = 0;
+    if (kr < k) {
+      const int8_t* src = X + static_cast<long long>(kr) * ldx + c0 + 4 * q;
+      if (vec) {
+        v = __ldg(reinterpret_cast<const unsigned int*>(src));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c0 + 4 * q + e < cols) v |= static_cast<uint32_t>(static_cast<uint8_t>(src[e])) << (8 * e);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(tile + i * kColPitch + 4 * q) = v;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int col = (threadIdx.x >> 5) * 8 + (lane >> 2);  // column within the tile, 0..63
+  const int q = lane & 3;                                // K elements 32 q .. 32 q + 31 of the block
+  uint32_t w[3][4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint32_t c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      c[e] = lut[static_cast<int>(static_cast<int8_t>(tile[(q * 32 + g * 8 + e) * kColPitch + col])) + 128];
+    pack8(c, w[0][g], w[1][g], w[2][g]);
+  }
+  uint8_t* o = planes + static_cast<long long>(c0 + col) * (3LL * k_p / 2) + kb * 192 + q * 16;
+#pragma unroll
+  for (int l = 0; l < 3; ++l)
+    *reinterpret_cast<uint4*>(o + l * 64) = make_uint4(w[l][0], w[l][1], w[l][2], w[l][3]);
+}
+
 // out[c][r] = in[r][c] for a rows x cols block of 32 x 32 tiles.
 template <typename T>
 __global__ void transpose_kernel(const T* __restrict__ in, long long ldin, int rows, int cols, T* __restrict__ out,
@@ -482,17 +535,19 @@ cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k
   return cudaGetLastError();
 }
 
+cudaError_t launch_split_cols_s8(const int8_t* X, long long ldx, int k, int cols, uint8_t* planes,
+                                 cudaStream_t stream) {
+  const int cols_p = round_up(cols, kRowAlign), k_p = round_up(k, kKAlign);
+  if (k_p / 128 > 65535) return cudaErrorInvalidValue;  // grid.y limit
+  dim3 grid(cols_p / kColTile, k_p / 128);
+  split_cols_s8_kernel<<<grid, 256, 0, stream>>>(X, ldx, k, cols, k_p, planes);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_transpose_f64(const double* in, long long ldin, int rows, int cols, double* out,
                                  long long ldout, cudaStream_t stream) {
   dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
   transpose_kernel<double><<<grid, block, 0, stream>>>(in, ldin, rows, cols, out, ldout);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_s8(const int8_t* in, long long ldin, int rows, int cols, int8_t* out, long long ldout,
-                                cudaStream_t stream) {
-  dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
-  transpose_kernel<int8_t><<<grid, block, 0, stream>>>(in, ldin, rows, cols, out, ldout);
   return cudaGetLastError();
 }
 

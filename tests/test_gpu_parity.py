@@ -81,6 +81,23 @@ def test_split_cols_f64_parity(oz, k, cols, p, r):
     assert (codes[:, :, cols:, :] == 0).all() and (codes[:, :, :, k:] == 0).all()
 
 
+@pytest.mark.parametrize("k,cols,pad", [(300, 256, 0), (1000, 200, 3), (129, 64, 1), (4096, 130, 0)])
+def test_split_cols_s8_direct(oz, k, cols, pad):
+    # Column split without a transposed copy: 4-byte loads when the rows are
+    # 4-byte aligned and the 64-column tile is full, byte loads otherwise.
+    rng = np.random.default_rng(k + cols)
+    B = rng.integers(-128, 128, size=(k, cols), dtype=np.int8)
+    B[0, :] = -128
+    B[:, -1] = 127
+    Bd = torch.zeros((k, cols + pad), dtype=torch.int8, device=DEV)
+    Bd[:, :cols] = to_dev(B)
+    planes = oz.split_cols_s8(Bd[:, :cols])
+    status_ok(oz)
+    digits, codes = decode_planes(planes.cpu().numpy(), cols, k, 1)
+    assert (digits[0, :, :cols, :k] == oracle.limb_digits(B.T)).all()
+    assert (codes[:, :, cols:, :] == 0).all() and (codes[:, :, :, k:] == 0).all()
+
+
 def test_split_s8_parity(oz):
     A, B = make_pair(150, 90, 333, seed=3, dist="int8")
     A[0, :] = -128
