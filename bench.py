@@ -725,12 +725,33 @@ def run_gpu(args):
                                                              C2.data_ptr(), n, sh), "crt 2"))]
             stage_times(stages2)
             st_ms = stage_times(stages2)
+            e2e2 = None
+            if not args.no_e2e:
+                # End to end with host buffers (pinned), as the e2e entry above.
+                def e2e2_step():
+                    check(oz.ozemu_dgemm_host_2limb(m, n, k, A_pin.data_ptr(), k, B_pin.data_ptr(), n,
+                                                    C_pin.data_ptr(), n, r2, sh), "dgemm_host_2limb")
+
+                e2e2_step()
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(3):
+                    e2e2_step()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                e2_ms = e0.elapsed_time(e1) / 3
+                if not torch.equal(C_pin.view(torch.int64), C2.cpu().view(torch.int64)):
+                    raise SystemExit("two-limb e2e result differs from the device result")
+                e2e2 = {"value": round(flop / (e2_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+                        "ms_per_step": round(e2_ms, 3), "steps": 3}
             g2_tflops = 4.0 * r2 * flop / (st_ms["limb_gemm"] / 1e3) / 1e12
             line["two_limb"] = {
                 "r": r2, "bit_budget": pA2 + pB2, "three_limb_bit_budget": P3,
                 "fp4_gemms": 4 * r2, "three_limb_fp4_gemms": 9 * r, "ms": round(t2, 3),
                 "tflops": round(flop / (t2 / 1e3) / 1e12, 2), "status": int(st2),
-                "stage_ms": {kk: round(v, 3) for kk, v in st_ms.items()},
+                "stage_ms": {kk: round(v, 3) for kk, v in st_ms.items()}, "e2e": e2e2,
                 "limb_gemm_roofline": {"bound": "tensor", "achieved": round(g2_tflops, 1),
                                        "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                                        "frac": round(g2_tflops / fp4_peak, 4),

@@ -329,6 +329,12 @@ int ozemu_crt_f64_2limb(int m, int n, int r, const uint8_t* residues, const int3
 int ozemu_dgemm_2limb(int m, int n, int k, const double* A, int lda, const double* B,
                       int ldb, double* C, int ldc, int r, cudaStream_t stream);
 
+/* ozemu_dgemm_2limb with HOST buffers, pipelined like ozemu_dgemm_host (same
+ * stream and synchronisation rules); the result equals ozemu_dgemm_2limb's
+ * bit for bit. */
+int ozemu_dgemm_host_2limb(int m, int n, int k, const double* A, int lda, const double* B,
+                           int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

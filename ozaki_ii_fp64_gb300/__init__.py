@@ -75,6 +75,7 @@ _SIGNATURES = {
     "ozemu_residue_gemm_2limb": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
     "ozemu_crt_f64_2limb": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P]),
     "ozemu_dgemm_2limb": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
+    "ozemu_dgemm_host_2limb": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
 }
 
 
@@ -248,6 +249,10 @@ def ozemu_crt_f64_2limb(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream):
 
 def ozemu_dgemm_2limb(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
     return _call("ozemu_dgemm_2limb", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
+
+
+def ozemu_dgemm_host_2limb(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
+    return _call("ozemu_dgemm_host_2limb", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
 
 
 # ------------------------------------------------------- torch marshalling
@@ -458,6 +463,22 @@ def dgemm_2limb(A, B, r, out=None, stream=None):
     C = torch.empty((m, n), dtype=torch.float64, device=A.device) if out is None else out
     _check(ozemu_dgemm_2limb(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
                              _stream(stream)), "ozemu_dgemm_2limb")
+    return C
+
+
+def dgemm_host_2limb(A, B, r, out=None, stream=None):
+    """ozemu_dgemm_host_2limb of CPU float64 tensors (pinned for overlap);
+    returns the CPU result after synchronising the stream."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2 or A.device.type != "cpu" or B.device.type != "cpu":
+        raise ValueError("expected CPU matrices with matching inner dimension")
+    C = torch.empty((m, n), dtype=torch.float64, pin_memory=A.is_pinned()) if out is None else out
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(ozemu_dgemm_host_2limb(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
+                                  s.cuda_stream), "ozemu_dgemm_host_2limb")
+    s.synchronize()
     return C
 
 

@@ -894,6 +894,31 @@ int ozemu_crt_f64_2limb(int m, int n, int r, const uint8_t* residues, const int3
   return crt_entry(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream, 2);
 }
 
+int ozemu_dgemm_host_2limb(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C,
+                           int ldc, int r, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (k > 0 && ozemu_bit_budget_2limb(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  s = pipeline_state(d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) {
+    uint8_t* buf = nullptr;
+    s = workspace(d, align256(static_cast<size_t>(m) * n * 8), &buf);
+    if (s != OZEMU_OK) return s;
+    double* Cd = reinterpret_cast<double*>(buf);
+    if (launch_zero_f64(Cd, m, n, n, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+    return cuda_status(cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 8, Cd, n * 8, static_cast<size_t>(n) * 8, m,
+                                         cudaMemcpyDeviceToHost, stream));
+  }
+  return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, true, d, stream, 2);
+}
+
 int ozemu_dgemm_2limb(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
                       int r, cudaStream_t stream) {
   if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;

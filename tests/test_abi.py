@@ -137,6 +137,8 @@ FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
     lambda oz: oz.ozemu_split_cols_f64_2limb(4, 4, FAKE, 3, 40, 16, FAKE, FAKE, NULL),  # ldx < cols
     lambda oz: oz.ozemu_residue_gemm_2limb(4, 4, 4, 16, FAKE, FAKE, FAKE + 4, NULL),  # unaligned residues
     lambda oz: oz.ozemu_crt_f64_2limb(4, 4, 0, FAKE, FAKE, FAKE, FAKE, 4, NULL),  # r < 1
+    lambda oz: oz.ozemu_dgemm_host_2limb(4, 4, 60, FAKE, 60, FAKE, 4, FAKE, 4, 1, NULL),  # 2k >= 113
+    lambda oz: oz.ozemu_dgemm_host_2limb(4, 4, 4, FAKE, 4, FAKE, 4, NULL, 4, 16, NULL),  # null C
 ])
 def test_invalid_arguments_rejected_on_host(oz, call):
     assert call(oz) == oz.OZEMU_ERR_INVALID_ARG

@@ -209,3 +209,24 @@ def test_two_limb_and_three_limb_agree_within_bound(oz):
     status_ok(oz)
     assert oracle.error_bound_ratio(A, B, C2) <= 1.0
     assert oracle.error_bound_ratio(A, B, C3) <= 1.0
+
+
+@pytest.mark.parametrize("m,n,k,r", [(300, 200, 500, 16), (4100, 4200, 200, 16), (3, 5, 0, 16)])
+def test_dgemm_host_two_limb_matches_device(oz, m, n, k, r):
+    # Host buffers through the pipelined copies (B in two column blocks and
+    # uneven row chunks for the larger shape): the same bits as the device
+    # entry point, and the oracle's on sampled rows.
+    A, B = make_pair(m, n, k, seed=m + n + k, dist="wide")
+    A_pin = torch.from_numpy(A).pin_memory()
+    B_pin = torch.from_numpy(B).pin_memory()
+    C = oz.dgemm_host_2limb(A_pin, B_pin, r).numpy()
+    status_ok(oz)
+    Cd = oz.dgemm_2limb(to_dev(A), to_dev(B), r).cpu().numpy()
+    status_ok(oz)
+    assert (C.view(np.int64) == Cd.view(np.int64)).all()
+    if k == 0:
+        assert (C == 0).all()
+        return
+    rows = np.unique(np.concatenate([sample_indices(m, 12, seed=k), [m - 1]]))
+    Cref = oracle.dgemm_block(A, B, r, rows=rows, ceiling=CEIL)
+    assert (C[rows].view(np.int64) == Cref.view(np.int64)).all()
