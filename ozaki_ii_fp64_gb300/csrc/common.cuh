@@ -306,6 +306,14 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&a)[16], uint32_t (&
       :
       : "memory");
 }
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&a)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+        "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+      :
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x N columns of 32-bit words: register i holds column i of the

@@ -22,6 +22,14 @@
 // each chunk the epilogue folds D1 + 169 D2 into a running value kept in a
 // third TMEM region and the MMAs restart the accumulators.
 //
+// Two-limb moduli (m <= 113, residues in [-56, 56], digits |d0| <= 8,
+// |d1| <= 4, no third limb): 4 products per K step.  The CTA-pair kernel
+// folds all four into one accumulator, D = A0B0 + 13 (A0B1 + A1B0) +
+// 169 A1B1 (A1's scale 26 in both of its products), which grows by at most
+// 64 + 2 * 13 * 32 + 169 * 16 = 3600 per K element and so stays exact over
+// chunks of 4096; with 224 columns per tile two accumulators fit in TMEM and
+// alternate between tiles.  The single-CTA kernel keeps D1 and D2.
+//
 // The epilogue copies the accumulators to registers and releases them at
 // once, so the next chunk's (or tile's) MMAs overlap the modular arithmetic
 // and the stores; the TMA producer runs ahead across tiles through the
@@ -503,9 +511,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2);
   uint64_t* empty = full + kStages2;
+  // Accumulator hand-off, per TMEM buffer (two-limb moduli: two buffers).
   uint64_t* tfull = empty + kStages2;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* mma_done = tempty + 1;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -513,14 +522,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_rank();
   const bool leader = (rank == 0);
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  // Three-limb moduli: D1 and D2 fill 448 of the 512 TMEM columns, one tile
+  // at a time.  Two-limb moduli: one accumulator D = D1 + 169 D2 per tile
+  // (exact for K chunks of 4096), so two tiles' accumulators alternate and
+  // the MMAs of one round run while the epilogue drains the other.
+  constexpr int kBufs = NL == 2 ? 2 : 1;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStages2; ++s) {
       mbar_init(&full[s], 1);   // armed by the first CTA with both CTAs' bytes
       mbar_init(&empty[s], 1);  // one commit from the pair's MMA issuer
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 2 * kEpiWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * kEpiWarps);
+    }
     mbar_init(mma_done, 1);
     *abort_word = 0;
     fence_mbar_init();
@@ -603,13 +619,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // g counts accumulation rounds: one per K chunk of each tile.
       for (int t = pair; t < args.total_tiles && ok; t += npairs) {
         for (int kc0 = 0; kc0 < kb_total && ok; kc0 += args.kc_blocks, ++g) {
-          if (g > 0) {
-            if (!mbar_wait(tempty, (g - 1) & 1, abort_word, args.flags)) {
+          // Round g fills buffer g % kBufs for its (g / kBufs)-th time; the
+          // epilogue must have released that buffer's previous round.
+          const int buf = g % kBufs, use = g / kBufs;
+          if (use > 0) {
+            if (!mbar_wait(&tempty[buf], (use - 1) & 1, abort_word, args.flags)) {
               ok = false;
               break;
             }
             tc_fence_after();
           }
+          const uint32_t dacc = tbase + static_cast<uint32_t>(buf * kBN2);  // two-limb accumulator
           const int kc1 = kc0 + args.kc_blocks < kb_total ? kc0 + args.kc_blocks : kb_total;
           for (int kb = kc0; kb < kc1; ++kb, ++it) {
             const int s = it % kStages2;
@@ -641,18 +661,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mma_fp4_pair_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
                 mma_fp4_pair(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
               } else {
-                // D1 = A0B0 + 13 (A0B1 + A1B0), D2 = A1B1 (weight 169 at the drain).
-                mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
-                mma_fp4_pair_lastuse(d1, a0, b1, idesc, s2, s26, 1u);   // 13
-                mma_fp4_pair_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
-                mma_fp4_pair_lastuse(d2, a1, b1, idesc, s2, s2, acc);   // 1 (in D2)
+                // One accumulator D = A0B0 + 13 (A0B1 + A1B0) + 169 A1B1: A1
+                // carries the scale 26 in both of its products.
+                mma_fp4_pair_fill(dacc, a0, b0, idesc, s2, s2, acc);       // 1
+                mma_fp4_pair_lastuse(dacc, a0, b1, idesc, s2, s26, 1u);    // 13
+                mma_fp4_pair_fill(dacc, a1, b0, idesc, s26, s2, 1u);       // 13
+                mma_fp4_pair_lastuse(dacc, a1, b1, idesc, s26, s26, 1u);   // 169
               }
               if (ks == 0)
                 known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
             }
             tc_commit_pair_multicast(&empty[s], 0x3);
           }
-          if (ok) tc_commit_pair_multicast(tfull, 0x3);
+          if (ok) tc_commit_pair_multicast(&tfull[buf], 0x3);
         }
       }
       tc_commit_pair_multicast(mma_done, 0x1);
@@ -671,7 +692,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int half = ew >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = static_cast<uint32_t>(half * CW);
-    const uint32_t tempty_leader = mapa_shared(tempty, 0);
     int g = 0;  // accumulation rounds, as counted by the MMA issuer
     bool live = true;
     for (int t = pair; t < args.total_tiles && live; t += npairs) {
@@ -684,11 +704,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t packed[CW / 4];
       for (int kc0 = 0; kc0 < kb_total; kc0 += args.kc_blocks, ++g) {
         const bool first = (kc0 == 0);
-        if (!warp_wait(tfull, g & 1, abort_word, args.flags)) {
+        const int buf = g % kBufs, use = g / kBufs;
+        if (!warp_wait(&tfull[buf], use & 1, abort_word, args.flags)) {
           live = false;
           break;
         }
         tc_fence_after();
+        if constexpr (NL == 2) {
+          // One accumulator, |D| < 3600 * 4096 < 2^24: one reduction modulo m.
+          const uint32_t dcol = tbase + lane_off + static_cast<uint32_t>(buf * kBN2) + col0;
+          uint32_t v1[kSlice], n1[kSlice];
+          tmem_ld_cols<kSlice>(dcol, n1);
+#pragma unroll
+          for (int c = 0; c < CW; c += kSlice) {
+            tmem_wait_ld_regs(n1);
+#pragma unroll
+            for (int i = 0; i < kSlice; ++i) v1[i] = n1[i];
+            if (c + kSlice < CW) tmem_ld_cols<kSlice>(dcol + c + kSlice, n1);
+#pragma unroll
+            for (int i = 0; i < kSlice; i += 4) {
+              uint32_t b[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float v = fmod_small(__uint_as_float(v1[i + e]), fm, finv);
+                v = v < 0.f ? v + fm : v;
+                if (!first) {
+                  v += __uint_as_float(__byte_perm(packed[(c + i) / 4], 0x4B000000u, 0x7650u | (e & 3))) - 8388608.0f;
+                  v = v >= fm ? v - fm : v;
+                }
+                b[e] = byte_of_float(v);
+              }
+              packed[(c + i) / 4] =
+                  __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+          continue;
+        }
         // Slice c + 1 is loaded from TMEM while slice c is folded.
         uint32_t v1[kSlice], v2[kSlice], n1[kSlice], n2[kSlice];
         tmem_ld_cols<kSlice>(tbase + lane_off + kColD1p + col0, n1);
@@ -748,7 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_leader);
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
       }
       if (kInt || !live || grow >= args.m) continue;
       uint8_t* rrow = args.res_out + (static_cast<long long>(l) * args.m + grow) * args.ldr;
@@ -852,7 +906,8 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   a.m = c.m;
   a.n = c.n;
   a.kb_total = k_p / 128;
-  a.kc_blocks = c.kc_blocks;
+  // Two-limb moduli: one accumulator, exact for chunks of 4096 (32 blocks).
+  a.kc_blocks = (NL == 2 && c.kc_blocks > 32) ? 32 : c.kc_blocks;
   a.rows_a_p = rows_a_p;
   a.rows_b_p = rows_b_p;
   a.tiles_m2 = (c.m + 255) / 256;

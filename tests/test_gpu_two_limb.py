@@ -102,7 +102,8 @@ def test_residue_gemm_two_limb_parity(oz, m, n, k, r, dist):
     assert (C.cpu().numpy().view(np.int64) == Cref.view(np.int64)).all()
 
 
-@pytest.mark.parametrize("m,n,k,r", [(200, 150, 300, 16), (513, 257, 4000, 15), (130, 250, 20000, 12)])
+@pytest.mark.parametrize("m,n,k,r", [(200, 150, 300, 16), (513, 257, 4000, 15), (256, 230, 4097, 16),
+                                     (130, 250, 20000, 12)])
 def test_two_limb_pair_and_single_cta_gemm_agree(oz, m, n, k, r, monkeypatch):
     # CTA-pair and single-CTA kernels, each with the 4-product schedule; for
     # k > 8192 both accumulate exact chunks and add their residues.
