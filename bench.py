@@ -34,6 +34,7 @@ from workloads import WORKLOADS, make_pair  # noqa: E402
 METRIC = "emulated DGEMM TFLOP/s (2MNK/t) and % of FP4 roofline at 1 GB300"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 NARROW_MAX_K = 1 << 24       # k limit of the fused narrow path
+PAIR_TILE_COLS = 224         # output columns of the library's CTA-pair GEMM tile
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CPU_SAMPLE = 128        # sampled rows and columns of C per oracle step
 CPU_MIN_SECONDS = 10.0  # bounded CPU baseline: repeat the sample at least this long
@@ -214,7 +215,7 @@ def cpu_oracle(name, r, min_seconds, max_steps=0, sample=CPU_SAMPLE, shape=None)
 
 # ------------------------------------------------------------------ GPU arm
 
-def kernel_traffic(workload, chunks):
+def kernel_traffic(workload, chunks, bblocks):
     """DRAM bytes per launch of the limb GEMM from the committed ncu record,
     used only for the workload and row chunking it was captured on and only
     while the kernel sources are unchanged since the capture."""
@@ -227,7 +228,7 @@ def kernel_traffic(workload, chunks):
     for fn in ("gemm_fp4.cu", "common.cuh"):
         with open(os.path.join(ROOT, "ozaki_ii_fp64_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
-    if d.get("source_sha256") != h.hexdigest() or d.get("workload") != workload or d.get("chunks") != chunks:
+    if d.get("source_sha256") != h.hexdigest() or d.get("workload") != workload or d.get("chunks") != chunks or d.get("b_blocks") != bblocks:
         return None
     return d
 
@@ -317,29 +318,54 @@ def run_gpu(args):
         dominant = "limb_gemm"
         launches_per_step = 5  # split rows, transpose, split rows of B^T, limb GEMM, CRT
 
-    # The timed step.  Limb-plane path: the stage calls pipelined over row
-    # chunks of A on three streams -- B's split, then each chunk's split
-    # (split stream), limb GEMM (main stream, bracketed by events) and CRT
-    # (CRT stream, beside the next chunk's GEMM); the same schedule as the
-    # library's host-buffer entry point.  Narrow path: its two calls in order.
+    # The timed step.  Limb-plane path: the library's device-operand schedule
+    # with the stage calls, on three streams -- B in two column blocks (the
+    # first a whole number of 224-column pair tiles) and A in row chunks:
+    # split B's first block (main stream), then each chunk's rows and, after
+    # the first half of A, B's second block (split stream); the limb GEMM of
+    # each (chunk, block) product on the main stream, bracketed by events;
+    # each product's CRT on the CRT stream beside the next GEMM.  The first
+    # chunks' products with B's first block run before those with its second.
+    # Narrow path: its two calls in order.
     chunks = 1 if narrow else max(1, args.chunks)
     crows = m if chunks == 1 else ((m + chunks - 1) // chunks + 255) // 256 * 256
+    bsplit = (n // 2) // PAIR_TILE_COLS * PAIR_TILE_COLS if (not narrow and n >= 4096) else n
+    bblocks = [(0, bsplit)] + ([(bsplit, n - bsplit)] if bsplit < n else [])
+    nbc = len(bblocks)
+    bbufs = [(col0, w, torch.empty(oz.ozemu_plane_bytes(w, k, r), dtype=torch.uint8, device=dev),
+              torch.empty(w, dtype=torch.int32, device=dev)) for col0, w in bblocks]
     chunk_bufs = []
     for row0 in range(0, m, crows):
         mc = min(crows, m - row0)
         chunk_bufs.append((row0, mc, torch.empty(oz.ozemu_plane_bytes(mc, k, r), dtype=torch.uint8, device=dev),
                            torch.empty(mc, dtype=torch.int32, device=dev),
-                           torch.empty(oz.ozemu_residue_bytes(mc, n, r), dtype=torch.uint8, device=dev)))
+                           [torch.empty(oz.ozemu_residue_bytes(mc, w, r), dtype=torch.uint8, device=dev)
+                            for _, w in bblocks]))
     nch = len(chunk_bufs)
+    nfirst = nch  # chunks covering the first half of A's rows
+    if nbc > 1:
+        nfirst = 1
+        while nfirst < nch and 2 * chunk_bufs[nfirst][0] < m:
+            nfirst += 1
+    order = [(c, 0) for c in range(nfirst)] + [(c, j) for j in range(1, nbc) for c in range(nfirst)] + \
+        [(c, j) for c in range(nfirst, nch) for j in range(nbc)]
     s_split = torch.cuda.Stream(dev)
     s_crt = torch.cuda.Stream(dev)
     ev_start = torch.cuda.Event()
+    ev_b0 = torch.cuda.Event()
     evA = [torch.cuda.Event() for _ in range(nch)]
-    evG = [torch.cuda.Event() for _ in range(nch)]
-    evC = [torch.cuda.Event() for _ in range(nch)]
+    evB = [torch.cuda.Event() for _ in range(nbc)]
+    evG = [torch.cuda.Event() for _ in order]
+    ev_crt_done = torch.cuda.Event()
     if not narrow:
-        launches_per_step = 2 + 3 * nch  # transpose + split of B; per chunk split, limb GEMM, CRT
-    n_dominant = 1 if narrow else nch
+        # transpose + split per B block; per chunk its split; per product its limb GEMM and CRT
+        launches_per_step = 2 * nbc + nch + 2 * len(order)
+    n_dominant = 1 if narrow else len(order)
+
+    def split_b_block(j, st):
+        col0, w, bpj, sbj = bbufs[j]
+        check(oz.ozemu_split_cols_f64(k, w, B.data_ptr() + col0 * 8, n, pB, r, bpj.data_ptr(), sbj.data_ptr(), st),
+              "split B block")
 
     def step(gev=None):
         if narrow:
@@ -351,27 +377,39 @@ def run_gpu(args):
             crt()
             return
         ev_start.record(stream)
-        s_split.wait_event(ev_start)
         s_crt.wait_event(ev_start)
-        split_b()
-        for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
+        split_b_block(0, sh)
+        # The column splits share the library's transposed-copy scratch, so
+        # the split stream starts after B's first block.
+        ev_b0.record(stream)
+        s_split.wait_event(ev_b0)
+        for c, (row0, mc, apc, sac, _) in enumerate(chunk_bufs):
             check(oz.ozemu_split_rows_f64(mc, k, A.data_ptr() + row0 * k * 8, k, pA, r, apc.data_ptr(),
                                           sac.data_ptr(), s_split.cuda_stream), "split A chunk")
             evA[c].record(s_split)
-        for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
-            stream.wait_event(evA[c])
+            if c == nfirst - 1:
+                for j in range(1, nbc):
+                    split_b_block(j, s_split.cuda_stream)
+                    evB[j].record(s_split)
+        for i, (c, j) in enumerate(order):
+            row0, mc, apc, sac, resl = chunk_bufs[c]
+            col0, w, bpj, sbj = bbufs[j]
+            if j == 0:
+                stream.wait_event(evA[c])
+            if j > 0 and c == 0:
+                stream.wait_event(evB[j])
             if gev is not None:
-                gev[c][0].record(stream)
-            check(oz.ozemu_residue_gemm(mc, n, k, r, apc.data_ptr(), bp.data_ptr(), resc.data_ptr(), sh),
-                  "limb gemm chunk")
+                gev[i][0].record(stream)
+            check(oz.ozemu_residue_gemm(mc, w, k, r, apc.data_ptr(), bpj.data_ptr(), resl[j].data_ptr(), sh),
+                  "limb gemm product")
             if gev is not None:
-                gev[c][1].record(stream)
-            evG[c].record(stream)
-            s_crt.wait_event(evG[c])
-            check(oz.ozemu_crt_f64(mc, n, r, resc.data_ptr(), sac.data_ptr(), sb.data_ptr(),
-                                   C.data_ptr() + row0 * n * 8, n, s_crt.cuda_stream), "crt chunk")
-            evC[c].record(s_crt)
-        stream.wait_event(evC[nch - 1])
+                gev[i][1].record(stream)
+            evG[i].record(stream)
+            s_crt.wait_event(evG[i])
+            check(oz.ozemu_crt_f64(mc, w, r, resl[j].data_ptr(), sac.data_ptr(), sbj.data_ptr(),
+                                   C.data_ptr() + (row0 * n + col0) * 8, n, s_crt.cuda_stream), "crt product")
+        ev_crt_done.record(s_crt)
+        stream.wait_event(ev_crt_done)
 
     def stage_times(which):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(which) + 1)]
@@ -382,6 +420,10 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         return {name: evs[i].elapsed_time(evs[i + 1]) for i, (name, _) in enumerate(which)}
 
+    if not narrow:
+        # Grow the library's cached workspace to the full-width column split
+        # once, so that no later call (timed or staged) reallocates it.
+        split_b()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -439,7 +481,7 @@ def run_gpu(args):
         t_roof = bytes_alg / (pk["hbm_gbs"] * 1e9)
     else:
         achieved = fp4_flop / (dom_ms / 1e3) / 1e12
-        tr = kernel_traffic(workload_name(args, spec), nch)
+        tr = kernel_traffic(workload_name(args, spec), nch, nbc)
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
                     "traffic": (int(tr["bytes_per_launch"]) if tr else None),
@@ -459,7 +501,7 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args, spec), "m": m, "n": n, "k": k, "r": r, "dist": spec["dist"],
                        "seed": spec["seed"], "path": "narrow (fused)" if narrow else "limb planes",
-                       "row_chunks": nch,
+                       "row_chunks": nch, "b_column_blocks": nbc,
                        "l2": "inputs larger than L2 (%d MiB per operand), no flush" % (m * k * 8 >> 20)},
             "pct_fp4_roofline" if not narrow else "pct_io_roofline": round(pct_roof, 2), "roofline": roofline,
             "stage_ms": {kk: round(v, 3) for kk, v in stage_ms.items()},

@@ -389,10 +389,13 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   row0s[nch] = m;
   int chunk = 0;  // tallest chunk (sizes the per-chunk buffers)
   for (int c = 0; c < nch; ++c) chunk = row0s[c + 1] - row0s[c] > chunk ? row0s[c + 1] - row0s[c] : chunk;
-  // With host operands B comes over in blocks of columns, so that the first
-  // products start once its first block is in and split.
-  const int bcols = (from_host && n >= 4096) ? round_up((n + 1) / 2, 256) : n;
-  const int nbc = (n + bcols - 1) / bcols;
+  // B is taken in two blocks of columns, so that the first products start
+  // once its first block is in (host operands) and split.  The first
+  // block is a whole number of pair tiles (224 columns), so that the split
+  // adds no partially filled tile column.
+  const int bsplit = n >= 4096 ? (n / 2) / kPairTileCols * kPairTileCols : n;
+  const int nbc = bsplit < n ? 2 : 1;
+  const int bcols = nbc > 1 && n - bsplit > bsplit ? n - bsplit : bsplit;  // widest block (sizes the buffers)
   const size_t szA = from_host ? align256(static_cast<size_t>(m) * k * 8) : 0;
   const size_t szB = from_host ? align256(static_cast<size_t>(k) * n * 8) : 0;
   const size_t szC = from_host ? align256(static_cast<size_t>(m) * n * 8) : 0;
@@ -401,15 +404,16 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   const size_t szAp = align256(plane_bytes(chunk, k, r, limbs)), szSa = align256(static_cast<size_t>(chunk) * 4);
   const size_t szRes = align256(ozemu_residue_bytes(chunk, bcols, r));
   uint8_t* buf = nullptr;
-  s = workspace(d, szA + szB + szC + szBt + nbc * (szBp + szSb) + nch * (szAp + szSa + nbc * szRes), &buf);
+  s = workspace(d, szA + szB + szC + nbc * (szBt + szBp + szSb) + nch * (szAp + szSa + nbc * szRes), &buf);
   if (s != OZEMU_OK) return s;
   // Operands on the device: copies in the workspace, or the caller's buffers.
   const double* Ad = from_host ? reinterpret_cast<const double*>(buf) : A;
   const double* Bd = from_host ? reinterpret_cast<const double*>(buf + szA) : B;
   double* Cd = from_host ? reinterpret_cast<double*>(buf + szA + szB) : C;
   const long long ldad = from_host ? k : lda, ldbd = from_host ? n : ldb, ldcd = from_host ? n : ldc;
-  double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
-  uint8_t* per_bblock = buf + szA + szB + szC + szBt;           // [nbc] planes + shifts of B's column blocks
+  // [nbc] transposed copies of B's column blocks (their splits may overlap), then their planes and shifts.
+  uint8_t* bt_base = buf + szA + szB + szC;
+  uint8_t* per_bblock = bt_base + nbc * szBt;
   uint8_t* per_chunk = per_bblock + nbc * (szBp + szSb);       // [nch] planes + shifts of A's rows, residues
   cudaStream_t cs = d->copy_stream, xs = d->crt_stream, ss = d->split_stream;
   cudaEvent_t* ev = d->ev;
@@ -419,25 +423,36 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   static_assert(evSA + kMaxChunks <= kHostEvents, "event slots");
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   const CrtModuli cm = crt_moduli(r, limbs);
-  auto bcol0 = [&](int j) { return j * bcols; };
-  auto bwidth = [&](int j) { return n - j * bcols < bcols ? n - j * bcols : bcols; };
+  auto bcol0 = [&](int j) { return j == 0 ? 0 : bsplit; };
+  auto bwidth = [&](int j) { return j == 0 ? bsplit : n - bsplit; };
   auto bplanes = [&](int j) { return per_bblock + j * (szBp + szSb); };
   auto bshifts = [&](int j) { return reinterpret_cast<int32_t*>(per_bblock + j * (szBp + szSb) + szBp); };
   // Host operands: each block of B is split on the split stream as soon as
   // it is in, beside the products of earlier blocks; device operands: B is
   // split on the caller's stream before the first product.
+  auto btmp = [&](int j) { return reinterpret_cast<double*>(bt_base + j * szBt); };
+  // Host operands: each block of B is copied in, then split on the split
+  // stream as soon as it is in, beside the products of earlier blocks.
+  // Device operands: block 0 is split on the caller's stream before the
+  // first product, later blocks on the copy stream after the row chunks
+  // that come before them.
   auto copy_b = [&](int j) {
+    if (!from_host)
+      return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), btmp(j), d, cs,
+                            limbs) == OZEMU_OK &&
+             cudaEventRecord(ev[evSB + j], cs) == cudaSuccess;
     return cudaMemcpy2DAsync(const_cast<double*>(Bd) + bcol0(j), static_cast<size_t>(n) * 8, B + bcol0(j),
                              static_cast<size_t>(ldb) * 8, static_cast<size_t>(bwidth(j)) * 8, k, h2d, cs) ==
                    cudaSuccess &&
            cudaEventRecord(ev[evB + j], cs) == cudaSuccess && cudaStreamWaitEvent(ss, ev[evB + j], 0) == cudaSuccess &&
-           split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), Bt, d, ss,
+           split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), btmp(j), d, ss,
                           limbs) == OZEMU_OK &&
            cudaEventRecord(ev[evSB + j], ss) == cudaSuccess;
   };
   auto split_b = [&](int j) -> int {
-    if (from_host) return cudaStreamWaitEvent(stream, ev[evSB + j], 0) == cudaSuccess ? OZEMU_OK : OZEMU_ERR_CUDA;
-    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), Bt, d, stream,
+    if (from_host || j > 0)
+      return cudaStreamWaitEvent(stream, ev[evSB + j], 0) == cudaSuccess ? OZEMU_OK : OZEMU_ERR_CUDA;
+    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), btmp(j), d, stream,
                           limbs);
   };
   if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
@@ -473,7 +488,7 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
       if (s != OZEMU_OK) return s;
       if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
     }
-    if (c == nfirst - 1 && from_host)
+    if (c == nfirst - 1)
       for (int j = 1; j < nbc; ++j)
         if (!copy_b(j)) return OZEMU_ERR_CUDA;
   }

@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // chunk is an accumulation round whose residues the epilogue adds, modulo
 // m_l, to the ones it keeps in registers (four per register).
 // ---------------------------------------------------------------------------
-constexpr int kBN2 = 224;                        // pair tile N
+constexpr int kBN2 = kPairTileCols;              // pair tile N (224)
 constexpr int kBHalf = kBN2 / 2;                 // B rows per CTA
 constexpr int kBTile2 = kBHalf * kBKBytes;       // 7168 B
 constexpr int kStage2 = 3 * kATile + 3 * kBTile2;

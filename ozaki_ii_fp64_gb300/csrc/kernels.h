@@ -52,6 +52,9 @@ cudaError_t launch_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_r
 // Fused deconstruction + product for narrow B (gemv.cu): residues of
 // C = A B for n <= kNarrowMaxN columns without limb planes.  Writes the
 // residues [r][m][ldr] and shifts that launch_crt_f64 consumes.
+// Output columns of one CTA-pair limb-GEMM tile (gemm_fp4.cu).
+constexpr int kPairTileCols = 224;
+
 constexpr int kNarrowMaxN = 2;
 constexpr int kNarrowMaxK = 1 << 24;
 constexpr int kNarrowMaxP = 52;  // p_A: scaled elements are right shifts of the significand
