@@ -34,7 +34,6 @@ from workloads import WORKLOADS, make_pair  # noqa: E402
 METRIC = "emulated DGEMM TFLOP/s (2MNK/t) and % of FP4 roofline at 1 GB300"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 NARROW_MAX_K = 1 << 24       # k limit of the fused narrow path
-PAIR_TILE_COLS = 224         # output columns of the library's CTA-pair GEMM tile
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CPU_SAMPLE = 128        # sampled rows and columns of C per oracle step
 CPU_MIN_SECONDS = 10.0  # bounded CPU baseline: repeat the sample at least this long
@@ -319,53 +318,29 @@ def run_gpu(args):
         launches_per_step = 5  # split rows, transpose, split rows of B^T, limb GEMM, CRT
 
     # The timed step.  Limb-plane path: the library's device-operand schedule
-    # with the stage calls, on three streams -- B in two column blocks (the
-    # first a whole number of 224-column pair tiles) and A in row chunks:
-    # split B's first block (main stream), then each chunk's rows and, after
-    # the first half of A, B's second block (split stream); the limb GEMM of
-    # each (chunk, block) product on the main stream, bracketed by events;
-    # each product's CRT on the CRT stream beside the next GEMM.  The first
-    # chunks' products with B's first block run before those with its second.
-    # Narrow path: its two calls in order.
+    # with the stage calls, pipelined over row chunks of A on three streams --
+    # B's split (main stream), each chunk's split (split stream, from the
+    # start), limb GEMM (main stream, bracketed by events) and CRT (CRT
+    # stream, beside the next chunk's GEMM).  Narrow path: its two calls in
+    # order.
     chunks = 1 if narrow else max(1, args.chunks)
     crows = m if chunks == 1 else ((m + chunks - 1) // chunks + 255) // 256 * 256
-    bsplit = (n // 2) // PAIR_TILE_COLS * PAIR_TILE_COLS if (not narrow and n >= 4096) else n
-    bblocks = [(0, bsplit)] + ([(bsplit, n - bsplit)] if bsplit < n else [])
-    nbc = len(bblocks)
-    bbufs = [(col0, w, torch.empty(oz.ozemu_plane_bytes(w, k, r), dtype=torch.uint8, device=dev),
-              torch.empty(w, dtype=torch.int32, device=dev)) for col0, w in bblocks]
     chunk_bufs = []
     for row0 in range(0, m, crows):
         mc = min(crows, m - row0)
         chunk_bufs.append((row0, mc, torch.empty(oz.ozemu_plane_bytes(mc, k, r), dtype=torch.uint8, device=dev),
                            torch.empty(mc, dtype=torch.int32, device=dev),
-                           [torch.empty(oz.ozemu_residue_bytes(mc, w, r), dtype=torch.uint8, device=dev)
-                            for _, w in bblocks]))
+                           torch.empty(oz.ozemu_residue_bytes(mc, n, r), dtype=torch.uint8, device=dev)))
     nch = len(chunk_bufs)
-    nfirst = nch  # chunks covering the first half of A's rows
-    if nbc > 1:
-        nfirst = 1
-        while nfirst < nch and 2 * chunk_bufs[nfirst][0] < m:
-            nfirst += 1
-    order = [(c, 0) for c in range(nfirst)] + [(c, j) for j in range(1, nbc) for c in range(nfirst)] + \
-        [(c, j) for c in range(nfirst, nch) for j in range(nbc)]
     s_split = torch.cuda.Stream(dev)
     s_crt = torch.cuda.Stream(dev)
     ev_start = torch.cuda.Event()
-    ev_b0 = torch.cuda.Event()
     evA = [torch.cuda.Event() for _ in range(nch)]
-    evB = [torch.cuda.Event() for _ in range(nbc)]
-    evG = [torch.cuda.Event() for _ in order]
-    ev_crt_done = torch.cuda.Event()
+    evG = [torch.cuda.Event() for _ in range(nch)]
+    evC = [torch.cuda.Event() for _ in range(nch)]
     if not narrow:
-        # transpose + split per B block; per chunk its split; per product its limb GEMM and CRT
-        launches_per_step = 2 * nbc + nch + 2 * len(order)
-    n_dominant = 1 if narrow else len(order)
-
-    def split_b_block(j, st):
-        col0, w, bpj, sbj = bbufs[j]
-        check(oz.ozemu_split_cols_f64(k, w, B.data_ptr() + col0 * 8, n, pB, r, bpj.data_ptr(), sbj.data_ptr(), st),
-              "split B block")
+        launches_per_step = 2 + 3 * nch  # transpose + split of B; per chunk split, limb GEMM, CRT
+    n_dominant = 1 if narrow else nch
 
     def step(gev=None):
         if narrow:
@@ -377,39 +352,28 @@ def run_gpu(args):
             crt()
             return
         ev_start.record(stream)
+        s_split.wait_event(ev_start)
         s_crt.wait_event(ev_start)
-        split_b_block(0, sh)
-        # The column splits share the library's transposed-copy scratch, so
-        # the split stream starts after B's first block.
-        ev_b0.record(stream)
-        s_split.wait_event(ev_b0)
-        for c, (row0, mc, apc, sac, _) in enumerate(chunk_bufs):
+        split_b()
+        for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
             check(oz.ozemu_split_rows_f64(mc, k, A.data_ptr() + row0 * k * 8, k, pA, r, apc.data_ptr(),
                                           sac.data_ptr(), s_split.cuda_stream), "split A chunk")
             evA[c].record(s_split)
-            if c == nfirst - 1:
-                for j in range(1, nbc):
-                    split_b_block(j, s_split.cuda_stream)
-                    evB[j].record(s_split)
-        for i, (c, j) in enumerate(order):
-            row0, mc, apc, sac, resl = chunk_bufs[c]
-            col0, w, bpj, sbj = bbufs[j]
-            if j == 0:
-                stream.wait_event(evA[c])
-            if j > 0 and c == 0:
-                stream.wait_event(evB[j])
+        for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
+            stream.wait_event(evA[c])
             if gev is not None:
-                gev[i][0].record(stream)
-            check(oz.ozemu_residue_gemm(mc, w, k, r, apc.data_ptr(), bpj.data_ptr(), resl[j].data_ptr(), sh),
-                  "limb gemm product")
+                gev[c][0].record(stream)
+            check(oz.ozemu_residue_gemm(mc, n, k, r, apc.data_ptr(), bp.data_ptr(), resc.data_ptr(), sh),
+                  "limb gemm chunk")
             if gev is not None:
-                gev[i][1].record(stream)
-            evG[i].record(stream)
-            s_crt.wait_event(evG[i])
-            check(oz.ozemu_crt_f64(mc, w, r, resl[j].data_ptr(), sac.data_ptr(), sbj.data_ptr(),
-                                   C.data_ptr() + (row0 * n + col0) * 8, n, s_crt.cuda_stream), "crt product")
-        ev_crt_done.record(s_crt)
-        stream.wait_event(ev_crt_done)
+                gev[c][1].record(stream)
+            evG[c].record(stream)
+            s_crt.wait_event(evG[c])
+            check(oz.ozemu_crt_f64(mc, n, r, resc.data_ptr(), sac.data_ptr(), sb.data_ptr(),
+                                   C.data_ptr() + row0 * n * 8, n, s_crt.cuda_stream), "crt chunk")
+            evC[c].record(s_crt)
+        stream.wait_event(evC[nch - 1])
+    nbc = 1  # B whole (column blocks are for host operands)
 
     def stage_times(which):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(which) + 1)]

@@ -178,7 +178,6 @@ struct DeviceState {
   // Host-buffer product: a copy stream, a CRT stream and their events.
   cudaStream_t copy_stream = nullptr;
   cudaStream_t crt_stream = nullptr;
-  cudaStream_t split_stream = nullptr;  // host operands: splits as soon as each block is in
   cudaEvent_t ev[kHostEvents] = {};
 };
 constexpr int kMaxDevices = 64;
@@ -352,22 +351,21 @@ int pipeline_state(DeviceState* d) {
   if (d->copy_stream) return OZEMU_OK;
   if (cudaStreamCreateWithFlags(&d->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return OZEMU_ERR_CUDA;
   if (cudaStreamCreateWithFlags(&d->crt_stream, cudaStreamNonBlocking) != cudaSuccess) return OZEMU_ERR_CUDA;
-  if (cudaStreamCreateWithFlags(&d->split_stream, cudaStreamNonBlocking) != cudaSuccess) return OZEMU_ERR_CUDA;
   for (int i = 0; i < kHostEvents; ++i)
     if (cudaEventCreateWithFlags(&d->ev[i], cudaEventDisableTiming) != cudaSuccess) return OZEMU_ERR_CUDA;
   return OZEMU_OK;
 }
 
 // C = A B over row chunks of A, each an independent product A_c B, pipelined
-// on the caller's stream and helper streams.  With host buffers (from_host):
-// the copy stream brings B's column blocks and A's row chunks in; the split
-// stream splits each of them as soon as it is in; the caller's stream runs
-// the limb GEMMs; the CRT stream runs each product's CRT beside the next
-// GEMM; the copy stream sends each block of C out as soon as it is ready.
-// With device buffers the caller's stream splits B first and the copy stream
-// splits the chunks' rows ahead of the GEMMs.  The caller's stream completes
-// after the last CRT (device) or copy out (host); the helper streams start
-// after everything the caller queued before.
+// on the caller's stream and two helper streams.  With host buffers
+// (from_host): the copy stream brings B in, then A_0, A_1, ...; the caller's
+// stream splits B's columns, then per chunk splits its rows and runs the limb
+// GEMM; the CRT stream runs each chunk's CRT beside the next chunk's GEMM;
+// the copy stream sends each chunk of C out as soon as it is ready.  With
+// device buffers the helper stream splits the chunks' rows ahead of the GEMMs
+// instead.  The caller's stream completes after the last CRT (device) or
+// copy out (host); the helper streams start after everything the caller
+// queued before.
 constexpr int kMaxChunks = 8;
 
 int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc, int r,
@@ -389,11 +387,11 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   row0s[nch] = m;
   int chunk = 0;  // tallest chunk (sizes the per-chunk buffers)
   for (int c = 0; c < nch; ++c) chunk = row0s[c + 1] - row0s[c] > chunk ? row0s[c + 1] - row0s[c] : chunk;
-  // B is taken in two blocks of columns, so that the first products start
-  // once its first block is in (host operands) and split.  The first
+  // With host operands B comes over in two blocks of columns, so that the
+  // first products start once its first block is in and split.  The first
   // block is a whole number of pair tiles (224 columns), so that the split
   // adds no partially filled tile column.
-  const int bsplit = n >= 4096 ? (n / 2) / kPairTileCols * kPairTileCols : n;
+  const int bsplit = (from_host && n >= 4096) ? (n / 2) / kPairTileCols * kPairTileCols : n;
   const int nbc = bsplit < n ? 2 : 1;
   const int bcols = nbc > 1 && n - bsplit > bsplit ? n - bsplit : bsplit;  // widest block (sizes the buffers)
   const size_t szA = from_host ? align256(static_cast<size_t>(m) * k * 8) : 0;
@@ -404,59 +402,38 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   const size_t szAp = align256(plane_bytes(chunk, k, r, limbs)), szSa = align256(static_cast<size_t>(chunk) * 4);
   const size_t szRes = align256(ozemu_residue_bytes(chunk, bcols, r));
   uint8_t* buf = nullptr;
-  s = workspace(d, szA + szB + szC + nbc * (szBt + szBp + szSb) + nch * (szAp + szSa + nbc * szRes), &buf);
+  s = workspace(d, szA + szB + szC + szBt + nbc * (szBp + szSb) + nch * (szAp + szSa + nbc * szRes), &buf);
   if (s != OZEMU_OK) return s;
   // Operands on the device: copies in the workspace, or the caller's buffers.
   const double* Ad = from_host ? reinterpret_cast<const double*>(buf) : A;
   const double* Bd = from_host ? reinterpret_cast<const double*>(buf + szA) : B;
   double* Cd = from_host ? reinterpret_cast<double*>(buf + szA + szB) : C;
   const long long ldad = from_host ? k : lda, ldbd = from_host ? n : ldb, ldcd = from_host ? n : ldc;
-  // [nbc] transposed copies of B's column blocks (their splits may overlap), then their planes and shifts.
-  uint8_t* bt_base = buf + szA + szB + szC;
-  uint8_t* per_bblock = bt_base + nbc * szBt;
+  double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
+  uint8_t* per_bblock = buf + szA + szB + szC + szBt;           // [nbc] planes + shifts of B's column blocks
   uint8_t* per_chunk = per_bblock + nbc * (szBp + szSb);       // [nch] planes + shifts of A's rows, residues
-  cudaStream_t cs = d->copy_stream, xs = d->crt_stream, ss = d->split_stream;
+  cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
   cudaEvent_t* ev = d->ev;
-  // Copied (evB, evA) and split (evSB, evSA) events of B's blocks (nbc <= 2) and A's chunks.
-  constexpr int evStart = 0, evB = 1, evA = 3, evG = 3 + kMaxChunks, evC = evG + 1, evD = evC + 1;
-  constexpr int evSB = evD + 1, evSA = evSB + 2;
-  static_assert(evSA + kMaxChunks <= kHostEvents, "event slots");
+  constexpr int evStart = 0, evB = 1, evA = 3, evG = 3 + kMaxChunks, evC = evG + 1, evD = evC + 1;  // nbc <= 2
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   const CrtModuli cm = crt_moduli(r, limbs);
   auto bcol0 = [&](int j) { return j == 0 ? 0 : bsplit; };
   auto bwidth = [&](int j) { return j == 0 ? bsplit : n - bsplit; };
   auto bplanes = [&](int j) { return per_bblock + j * (szBp + szSb); };
   auto bshifts = [&](int j) { return reinterpret_cast<int32_t*>(per_bblock + j * (szBp + szSb) + szBp); };
-  // Host operands: each block of B is split on the split stream as soon as
-  // it is in, beside the products of earlier blocks; device operands: B is
-  // split on the caller's stream before the first product.
-  auto btmp = [&](int j) { return reinterpret_cast<double*>(bt_base + j * szBt); };
-  // Host operands: each block of B is copied in, then split on the split
-  // stream as soon as it is in, beside the products of earlier blocks.
-  // Device operands: block 0 is split on the caller's stream before the
-  // first product, later blocks on the copy stream after the row chunks
-  // that come before them.
   auto copy_b = [&](int j) {
-    if (!from_host)
-      return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), btmp(j), d, cs,
-                            limbs) == OZEMU_OK &&
-             cudaEventRecord(ev[evSB + j], cs) == cudaSuccess;
     return cudaMemcpy2DAsync(const_cast<double*>(Bd) + bcol0(j), static_cast<size_t>(n) * 8, B + bcol0(j),
                              static_cast<size_t>(ldb) * 8, static_cast<size_t>(bwidth(j)) * 8, k, h2d, cs) ==
                    cudaSuccess &&
-           cudaEventRecord(ev[evB + j], cs) == cudaSuccess && cudaStreamWaitEvent(ss, ev[evB + j], 0) == cudaSuccess &&
-           split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), btmp(j), d, ss,
-                          limbs) == OZEMU_OK &&
-           cudaEventRecord(ev[evSB + j], ss) == cudaSuccess;
+           cudaEventRecord(ev[evB + j], cs) == cudaSuccess;
   };
   auto split_b = [&](int j) -> int {
-    if (from_host || j > 0)
-      return cudaStreamWaitEvent(stream, ev[evSB + j], 0) == cudaSuccess ? OZEMU_OK : OZEMU_ERR_CUDA;
-    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), btmp(j), d, stream,
+    if (from_host && cudaStreamWaitEvent(stream, ev[evB + j], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
+    return split_cols_f64(k, bwidth(j), Bd + bcol0(j), ldbd, pb_bits, r, bplanes(j), bshifts(j), Bt, d, stream,
                           limbs);
   };
   if (cudaEventRecord(ev[evStart], stream) != cudaSuccess || cudaStreamWaitEvent(cs, ev[evStart], 0) != cudaSuccess ||
-      cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess || cudaStreamWaitEvent(ss, ev[evStart], 0) != cudaSuccess)
+      cudaStreamWaitEvent(xs, ev[evStart], 0) != cudaSuccess)
     return OZEMU_ERR_CUDA;
   // Copy stream: B's first block, the first nfirst row chunks of A, B's other
   // block, A's other rows (device operands: the splits of A's rows).  The
@@ -470,25 +447,18 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   for (int c = 0; c < nch; ++c) {
     const int row0 = row0s[c], mc = row0s[c + 1] - row0;
     if (from_host) {
-      // The chunk's copy, then its split on the split stream.
-      uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
       if (cudaMemcpy2DAsync(const_cast<double*>(Ad) + static_cast<size_t>(row0) * k, k * 8,
                             A + static_cast<size_t>(row0) * lda, static_cast<size_t>(lda) * 8,
-                            static_cast<size_t>(k) * 8, mc, h2d, cs) != cudaSuccess ||
-          cudaEventRecord(ev[evA + c], cs) != cudaSuccess || cudaStreamWaitEvent(ss, ev[evA + c], 0) != cudaSuccess)
+                            static_cast<size_t>(k) * 8, mc, h2d, cs) != cudaSuccess)
         return OZEMU_ERR_CUDA;
-      s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, reinterpret_cast<int32_t*>(ap + szAp), d, ss,
-                         limbs);
-      if (s != OZEMU_OK) return s;
-      if (cudaEventRecord(ev[evSA + c], ss) != cudaSuccess) return OZEMU_ERR_CUDA;
     } else {
       uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
       s = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, reinterpret_cast<int32_t*>(ap + szAp), d, cs,
                          limbs);
       if (s != OZEMU_OK) return s;
-      if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
     }
-    if (c == nfirst - 1)
+    if (cudaEventRecord(ev[evA + c], cs) != cudaSuccess) return OZEMU_ERR_CUDA;
+    if (c == nfirst - 1 && from_host)
       for (int j = 1; j < nbc; ++j)
         if (!copy_b(j)) return OZEMU_ERR_CUDA;
   }
@@ -498,8 +468,13 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
     const int row0 = row0s[c], mc = row0s[c + 1] - row0;
     uint8_t* ap = per_chunk + c * (szAp + szSa + nbc * szRes);
     int32_t* sap = reinterpret_cast<int32_t*>(ap + szAp);
-    if (j == 0 && cudaStreamWaitEvent(stream, ev[from_host ? evSA + c : evA + c], 0) != cudaSuccess)
-      return OZEMU_ERR_CUDA;
+    if (j == 0) {
+      if (cudaStreamWaitEvent(stream, ev[evA + c], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
+      if (from_host) {
+        const int st = split_rows_f64(mc, k, Ad + row0 * ldad, ldad, pa_bits, r, ap, sap, d, stream, limbs);
+        if (st != OZEMU_OK) return st;
+      }
+    }
     const int col0 = bcol0(j), nc = bwidth(j);
     uint8_t* res = ap + szAp + szSa + j * szRes;
     const int st = residue_gemm(mc, nc, k, r, ap, bplanes(j), res, d, stream, limbs);
