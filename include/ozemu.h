@@ -108,10 +108,9 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
  * (m x n, ldc) are row-major host pointers; the result is the same as
  * ozemu_dgemm's, bit for bit.  The copies in and out are pipelined with the
  * work: column blocks of B and row chunks of A are copied on a copy stream
- * and deconstructed on a split stream as soon as each is in, while earlier
- * (chunk, block) products run on `stream`; each product's CRT runs on a
- * further stream beside the next product, and each finished block of C is
- * copied out at once.  Page-locked (pinned) host buffers are needed for
+ * while earlier blocks and chunks are deconstructed and multiplied on
+ * `stream`; each (chunk, block) product's CRT runs on a second stream beside
+ * the next product, and each finished block of C is copied out at once.  Page-locked (pinned) host buffers are needed for
  * the copies to overlap; pageable ones give the same result, serialised.
  * All work is ordered after what `stream` already holds, and `stream`
  * completes only after C is on the host: synchronise `stream` (or call
