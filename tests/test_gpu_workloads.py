@@ -75,6 +75,41 @@ def test_workload_parity_sampled(oz, name, n_rows, n_cols):
     assert ratio <= 1.0
 
 
+@pytest.mark.parametrize("name,r,n_rows,n_cols", [
+    ("dgemm_8192_wide", 16, 8, 8),
+    ("dgemm_4096_k65536", 14, 6, 6),
+])
+def test_workload_two_limb_sampled(oz, name, r, n_rows, n_cols):
+    # The two-limb moduli (<= 113) at full size, with the smallest r whose
+    # bit budget reaches the three-limb r's: the device entry point and the
+    # stage calls agree bit for bit, and sampled entries equal the oracle's
+    # at the same modulus ceiling and meet the bound.
+    A_h, B_h, spec = workload_inputs(name)
+    m, n, k = spec["m"], spec["n"], spec["k"]
+    ceil = oracle.MODULUS_CEILING_2LIMB
+    assert sum(oracle.bit_budget(k, r, ceil)[1:]) >= sum(oracle.bit_budget(k, spec["r"])[1:])
+    A = torch.from_numpy(A_h).to(DEV)
+    B = torch.from_numpy(B_h).to(DEV)
+    C = oz.dgemm_2limb(A, B, r)
+    assert oz.get_status() == oz.OZEMU_OK
+    pA, pB = oz.ozemu_bit_budget_2limb(k, r)
+    ap, sa = oz.split_rows_f64_2limb(A, pA, r)
+    bp, sb = oz.split_cols_f64_2limb(B, pB, r)
+    res = oz.residue_gemm_2limb(m, n, k, r, ap, bp)
+    Cs = oz.crt_f64_2limb(m, n, r, res, sa, sb)
+    assert oz.get_status() == oz.OZEMU_OK
+    assert torch.equal(C.view(torch.int64), Cs.view(torch.int64))
+    del ap, bp, A, B, Cs
+    rows = sample_indices(m, n_rows, seed=21)
+    cols = sample_indices(n, n_cols, seed=22)
+    Cref, st = oracle.dgemm_block(A_h, B_h, r, rows=rows, cols=cols, stages=True, ceiling=ceil)
+    got_res = res[:, rows][:, :, cols].cpu().numpy().astype(np.int64)
+    assert (got_res == st["res"]).all()
+    Cg = C.cpu().numpy()[np.ix_(rows, cols)]
+    assert (Cg.view(np.int64) == Cref.view(np.int64)).all()
+    assert oracle.error_bound_ratio(A_h[rows], B_h[:, cols], Cg) <= 1.0
+
+
 def test_igemm_s8_4096_full(oz):
     A_h, B_h, spec = workload_inputs("igemm_s8_4096")
     C = oz.igemm_s8(torch.from_numpy(A_h).to(DEV), torch.from_numpy(B_h).to(DEV))
