@@ -152,6 +152,15 @@ def test_dgemm_two_limb_shapes(oz, m, n, k, r, dist):
         assert oracle.error_bound_ratio(A, B, C) <= 1.0
 
 
+@pytest.mark.parametrize("m,n,k,r", [(20, 30, 40, 1), (33, 70, 100, 2), (65, 17, 300, 3), (40, 90, 500, 5),
+                                     (130, 80, 1000, 8), (50, 66, 700, 11)])
+def test_dgemm_two_limb_few_moduli(oz, m, n, k, r):
+    # Small r: the CRT's word counts (bytes of W_l, 16-bit positions, limbs of
+    # C') change with the bit length of M; every instance against the oracle.
+    A, B = make_pair(m, n, k, seed=m + n + k + r, dist="normal")
+    check_dgemm(oz, A, B, r)
+
+
 def test_dgemm_two_limb_k1_correctly_rounded(oz):
     # r = 16 two-limb moduli leave p_A = p_B = 51 bits at k = 1, so operands
     # with at most 51 significant bits pass exactly and C = fl(A B).
