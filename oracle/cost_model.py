@@ -11,9 +11,14 @@ match native fp64 whatever the tensor-core throughput.
 
 Reading (units are not printed): c_q is instructions per input element per
 modulus, P_int integer instructions per second, P_fp64 native fp64 flop/s,
-8 the bytes of one fp64 input.  Pin: tests solve "deconstruction time equals
-native fp64 time" by bisection and compare with the closed form.  The B300
-value 0.56 flop/B is parity unpinned: none of its constituents is printed.
+8 the bytes of one fp64 input.  Pins (tests/test_oracle_pins.py): the closed
+form equals the crossing point of the deconstruction time and native fp64
+time found by bisection, both from :func:`deconstruction_time` alone and
+through the full :func:`tme_time` with unbounded tensor and HBM rates; each
+term of :func:`tme_time` is recovered when the others vanish; and the fourth
+term's share of a dense n^3 product halves when n doubles (the page's "dense
+GEMM is unaffected").  The B300 value 0.56 flop/B is parity unpinned: none of
+its constituents is printed.
 """
 
 

@@ -28,7 +28,10 @@ e2m1 definition; exhaustive int8 limb round trip; greedy moduli by brute force;
 vectorised rounding against exact Fractions; CRT round trips and brute force on
 small moduli; limb GEMMs against a triple loop and closed forms; the modular
 recombination against a direct modular product; the full product against the
-exact rational product, the error bound and exactly representable cases.
+exact rational product, the error bound and exactly representable cases;
+single roundings in the subnormal range (hand-derived values where one
+rounding and two differ) and at the overflow threshold; the sliced exact
+product against Fraction sums, including heavy cancellation.
 """
 
 from fractions import Fraction
@@ -506,3 +509,169 @@ def error_bound_ratio(A, B, C, rows=None, cols=None):
         ratio = np.where(bound > 0, res / np.where(bound > 0, bound, 1.0),
                          np.where(res == 0, 0.0, np.inf))
     return float(ratio.max()) if ratio.size else 0.0
+
+
+# ----------------------------------------------------------------------------
+# The exact product at full size: error-free slices summed by float64 BLAS
+# ----------------------------------------------------------------------------
+#
+# The bound check needs sum_k A_ik B_kj exactly for whole rows and columns of
+# the largest workloads, where Fractions are far too slow.  Every fp64 value
+# is a dyadic rational, so the product can be taken exactly in pieces: each
+# row of A (column of B) is cut into slices whose entries are integers below
+# 2^beta times one power of two per row and slice, with beta chosen so that
+# K 2^(2 beta) <= 2^53.  Every partial sum of a slice-by-slice product is then
+# an integer below 2^53 and float64 BLAS returns it exactly, in any summation
+# order.  The exact product is the sum of those exact terms, each scaled by a
+# power of two; the residual sum - C is rounded once with math.fsum.  Pinned
+# against the Fraction sums above (tests/test_oracle_pins.py).
+
+def _slice_beta(k):
+    """Bits per slice entry: the largest beta with k 2^(2 beta) <= 2^53."""
+    beta = 26
+    while k * 2 ** (2 * beta) > 2 ** 53:
+        beta -= 1
+    if beta < 1:
+        raise ValueError("k too large for exact float64 slices")
+    return beta
+
+
+def _slices(X, beta, max_slices=80):
+    """Cut the rows of X into slices: X = sum_s Q_s 2^(e_i - beta (s+1)) with
+    every Q_s integer-valued and |Q_s| < 2^beta.  Returns (e, [Q_s])."""
+    rem = np.array(X, dtype=np.float64, order="C")  # a contiguous copy
+    e = np.zeros(rem.shape[0], dtype=np.int64)
+    mx = np.max(np.abs(rem), axis=1) if rem.shape[1] else np.zeros(rem.shape[0])
+    for i in range(rem.shape[0]):
+        ex = frexp_exponent(float(mx[i]))
+        e[i] = 0 if ex is None else ex
+    out = []
+    lim = 2.0 ** beta
+    for s in range(max_slices):
+        if not rem.any():
+            return e, out
+        sc = np.ldexp(1.0, (beta * (s + 1) - e))[:, None]
+        q = rem * sc                       # exact: a power-of-two scaling ...
+        np.trunc(q, out=q)                 # ... then truncation: an integer below 2^beta
+        if np.abs(q).max() >= lim:
+            raise ArithmeticError("slice out of range")
+        q /= sc                            # exact: fewer than beta significant bits
+        rem -= q                           # exact: the bits below the slice's grid
+        q *= sc
+        out.append(q)
+    raise ArithmeticError("values span more bits than %d slices hold" % max_slices)
+
+
+def _exact_terms_block(A, B):
+    """Exact sum_k A_ik B_kj as a list of float64 arrays whose sum (taken
+    exactly) is the product, for a block A (R x K) @ B (K x N)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    k = A.shape[1]
+    beta = _slice_beta(max(k, 1))
+    ea, sa = _slices(A, beta)
+    eb, sb = _slices(B.T, beta)
+    terms = []
+    for s, qa in enumerate(sa):
+        for t, qb in enumerate(sb):
+            g = qa @ qb.T                  # integer partial sums below 2^53: exact
+            ex = (ea[:, None] + eb[None, :]) - beta * (s + t + 2)
+            term = np.ldexp(g, ex)
+            if not np.array_equal(np.ldexp(term, -ex), g):
+                raise ArithmeticError("scaled term not exact (range)")
+            terms.append(term)
+    return terms
+
+
+def exact_residual_sliced(A, B, C, block=512):
+    """RN(sum_k A_ik B_kj - C_ij) for every entry of C = (A @ B)'s block,
+    exactly (see the section comment); A is R x K, B is K x N, C is R x N.
+    B is taken ``block`` columns at a time (the same terms, less memory)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    C = np.asarray(C, dtype=np.float64)
+    out = np.empty(C.shape, dtype=np.float64)
+    for j0 in range(0, C.shape[1], block):
+        j1 = min(j0 + block, C.shape[1])
+        terms = _exact_terms_block(A, B[:, j0:j1])
+        T = np.stack(terms + [-C[:, j0:j1]])
+        for i in range(C.shape[0]):
+            Ti = T[:, i, :]
+            for j in range(j1 - j0):
+                out[i, j0 + j] = math.fsum(Ti[:, j].tolist())
+    return out
+
+
+def exact_residual_pairs(A, B, C, rows, cols, block=512):
+    """RN(sum_k A_(rows_e) k B_k (cols_e) - C_e) for the entry pairs (rows[e],
+    cols[e]), exactly; C holds the entries (length len(rows)).  Taken
+    ``block`` pairs at a time."""
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    C = np.asarray(C, dtype=np.float64)
+    beta = _slice_beta(max(A.shape[1], 1))
+    out = np.empty(len(rows), dtype=np.float64)
+    for e0 in range(0, len(rows), block):
+        e1 = min(e0 + block, len(rows))
+        ea, sa = _slices(A[rows[e0:e1]], beta)
+        eb, sb = _slices(B[:, cols[e0:e1]].T, beta)   # entry e: row e of each
+        terms = []
+        for s, qa in enumerate(sa):
+            for t, qb in enumerate(sb):
+                g = np.einsum("ek,ek->e", qa, qb)  # integer partial sums below 2^53: exact
+                ex = (ea + eb) - beta * (s + t + 2)
+                term = np.ldexp(g, ex)
+                if not np.array_equal(np.ldexp(term, -ex), g):
+                    raise ArithmeticError("scaled term not exact (range)")
+                terms.append(term)
+        T = np.stack(terms + [-C[e0:e1]])
+        for e in range(e1 - e0):
+            out[e0 + e] = math.fsum(T[:, e].tolist())
+    return out
+
+
+def bound_ratio_from_residual(res, absum, k):
+    """Max of |res| / (2 k 2^-53 absum) (entries with a zero bound must be
+    exact: ratio 0 when they are, inf otherwise)."""
+    res = np.abs(np.asarray(res, dtype=np.float64))
+    bound = 2.0 * k * 2.0 ** -53 * np.asarray(absum, dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, res / np.where(bound > 0, bound, 1.0), np.where(res == 0, 0.0, np.inf))
+    return float(ratio.max()) if ratio.size else 0.0
+
+
+def error_bound_ratio_sliced(A, B, C):
+    """:func:`error_bound_ratio` for a block with the exact residual from
+    slices; (|A||B|)_ij from one float64 product of the magnitudes (all terms
+    positive: relative error below K 2^-53, which moves the ratio by that
+    relative amount at most)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    res = exact_residual_sliced(A, B, C)
+    return bound_ratio_from_residual(res, np.abs(A) @ np.abs(B), A.shape[1])
+
+
+def error_bound_ratio_pairs(A, B, C, rows, cols):
+    """:func:`error_bound_ratio_sliced` for the entry pairs (rows[e], cols[e])."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    res = exact_residual_pairs(A, B, C, rows, cols)
+    absum = np.einsum("ek,ek->e", np.abs(A[np.asarray(rows)]), np.abs(B[:, np.asarray(cols)].T))
+    return bound_ratio_from_residual(res, absum, A.shape[1])
+
+
+def residues_one_modulus(A, B, r, l, ceiling=MODULUS_CEILING):
+    """Residues in [0, m_l) of C' = A'B' modulo the l-th of r moduli, for the
+    whole product, from the balanced residues of A' and B' and one exact
+    float64 product (:func:`mod_product_direct`); memory is one int64 copy of
+    each operand rather than all r residues and limb digits."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    k = A.shape[1]
+    m = moduli(r, ceiling)[l]
+    _, pA, pB = bit_budget(k, r, ceiling)
+    a = balanced_residue_array(scale_round(A, row_shifts(A, pA)), m)
+    bt = balanced_residue_array(scale_round(B.T, row_shifts(B.T, pB)), m)
+    return mod_product_direct(a, bt.T, m)

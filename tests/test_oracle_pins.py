@@ -132,15 +132,20 @@ def test_bit_budget_rejects_too_few_moduli():
 # Scaling and rounding
 # --------------------------------------------------------------------------
 
+def _check_round_half_even_ties(oz):
+    """Ties of the scaled values round to the even integer, in the scalar
+    (Fraction) rounding and in the vectorised integer rounding alike."""
+    cases = [(2.5, 0, 2), (3.5, 0, 4), (-2.5, 0, -2), (0.5, 0, 0), (1.5, 0, 2), (-1.5, 0, -2),
+             (5.0, -1, 2), (7.0, -1, 4), (0.75, 1, 2), (2.0 ** -1074 * 3, 1073, 2)]
+    for x, s, want in cases:
+        assert oz.scale_round_scalar(x, s) == want, (x, s)
+        got = oz.scale_round(np.array([[x]]), np.array([s]))
+        assert int(got[0, 0]) == want, (x, s, int(got[0, 0]))
+
+
 def test_round_half_even_ties():
-    assert oracle.scale_round_scalar(2.5, 0) == 2
-    assert oracle.scale_round_scalar(3.5, 0) == 4
-    assert oracle.scale_round_scalar(-2.5, 0) == -2
-    assert oracle.scale_round_scalar(0.5, 0) == 0
-    assert oracle.scale_round_scalar(1.5, 0) == 2
-    assert oracle.scale_round_scalar(5.0, -1) == 2   # 2.5 -> 2
-    assert oracle.scale_round_scalar(7.0, -1) == 4   # 3.5 -> 4
-    assert oracle.scale_round_scalar(0.75, 1) == 2   # 1.5 -> 2
+    import oracle.ozaki2 as oz
+    _check_round_half_even_ties(oz)
 
 
 def _edge_values():
@@ -391,14 +396,46 @@ def test_planted_transposed_operand_is_caught():
 
 
 def test_planted_wrong_rounding_is_caught(monkeypatch):
+    # A floor planted inside the oracle's vectorised rounding (the one every
+    # pipeline uses) must make the tie pin above fail.
     import oracle.ozaki2 as oz
-    monkeypatch.setattr(oz, "scale_round_scalar", lambda x, s: math.floor(Fraction(float(x)) * Fraction(2) ** int(s)))
-    assert oz.scale_round_scalar(2.5, 0) != 2 or oz.scale_round_scalar(-2.5, 0) != -2
+    real = oz.scale_round
+
+    def floored(X, shifts):
+        X = np.asarray(X, dtype=np.float64)
+        s = np.asarray(shifts, dtype=np.int64).reshape(-1, 1)
+        return np.array([[math.floor(Fraction(float(x)) * Fraction(2) ** int(si)) for x in row]
+                         for row, si in zip(X, s[:, 0])], dtype=np.int64)
+
+    monkeypatch.setattr(oz, "scale_round", floored)
+    with pytest.raises(AssertionError):
+        _check_round_half_even_ties(oz)
+    monkeypatch.setattr(oz, "scale_round", real)
+    _check_round_half_even_ties(oz)
+
+
+def test_planted_double_rounding_in_scale_back_is_caught(monkeypatch):
+    # Rounding C' to fp64 first and scaling afterwards (two roundings) must
+    # fail the subnormal-range pins below.
+    import oracle.ozaki2 as oz
+    monkeypatch.setattr(oz, "scale_back", lambda Cp, S: math.ldexp(float(int(Cp)), -int(S)))
+    with pytest.raises(AssertionError):
+        _check_scale_back_subnormal(oz)
 
 
 # --------------------------------------------------------------------------
 # TME time model and OI* (The Missing Fourth Term ..., abstract)
 # --------------------------------------------------------------------------
+
+def _bisect_crossing(gap, lo=1e-6, hi=1e6):
+    for _ in range(200):
+        mid = math.sqrt(lo * hi)
+        if gap(mid) > 0:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
 
 def test_oi_star_is_the_crossing_point():
     # OI* is where deconstruction time (infinite tensor throughput, no HBM
@@ -411,14 +448,49 @@ def test_oi_star_is_the_crossing_point():
         flops = oi * bytes_
         return oracle.deconstruction_time(n_in, c_q, r, P_int) - flops / P_fp64
 
-    lo, hi = 1e-6, 1e6
-    for _ in range(200):
-        mid = math.sqrt(lo * hi)
-        if gap(mid) > 0:
-            lo = mid
-        else:
-            hi = mid
+    lo = _bisect_crossing(gap)
     assert abs(lo - oracle.oi_star(c_q, r, P_fp64, P_int)) / lo < 1e-9
+
+
+def test_tme_time_crossing_with_unbounded_tensor_and_hbm():
+    # The same crossing through the full four-term model: with unbounded
+    # tensor and HBM rates and a free reconstruction, the model's emulation
+    # time equals native fp64 time exactly at the closed-form OI*, for any
+    # problem size ([TME4] abstract: the threshold holds regardless of
+    # tensor-core throughput).
+    c_q, r, P_fp64, P_int = 2.5, 12, 1.3e12, 4.1e13
+    for n_in in (1e6, 3e9):
+        def gap(oi):
+            flops = oi * 8 * n_in
+            t_emu = oracle.tme_time(flops * 9 * r, math.inf, 8 * n_in, math.inf, 1000, 0.0,
+                                    n_inputs=n_in, c_q=c_q, r=r, P_int=P_int)
+            return t_emu - flops / P_fp64
+        lo = _bisect_crossing(gap)
+        assert abs(lo - oracle.oi_star(c_q, r, P_fp64, P_int)) / lo < 1e-9
+
+
+def test_tme_time_terms_and_dense_gemm_unaffected():
+    # The model is the larger of the tensor and HBM terms plus the two
+    # per-element terms: each term alone is recovered when the others vanish.
+    assert oracle.tme_time(6.0, 2.0, 0.0, 1.0, 0, 0.0) == 3.0          # tensor-bound
+    assert oracle.tme_time(0.0, 1.0, 10.0, 2.0, 0, 0.0) == 5.0         # HBM-bound
+    assert oracle.tme_time(0.0, 1.0, 0.0, 1.0, 4, 0.25) == 1.0          # reconstruction only
+    assert oracle.tme_time(0.0, 1.0, 0.0, 1.0, 0, 0.0, n_inputs=8, c_q=2.0, r=3, P_int=4.0) == 12.0
+    # [TME4] abstract: dense GEMM is unaffected by the fourth term.  An
+    # n x n x n product streams 2 n^2 inputs against 2 n^3 flop, so the
+    # fourth term's share of the time halves each time n doubles and
+    # vanishes for large n, whatever c_q and the integer rate are.
+    r = 13
+
+    def overhead(n, c_q, P_int):
+        flops = 9 * r * 2.0 * n ** 3
+        t3 = oracle.tme_time(flops, 1e16, 0.0, 1.0, n * n, 0.0)
+        t4 = oracle.tme_time(flops, 1e16, 0.0, 1.0, n * n, 0.0, n_inputs=2 * n * n, c_q=c_q, r=r, P_int=P_int)
+        return (t4 - t3) / t3
+
+    for c_q, P_int in ((3.0, 1e14), (13.0, 7e13)):
+        assert overhead(8192, c_q, P_int) == pytest.approx(2 * overhead(16384, c_q, P_int), rel=1e-12)
+        assert 0 < overhead(65536, c_q, P_int) < 0.01
 
 
 def test_scale_back_overflow_rounds_to_signed_inf():
@@ -429,6 +501,91 @@ def test_scale_back_overflow_rounds_to_signed_inf():
     assert oracle.scale_back(-big, 0) == -math.inf
     assert oracle.scale_back(3, -1100) == math.inf
     assert oracle.scale_back(3, 1100) == 0.0
+    # The largest finite double, and the tie just above it, which IEEE
+    # round-to-nearest sends to infinity.
+    fmax = (2 ** 53 - 1) * 2 ** 971
+    assert oracle.scale_back(fmax, 0) == 1.7976931348623157e308
+    # fmax + ulp/2 = (2^54 - 1) 2^970 is a tie; the even neighbour is 2^1024.
+    assert oracle.scale_back(2 ** 54 - 1, -970) == math.inf
+    # a quarter ulp above fmax rounds back down to it
+    assert oracle.scale_back(2 ** 55 - 3, -969) == 1.7976931348623157e308
+
+
+def _check_scale_back_subnormal(oz):
+    """Hand-derived single roundings in the subnormal range, where one
+    rounding and two (to 53 bits, then to the subnormal grid) differ."""
+    tiny = 2.0 ** -1074                       # the subnormal grid
+    # 1.5 grid units: a tie, rounded to the even 2 units.
+    assert oz.scale_back(3, 1075) == 2 * tiny
+    assert oz.scale_back(-3, 1075) == -2 * tiny
+    # 0.5 grid units: a tie between 0 and 1 unit, rounded to even 0.
+    assert oz.scale_back(1, 1075) == 0.0
+    # 0.75 grid units rounds up to one unit.
+    assert oz.scale_back(3, 1076) == tiny
+    # 2.5 units + 2^-61 units: above the tie, so one rounding gives 3 units.
+    # Rounding C' = 5 2^60 + 1 to 53 bits first drops the +1 and leaves the
+    # exact tie 2.5 units, which then rounds to even, 2 units.
+    cp = 5 * 2 ** 60 + 1
+    assert oz.scale_back(cp, 1135) == 3 * tiny
+    assert oz.scale_back(-cp, 1135) == -3 * tiny
+    # Just below the smallest normal: (2^52 - 0.5) units is a tie that rounds
+    # to even 2^52 units, the smallest normal number.
+    assert oz.scale_back(2 ** 53 - 1, 1075) == 2.0 ** -1022
+
+
+def test_scale_back_subnormal_single_rounding():
+    import oracle.ozaki2 as oz
+    _check_scale_back_subnormal(oz)
+
+
+# --------------------------------------------------------------------------
+# The exact product at full size (error-free slices)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dist,k", [("wide", 300), ("normal", 1000), ("uniform", 4097)])
+def test_sliced_residual_matches_fraction(dist, k):
+    A, B = make_pair(3, 4, k, seed=40, dist=dist)
+    C = A @ B
+    C[0, 0] = np.nextafter(C[0, 0], np.inf)   # a residual of one ulp
+    res = oracle.exact_residual_sliced(A, B, C, block=3)
+    for i in range(3):
+        for j in range(4):
+            ex = oracle.exact_dot_fraction(A[i], B[:, j]) - Fraction(C[i, j])
+            assert res[i, j] == float(ex), (i, j)
+    rows, cols = [2, 0, 1, 2], [3, 0, 1, 3]
+    pr = oracle.exact_residual_pairs(A, B, C[rows, cols], rows, cols, block=3)
+    assert (pr == res[rows, cols]).all()
+
+
+def test_sliced_residual_exact_under_cancellation():
+    # A row built so that the exact dot product is a tiny value far below
+    # the terms: x, -x pairs plus one small term (and subnormal-free tails).
+    rng = np.random.default_rng(41)
+    k = 2048
+    a = np.ldexp(rng.uniform(0.5, 1, k), rng.integers(-30, 30, k))
+    b = np.ldexp(rng.uniform(0.5, 1, k), rng.integers(-30, 30, k))
+    a[k // 2:] = a[:k // 2]
+    b[k // 2:] = -b[:k // 2]
+    a[0] *= 1 + 2.0 ** -50
+    A, B = a[None, :], b[:, None]
+    C = np.zeros((1, 1))
+    res = oracle.exact_residual_sliced(A, B, C)
+    assert res[0, 0] == float(oracle.exact_dot_fraction(a, b)) != 0.0
+
+
+def test_sliced_bound_ratio_matches_fraction_bound():
+    A, B = make_pair(6, 5, 700, seed=42, dist="wide")
+    C = oracle.dgemm(A, B, 14)
+    assert oracle.error_bound_ratio_sliced(A, B, C) == pytest.approx(oracle.error_bound_ratio(A, B, C), rel=1e-12)
+    C[1, 1] = np.nextafter(C[1, 1], np.inf) * (1 + 2.0 ** -30)
+    assert oracle.error_bound_ratio_sliced(A, B, C) > 1.0
+
+
+def test_residues_one_modulus_matches_stages():
+    A, B = make_pair(9, 7, 130, seed=43, dist="wide")
+    _, st = oracle.dgemm(A, B, 13, stages=True)
+    for l in (0, 5, 12):
+        assert (oracle.residues_one_modulus(A, B, 13, l) == st["res"][l]).all()
 
 
 # --------------------------------------------------------------------------
