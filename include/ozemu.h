@@ -229,8 +229,12 @@ int ozemu_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8,
                           const int8_t* b_res8, uint8_t* residues, cudaStream_t stream);
 
 /* Per-output reconstruction ([TME4] abstract): C' in (-M/2, M/2) from its r
- * residues by mixed-radix CRT, then C[i*ldc + j] = RN(C' 2^-(sA[i] + sB[j])),
- * one correct rounding (subnormal and overflow included). */
+ * residues by the CRT in direct form, C' = sum_l c_l W_l - q M with
+ * W_l = (M/m_l) ((M/m_l)^-1 mod m_l) (byte-wise integer dot products and one
+ * quotient estimate q); an output whose quotient estimate is within 2^-8 of
+ * ambiguous takes the exact mixed-radix (Garner) digits instead.  Then
+ * C[i*ldc + j] = RN(C' 2^-(sA[i] + sB[j])), one correct rounding (subnormal
+ * and overflow included). */
 int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a,
                   const int32_t* shifts_b, double* C, int ldc, cudaStream_t stream);
 
@@ -240,12 +244,35 @@ int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* s
 
 /* Synchronises `stream`, then returns and clears the current device's flags:
  * OZEMU_ERR_NONFINITE, OZEMU_ERR_TIMEOUT, OZEMU_ERR_CUDA (a sticky CUDA error)
- * or OZEMU_OK. */
+ * or OZEMU_OK.  The flags of ozemu_dgemm_noalloc are separate: see
+ * ozemu_get_status_noalloc. */
 int ozemu_get_status(cudaStream_t stream);
 
 /* Frees the workspace cached for the current device (synchronises it).
  * Calls after this re-allocate on demand. */
 void ozemu_release(void);
+
+/* Caps the cached workspace of every device at `bytes` (0 removes the cap).
+ * A call that needs a larger workspace then returns OZEMU_ERR_ALLOC before
+ * enqueueing anything, instead of growing it; a cached block already above
+ * the new cap on the current device is freed (which synchronises it).  For
+ * callers that share the GPU's memory with other work.  host. */
+int ozemu_set_workspace_limit(size_t bytes);
+
+/* The cap set by ozemu_set_workspace_limit (0: none).  host. */
+size_t ozemu_workspace_limit(void);
+
+/* Diagnostic of the kernels' failure detection.  Every pipeline wait in the
+ * GEMM kernels is bounded in time: a wait that gives up sets the time-out
+ * flag, and the kernel drains what it issued, frees its tensor memory and
+ * returns, so the context stays usable.  This call launches one CTA whose
+ * thread makes the same bounded wait (limit_ns nanoseconds, 1 ns .. 1 s) on a
+ * barrier phase that nothing completes, with no copy or tensor operation in
+ * flight: it always gives up.  A following ozemu_get_status(stream) returns
+ * OZEMU_ERR_TIMEOUT and clears the flag; until then, GEMM launches on the
+ * device skip their work (they see the flag).  limit_ns out of range ->
+ * OZEMU_ERR_INVALID_ARG.  The pages have no counterpart. */
+int ozemu_probe_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Allocation-free product                                                   */
@@ -275,10 +302,23 @@ void ozemu_release(void);
  * left there, so calls that overlap on the GPU (different streams, or several
  * host threads) race: serialise them.  Device-side conditions (non-finite
  * input, a pipeline wait time-out) are recorded in the array's status word,
- * which each call clears first; ozemu_get_status does not report them.
- * Arguments and errors otherwise as ozemu_dgemm. */
+ * which each call clears first: ozemu_get_status does not report them, and
+ * ozemu_get_status_noalloc does.  After a time-out C is not the product
+ * (the GEMM skipped its work and the reconstruction used stale residues), so
+ * check the status before using C.  This call always takes the limb-plane
+ * path, also for n <= ozemu_narrow_max_n() where ozemu_dgemm takes the fused
+ * narrow path; the size formula above therefore bounds narrow shapes too
+ * (m = 16384, n = 1, k = 16384 at r = 12 needs about 4.8 GB of planes and is
+ * rejected).  Arguments and errors otherwise as ozemu_dgemm. */
 int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const double* B,
                         int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the status word of
+ * ozemu_dgemm_noalloc on the current device: OZEMU_ERR_TIMEOUT,
+ * OZEMU_ERR_NONFINITE or OZEMU_OK (the word reflects the last noalloc call
+ * that ran).  Allocates nothing: it copies the 4-byte word into a host
+ * variable and clears it. */
+int ozemu_get_status_noalloc(cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Two-limb moduli                                                          */
@@ -287,9 +327,11 @@ int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const dou
 /* A variant of the same scheme with smaller moduli, so that each balanced
  * residue needs only two base-13 limbs.  [AWE] abstract: limbs in S with
  * weights (1, 13, 169) and 9 FP4 products per modulus.  Two limbs d0 + 13 d1
- * with d_i in S cover every integer of [-56, 56] (-56 = -4 + 13 (-4),
- * 56 = 4 + 13 * 4, and each class mod 13 has a member of S of magnitude
- * <= 6), so a modulus m <= 113 needs no third limb.  The product of two such
+ * with d_i in S cover every integer of [-56, 56]: the low digit d0 is the
+ * smallest-magnitude member of S in x's class mod 13 (|d0| <= 6 except for
+ * classes 5 and 8, whose only members are -8 and 8), and across [-56, 56]
+ * the carry d1 = (x - d0)/13 stays within [-4, 4], in S (checked for every
+ * x by the oracle pins).  So a modulus m <= 113 needs no third limb.  The product of two such
  * residues then takes 4 FP4 GEMMs instead of 9:
  *   D1 = A0 B0 + 13 (A0 B1 + A1 B0),   D2 = A1 B1,   residue = D1 + 169 D2 mod m.
  * Each modulus carries about 6.7 bits instead of 8, so about 16/13 as many

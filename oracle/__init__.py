@@ -31,6 +31,6 @@ from .ozaki2 import (  # noqa: F401
     dgemm, dgemm_block, igemm_s8, igemm_s8_direct,
     exact_dot_fraction, two_product, exact_residual, abs_product_sum,
     error_bound_ratio, exact_residual_sliced, exact_residual_pairs,
-    error_bound_ratio_sliced, error_bound_ratio_pairs, residues_one_modulus,
+    error_bound_ratio_sliced, error_bound_ratio_pairs, residues_one_modulus, residues_of_moduli,
 )
 from .cost_model import oi_star, tme_time, deconstruction_time  # noqa: F401

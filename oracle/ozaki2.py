@@ -146,25 +146,25 @@ def scale_round(X, shifts):
     """
     X = np.asarray(X, dtype=np.float64)
     s = np.asarray(shifts, dtype=np.int64).reshape(-1, 1)
+    if X.ndim == 2 and X.size > (1 << 20):
+        # Large matrices a block of rows at a time (same values, small temporaries).
+        step = max(1, (1 << 20) // max(X.shape[1], 1))
+        return np.concatenate([scale_round(X[i:i + step], s[i:i + step]) for i in range(0, X.shape[0], step)])
     mant, e = np.frexp(X)
     q = (np.abs(mant) * 2.0 ** 53).astype(np.int64)  # exact, < 2^53
     sh = e.astype(np.int64) - 53 + s
-    sh = np.broadcast_to(sh, X.shape)
-    out = np.zeros(X.shape, dtype=np.int64)
-    left = sh >= 0
-    if np.any(left):
-        if np.any(np.ldexp(q[left].astype(np.float64), sh[left]) > 2.0 ** 62):
-            raise OverflowError("scaled integer exceeds 2^62")
-        out[left] = q[left] << sh[left]
-    right = ~left
-    if np.any(right):
-        d = np.minimum(-sh[right], 62)
-        qq = q[right]
-        qd = qq >> d
-        rem = qq & ((np.int64(1) << d) - 1)
-        half = np.int64(1) << (d - 1)
-        up = (rem > half) | ((rem == half) & ((qd & 1) == 1))
-        out[right] = qd + up.astype(np.int64)
+    # Left shifts (sh >= 0): the integer is q 2^sh; it must stay <= 2^62.
+    shl = np.clip(sh, 0, 62)
+    if np.any((sh > 0) & ((sh > 62) | (q > (np.int64(1) << 62) >> shl))):
+        raise OverflowError("scaled integer exceeds 2^62")
+    left = q << shl
+    # Right shifts (sh < 0) by d = min(-sh, 62), rounded half to even.
+    d = np.clip(-sh, 1, 62)
+    qd = q >> d
+    rem = q & ((np.int64(1) << d) - 1)
+    half = np.int64(1) << (d - 1)
+    up = (rem > half) | ((rem == half) & ((qd & 1) == 1))
+    out = np.where(sh >= 0, left, qd + up.astype(np.int64))
     return np.where(X < 0, -out, out)
 
 
@@ -178,7 +178,11 @@ def balanced_residue(x, m):
 
 def balanced_residue_array(X, m):
     """Element-wise :func:`balanced_residue` on an int64 array."""
-    v = np.mod(np.asarray(X, dtype=np.int64), m)
+    X = np.asarray(X, dtype=np.int64)
+    if X.ndim == 2 and X.size > (1 << 20):
+        step = max(1, (1 << 20) // max(X.shape[1], 1))
+        return np.concatenate([balanced_residue_array(X[i:i + step], m) for i in range(0, X.shape[0], step)])
+    v = np.mod(X, m)
     return np.where(v > (m - 1) // 2, v - m, v)
 
 
@@ -662,16 +666,38 @@ def error_bound_ratio_pairs(A, B, C, rows, cols):
     return bound_ratio_from_residual(res, absum, A.shape[1])
 
 
-def residues_one_modulus(A, B, r, l, ceiling=MODULUS_CEILING):
-    """Residues in [0, m_l) of C' = A'B' modulo the l-th of r moduli, for the
-    whole product, from the balanced residues of A' and B' and one exact
-    float64 product (:func:`mod_product_direct`); memory is one int64 copy of
-    each operand rather than all r residues and limb digits."""
+def residues_of_moduli(A, B, r, ls, ceiling=MODULUS_CEILING):
+    """{l: residues in [0, m_l) of C' = A'B' modulo the l-th of r moduli} for
+    the whole product and each l in ls, from the balanced residues of A' and
+    B' and exact float64 products (as :func:`mod_product_direct`, a block of
+    rows at a time); memory is one integer copy of each operand rather than
+    all r residues and limb digits."""
     A = np.asarray(A, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
     k = A.shape[1]
-    m = moduli(r, ceiling)[l]
+    mods = moduli(r, ceiling)
     _, pA, pB = bit_budget(k, r, ceiling)
-    a = balanced_residue_array(scale_round(A, row_shifts(A, pA)), m)
-    bt = balanced_residue_array(scale_round(B.T, row_shifts(B.T, pB)), m)
-    return mod_product_direct(a, bt.T, m)
+    if k * 128 * 128 >= 2 ** 53:
+        raise OverflowError("direct product not exact in float64")
+    ai = scale_round(A, row_shifts(A, pA))
+    Bt = np.ascontiguousarray(B.T)
+    bi = scale_round(Bt, row_shifts(Bt, pB))
+    del Bt
+    out = {}
+    for l in ls:
+        m = mods[l]
+        a = balanced_residue_array(ai, m)
+        bf = np.ascontiguousarray(balanced_residue_array(bi, m).T, dtype=np.float64)
+        res = np.empty((A.shape[0], B.shape[1]), dtype=np.int64)
+        step = 512
+        for i in range(0, A.shape[0], step):
+            # |residues| <= 128: every partial sum is an integer below 2^53, exact
+            prod = a[i:i + step].astype(np.float64) @ bf
+            res[i:i + step] = np.mod(np.rint(prod).astype(np.int64), m)
+        out[l] = res
+    return out
+
+
+def residues_one_modulus(A, B, r, l, ceiling=MODULUS_CEILING):
+    """:func:`residues_of_moduli` for one modulus."""
+    return residues_of_moduli(A, B, r, [l], ceiling)[l]

@@ -76,6 +76,10 @@ _SIGNATURES = {
     "ozemu_crt_f64_2limb": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P]),
     "ozemu_dgemm_2limb": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
     "ozemu_dgemm_host_2limb": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
+    "ozemu_get_status_noalloc": (_I, [_P]),
+    "ozemu_set_workspace_limit": (_I, [_S]),
+    "ozemu_workspace_limit": (_S, []),
+    "ozemu_probe_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
 }
 
 
@@ -209,6 +213,22 @@ def ozemu_release():
 
 def ozemu_dgemm_noalloc(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
     return _call("ozemu_dgemm_noalloc", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
+
+
+def ozemu_get_status_noalloc(stream):
+    return _call("ozemu_get_status_noalloc", stream)
+
+
+def ozemu_set_workspace_limit(nbytes):
+    return _call("ozemu_set_workspace_limit", nbytes)
+
+
+def ozemu_workspace_limit():
+    return _call("ozemu_workspace_limit")
+
+
+def ozemu_probe_wait_timeout(limit_ns, stream):
+    return _call("ozemu_probe_wait_timeout", limit_ns, stream)
 
 
 def ozemu_moduli_2limb(r):

@@ -219,10 +219,15 @@ int device_state(DeviceState** out) {
   return OZEMU_OK;
 }
 
+// Caller-set cap on each device's cached workspace (0: none).
+size_t g_ws_limit = 0;
+
 // Workspace of at least `bytes` on the current device (grows; synchronises
-// the device when it has to replace a smaller buffer).
+// the device when it has to replace a smaller buffer).  A request above the
+// cap fails with OZEMU_ERR_ALLOC before anything is allocated.
 int workspace(DeviceState* d, size_t bytes, uint8_t** out) {
   std::lock_guard<std::mutex> lk(g_mu);
+  if (g_ws_limit != 0 && bytes > g_ws_limit) return OZEMU_ERR_ALLOC;
   if (bytes > d->ws_bytes) {
     if (d->ws) {
       cudaDeviceSynchronize();
@@ -231,6 +236,7 @@ int workspace(DeviceState* d, size_t bytes, uint8_t** out) {
       d->ws_bytes = 0;
     }
     size_t want = bytes + bytes / 8;
+    if (g_ws_limit != 0 && want > g_ws_limit) want = g_ws_limit;
     if (cudaMalloc(&d->ws, want) != cudaSuccess) {
       cudaGetLastError();
       return OZEMU_ERR_ALLOC;
@@ -553,6 +559,21 @@ std::mutex g_noalloc_mu;
 
 // Device address of the static scratch for the current device; the lookup
 // happens once per device with that device current.
+// Diagnostic of the bounded pipeline wait: one thread waits, with a short
+// limit, on an mbarrier phase that nothing completes.  The wait gives up,
+// sets the time-out bit of `flags` and returns; no copy or MMA is in flight.
+__global__ void wait_probe_kernel(uint32_t* flags, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_word = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, &abort_word, flags, limit_ns);
+  __syncthreads();
+}
+
 int noalloc_scratch(uint8_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OZEMU_ERR_CUDA;
@@ -1080,6 +1101,47 @@ int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const dou
   s = residue_gemm(m, n, k, r, ap, bp, res, &d, stream);
   if (s != OZEMU_OK) return s;
   return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), stream));
+}
+
+int ozemu_get_status_noalloc(cudaStream_t stream) {
+  uint8_t* base = nullptr;
+  int s = noalloc_scratch(&base);
+  if (s != OZEMU_OK) return s;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+  uint32_t f = 0;
+  // A copy into a host variable and a fill of the word: nothing is allocated.
+  if (cudaMemcpy(&f, base, sizeof(f), cudaMemcpyDeviceToHost) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (cudaMemset(base, 0, sizeof(f)) != cudaSuccess) return OZEMU_ERR_CUDA;
+  if (f & kFlagTimeout) return OZEMU_ERR_TIMEOUT;
+  if (f & kFlagNonFinite) return OZEMU_ERR_NONFINITE;
+  return OZEMU_OK;
+}
+
+int ozemu_set_workspace_limit(size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_ws_limit = bytes;
+  if (bytes == 0 || dev < 0 || dev >= kMaxDevices) return OZEMU_OK;
+  DeviceState& d = g_dev[dev];
+  if (d.ws && d.ws_bytes > bytes) {  // the cached block is above the new cap: give it back
+    cudaDeviceSynchronize();
+    cudaFree(d.ws);
+    d.ws = nullptr;
+    d.ws_bytes = 0;
+  }
+  return OZEMU_OK;
+}
+
+size_t ozemu_workspace_limit(void) { return g_ws_limit; }
+
+int ozemu_probe_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  wait_probe_kernel<<<1, 32, 0, stream>>>(d->flags, limit_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 void ozemu_release(void) {

@@ -130,12 +130,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete, at most kWaitLimitNs.
+// Waits for the phase with the given parity to complete, at most limit_ns
+// (kWaitLimitNs in the kernels; the wait probe passes a short limit).
 // On time-out sets the device timeout flag and the CTA's abort word and
 // returns false.  Also returns false early once another role of this CTA, or
 // any CTA on the device, has timed out (the flag word is device-wide).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_word,
-                                          uint32_t* flags) {
+                                          uint32_t* flags, uint64_t limit_ns = kWaitLimitNs) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -147,7 +148,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         atomicOr(flags, kFlagTimeout);
         *abort_word = 1;
         return false;

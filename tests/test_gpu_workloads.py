@@ -4,8 +4,11 @@ The GPU computes every output; the oracle computes sampled rows and columns
 at the full inner dimension (its row/column exponents always see the whole
 row/column).  Sampled fp64 entries must match the oracle bit for bit and lie
 within |C - C_exact| <= 2 K 2^-53 (|A||B|)_ij; the shifts of every row and
-column and the residues of the sampled block must match exactly.  The INT8
-product is compared in full.
+column and the residues of the sampled block must match exactly.  At full
+size, every residue of two moduli (the first and the last) is compared with
+the oracle's, and the bound is checked with exact products on 16 full rows,
+16 full columns (all columns when there are fewer) and 4096 random entries of
+the result ozemu_dgemm returns.  The INT8 product is compared in full.
 """
 
 import numpy as np
@@ -108,6 +111,46 @@ def test_workload_two_limb_sampled(oz, name, r, n_rows, n_cols):
     Cg = C.cpu().numpy()[np.ix_(rows, cols)]
     assert (Cg.view(np.int64) == Cref.view(np.int64)).all()
     assert oracle.error_bound_ratio(A_h[rows], B_h[:, cols], Cg) <= 1.0
+
+
+@pytest.mark.parametrize("name", ["dgemm_8192_wide", "dgemv_16384_n1", "dgemv_16384_n8", "dgemm_4096_k65536"])
+def test_workload_full_modulus_and_bound_samples(oz, name):
+    A_h, B_h, spec = workload_inputs(name)
+    r = spec["r"]
+    m, n, k = spec["m"], spec["n"], spec["k"]
+    A = torch.from_numpy(A_h).to(DEV)
+    B = torch.from_numpy(B_h).to(DEV)
+    C = oz.dgemm(A, B, r)
+    assert oz.get_status() == oz.OZEMU_OK
+    C = C.cpu().numpy()
+    # Every residue of two moduli, from the path ozemu_dgemm takes for the shape.
+    if n <= oz.ozemu_narrow_max_n():
+        res, _, _ = oz.residues_narrow_f64(A, B, r)
+    else:
+        pA, pB = oz.ozemu_bit_budget(k, r)
+        ap, sa = oz.split_rows_f64(A, pA, r)
+        bp, sb = oz.split_cols_f64(B, pB, r)
+        res = oz.residue_gemm(m, n, k, r, ap, bp)
+        del ap, bp
+    assert oz.get_status() == oz.OZEMU_OK
+    del A, B
+    want = oracle.residues_of_moduli(A_h, B_h, r, (0, r - 1))
+    for l in (0, r - 1):
+        got = res[l, :, :n].cpu().numpy().astype(np.int64)
+        assert (got == want[l]).all(), l
+    del res
+    # The bound, with exact products, on 16 full rows, 16 full columns and
+    # 4096 random entries.
+    rows = sample_indices(m, 16, seed=31)
+    cols = sample_indices(n, 16, seed=32)
+    rng = np.random.default_rng(33)
+    I = rng.integers(0, m, 4096)
+    J = rng.integers(0, n, 4096)
+    ratios = (oracle.error_bound_ratio_sliced(A_h[rows], B_h, C[rows]),
+              oracle.error_bound_ratio_sliced(A_h, B_h[:, cols], C[:, cols]),
+              oracle.error_bound_ratio_pairs(A_h, B_h, C[I, J], I, J))
+    print("%s r=%d max |C - C_exact| / bound: rows %.4f, columns %.4f, entries %.4f" % ((name, r) + ratios))
+    assert max(ratios) <= 1.0
 
 
 def test_igemm_s8_4096_full(oz):

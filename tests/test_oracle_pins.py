@@ -586,6 +586,8 @@ def test_residues_one_modulus_matches_stages():
     _, st = oracle.dgemm(A, B, 13, stages=True)
     for l in (0, 5, 12):
         assert (oracle.residues_one_modulus(A, B, 13, l) == st["res"][l]).all()
+    both = oracle.residues_of_moduli(A, B, 13, (0, 12))
+    assert (both[0] == st["res"][0]).all() and (both[12] == st["res"][12]).all()
 
 
 # --------------------------------------------------------------------------
