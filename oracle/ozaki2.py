@@ -155,7 +155,7 @@ def scale_round(X, shifts):
     sh = e.astype(np.int64) - 53 + s
     # Left shifts (sh >= 0): the integer is q 2^sh; it must stay <= 2^62.
     shl = np.clip(sh, 0, 62)
-    if np.any((sh > 0) & ((sh > 62) | (q > (np.int64(1) << 62) >> shl))):
+    if np.any((q > 0) & (sh > 0) & ((sh > 62) | (q > (np.int64(1) << 62) >> shl))):
         raise OverflowError("scaled integer exceeds 2^62")
     left = q << shl
     # Right shifts (sh < 0) by d = min(-sh, 62), rounded half to even.

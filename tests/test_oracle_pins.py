@@ -172,6 +172,18 @@ def test_scale_round_vector_matches_fraction(seed):
             assert np.max(np.abs(got[i])) <= 2 ** p
 
 
+def test_scale_round_zeros_beside_tiny_values():
+    # A row of tiny magnitudes takes a shift near 1000; its zeros must stay 0
+    # (no overflow), and every element must match the Fraction rounding.
+    X = np.array([[0.0, 5e-300, -7e-301, 0.0, 2.0 ** -1074], [1.0, -3.0, 0.0, 0.5, 2.5]])
+    for p in (30, 52, 62):
+        s = oracle.row_shifts(X, p)
+        got = oracle.scale_round(X, s)
+        for i in range(2):
+            for k in range(X.shape[1]):
+                assert got[i, k] == oracle.scale_round_scalar(X[i, k], s[i])
+
+
 def test_row_shift_scaling_is_tight():
     # After scaling, the largest |X'| of each nonzero row lies in [2^(p-1), 2^p].
     A, _ = make_pair(32, 1, 300, seed=7, dist="wide")
