@@ -57,13 +57,52 @@ MODULUS_CEILING = 256
 MODULUS_CEILING_2LIMB = 113
 
 
+# Mixed-digit reading ([AWE] abstract: the formulation holds modulo m, and the
+# encodings may differ per input range).  A modulus m whose every residue
+# class holds a member of S needs ONE digit per residue, so its residue
+# product is one FP4 product.  The list starts with such moduli (the set of
+# largest product, pairwise coprime) and continues with the two-limb moduli
+# (greedy from 113, coprime to all taken).  Passed as ``ceiling=MIXED``.
+MIXED = "mixed"
+
+
 # ----------------------------------------------------------------------------
 # Stage 0: moduli and bit budget (reading of [TME4] abstract; configs)
 # ----------------------------------------------------------------------------
 
+def single_digit_moduli(limit=16):
+    """Every m in [2, limit] for which S meets every residue class mod m."""
+    return [m for m in range(2, limit + 1) if len({d % m for d in S}) == m]
+
+
+def single_digit_set():
+    """The pairwise-coprime subset of :func:`single_digit_moduli` with the
+    largest product, the even member first, the others descending."""
+    cands = single_digit_moduli()
+    best, best_prod = (), 1
+    for mask in range(1 << len(cands)):
+        pick = [m for i, m in enumerate(cands) if mask >> i & 1]
+        if all(math.gcd(a, b) == 1 for i, a in enumerate(pick) for b in pick[:i]):
+            prod = math.prod(pick)
+            if prod > best_prod:
+                best, best_prod = pick, prod
+    even = [m for m in best if m % 2 == 0]
+    return even + sorted((m for m in best if m % 2), reverse=True)
+
+
+def single_digit(x, m):
+    """The digit of residue x modulo a single-digit modulus m: x itself if it
+    lies in S, otherwise the member of S in x's class of smallest magnitude."""
+    x = int(x)
+    if x in S:
+        return x
+    return min((d for d in S if (d - x) % m == 0), key=abs)
+
+
 def moduli(r, ceiling=MODULUS_CEILING):
     """First ``r`` greedy pairwise-coprime integers counting down from
-    ``ceiling`` (256; 113 for the two-limb reading).
+    ``ceiling`` (256; 113 for the two-limb reading); with ``ceiling=MIXED``
+    the single-digit set first, then the greedy count from 113.
 
     The sources name no moduli.  Reading: take each integer from the ceiling
     down that is coprime to every modulus already taken.
@@ -71,6 +110,9 @@ def moduli(r, ceiling=MODULUS_CEILING):
     if r < 1:
         raise ValueError("r must be >= 1")
     out = []
+    if ceiling == MIXED:
+        out = single_digit_set()[:r]
+        ceiling = MODULUS_CEILING_2LIMB
     m = ceiling
     while len(out) < r:
         if m < 2:
@@ -365,17 +407,38 @@ def scale_back_array(Cp, sA, sB):
 # Pipelines
 # ----------------------------------------------------------------------------
 
+def digits_of_modulus(res, m, l, ceiling=MODULUS_CEILING):
+    """Limb digits (3, ...) of the balanced residues ``res`` of the l-th
+    modulus m: base-13 limbs, or for a single-digit modulus of the mixed list
+    (d, 0, 0) with d = :func:`single_digit`."""
+    if ceiling == MIXED and l < len(single_digit_set()):
+        h = m // 2
+        table = np.array([single_digit(x, m) for x in range(-h, m - h)], dtype=np.int64)
+        d = table[np.asarray(res, dtype=np.int64) + h]
+        return np.stack([d, np.zeros_like(d), np.zeros_like(d)])
+    return limb_digits(res)
+
+
+def products_per_modulus(l, ceiling=MODULUS_CEILING):
+    """FP4 products the l-th modulus takes: 9 (three limbs), 4 (two limbs),
+    1 (a single-digit modulus of the mixed list)."""
+    if ceiling == MIXED:
+        return 1 if l < len(single_digit_set()) else 4
+    return 4 if ceiling == MODULUS_CEILING_2LIMB else 9
+
+
 def deconstruct(X, p, r, ceiling=MODULUS_CEILING):
     """Stage 1 + 2 for the rows of X: shifts, integers, residues, limb digits.
 
     Returns dict(shift=(rows,), xint=(rows, k), res=(r, rows, k),
-    digits=(r, 3, rows, k)); with ceiling 113 the top digit is 0 throughout.
+    digits=(r, 3, rows, k)); with ceiling 113 the top digit is 0 throughout;
+    with ceiling MIXED single-digit moduli have digits (d, 0, 0).
     """
     s = row_shifts(X, p)
     xi = scale_round(X, s)
     mods = moduli(r, ceiling)
     res = np.stack([balanced_residue_array(xi, m) for m in mods]) if r else None
-    digits = np.stack([limb_digits(res[l]) for l in range(r)])
+    digits = np.stack([digits_of_modulus(res[l], mods[l], l, ceiling) for l in range(r)])
     return dict(shift=s, xint=xi, res=res, digits=digits)
 
 
