@@ -138,7 +138,8 @@ int ozemu_bit_budget(int k, int r, int* p_a, int* p_b);
  * (r = 1 for INT8 planes); 0 on bad arguments.  host. */
 size_t ozemu_plane_bytes(int rows, int k, int r);
 
-/* Bytes of the residue output of an m x n product with r moduli. host. */
+/* Bytes of the residue output of an m x n product with r moduli (r up to
+ * 20, the mixed-digit list's limit; 0 on bad arguments). host. */
 size_t ozemu_residue_bytes(int m, int n, int r);
 
 /* ------------------------------------------------------------------------ */
@@ -375,6 +376,74 @@ int ozemu_dgemm_2limb(int m, int n, int k, const double* A, int lda, const doubl
  * stream and synchronisation rules); the result equals ozemu_dgemm_2limb's
  * bit for bit. */
 int ozemu_dgemm_host_2limb(int m, int n, int k, const double* A, int lda, const double* B,
+                           int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Mixed-digit moduli: fewer FP4 products per output                        */
+/* ------------------------------------------------------------------------ */
+
+/* [AWE] abstract: the digit set S holds every residue modulo 13, encodings
+ * are chosen per input range, and the formulation holds modulo m, so the
+ * residue number system of Ozaki scheme II can take fewer FP4 products than
+ * nine per modulus (the page counts 75 products of prior work for the FP64
+ * significand and 59 with its encodings, which it does not print).  This
+ * family is our reading of that: a modulus m for which S meets every residue
+ * class mod m (only m <= 13: 2..9, 11, 13, found by brute force over S)
+ * needs ONE digit per residue, and its residue product is ONE FP4 product.
+ *
+ *   - Moduli: the pairwise-coprime set of such m with the largest product,
+ *     8, 13, 11, 9, 7, 5 (the "single-digit" moduli, even one first), then
+ *     the greedy pairwise-coprime integers counting down from 113 coprime to
+ *     those (113, 109, 107, 103, 101, 97, 89, 83, 79, 73, 71, 67, 61, 59),
+ *     which take two base-13 digits and 4 FP4 products as the two-limb
+ *     moduli do.  1 <= r <= ozemu_max_moduli_mixed() (20).
+ *   - Digits: for a single-digit modulus, the balanced residue x itself when
+ *     it lies in S, else the member of S in x's class of smallest magnitude
+ *     (13: +-5 -> -+8; 11: +-5 -> -+6); its product digit(a) digit(b) is
+ *     congruent to a b mod m.  Two-digit moduli: d0 + 13 d1 as the two-limb
+ *     family.
+ *   - Products per output: ozemu_products_mixed(r) = min(r, 6) + 4 max(r-6, 0):
+ *     r = 19 gives 58 products and, at k = 8192, the bit budget P = 88 that
+ *     r = 13 three-limb moduli (117 products) give.
+ *   - Limb planes: the single-digit moduli first, each [rows_p][k_p/2]
+ *     (the digit of element k at row byte (k/128)*64 + (k%128)/2, two codes
+ *     per byte, low nibble for even k); then the two-digit moduli, each
+ *     [rows_p][k_p] in the two-limb layout.  Total: ozemu_plane_bytes_mixed.
+ *   - Residue layout: as the three-limb calls, with these moduli (r of them).
+ * Bit budget, rounding, CRT and scale-back are those of the other families
+ * with these moduli.  Planes and residues of one family are not valid input
+ * to another family's calls.  Arguments, ownership and errors are those of
+ * the three-limb call of the same name, with r up to 20. */
+int ozemu_max_moduli_mixed(void);          /* 20. host. */
+int ozemu_single_digit_moduli_mixed(void); /* 6: moduli 0..5 are single-digit. host. */
+int ozemu_moduli_mixed(int r, int32_t* out);
+int ozemu_bit_budget_mixed(int k, int r, int* p_a, int* p_b);
+size_t ozemu_plane_bytes_mixed(int rows, int k, int r);
+/* FP4 products per output of the first r moduli; OZEMU_ERR_INVALID_ARG for r
+ * out of range. host. */
+int ozemu_products_mixed(int r);
+int ozemu_split_rows_f64_mixed(int rows, int k, const double* X, int ldx, int p, int r,
+                               uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+int ozemu_split_cols_f64_mixed(int k, int cols, const double* X, int ldx, int p, int r,
+                               uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+/* Residues of C' = A'B' for the mixed-digit moduli: one launch of one FP4
+ * product per K step for the single-digit moduli (exact FP32 accumulation
+ * over chunks of 2^18, |digit| <= 8) and one of four products for the
+ * two-digit ones. */
+int ozemu_residue_gemm_mixed(int m, int n, int k, int r, const uint8_t* a_planes,
+                             const uint8_t* b_planes, uint8_t* residues, cudaStream_t stream);
+int ozemu_crt_f64_mixed(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a,
+                        const int32_t* shifts_b, double* C, int ldc, cudaStream_t stream);
+
+/* C = A B (device buffers, as ozemu_dgemm) through the mixed-digit stages.
+ * Requires 2k < m_1...m_r of these moduli.  No narrow path; m >= 2048
+ * pipelines the stages over row chunks like ozemu_dgemm.  Cached workspace. */
+int ozemu_dgemm_mixed(int m, int n, int k, const double* A, int lda, const double* B,
+                      int ldb, double* C, int ldc, int r, cudaStream_t stream);
+
+/* ozemu_dgemm_mixed with HOST buffers, pipelined like ozemu_dgemm_host; the
+ * result equals ozemu_dgemm_mixed's bit for bit. */
+int ozemu_dgemm_host_mixed(int m, int n, int k, const double* A, int lda, const double* B,
                            int ldb, double* C, int ldc, int r, cudaStream_t stream);
 
 #ifdef __cplusplus

@@ -80,6 +80,18 @@ _SIGNATURES = {
     "ozemu_set_workspace_limit": (_I, [_S]),
     "ozemu_workspace_limit": (_S, []),
     "ozemu_probe_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
+    "ozemu_max_moduli_mixed": (_I, []),
+    "ozemu_single_digit_moduli_mixed": (_I, []),
+    "ozemu_moduli_mixed": (_I, [_I, _P]),
+    "ozemu_bit_budget_mixed": (_I, [_I, _I, _P, _P]),
+    "ozemu_plane_bytes_mixed": (_S, [_I, _I, _I]),
+    "ozemu_products_mixed": (_I, [_I]),
+    "ozemu_split_rows_f64_mixed": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "ozemu_split_cols_f64_mixed": (_I, [_I, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "ozemu_residue_gemm_mixed": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
+    "ozemu_crt_f64_mixed": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P]),
+    "ozemu_dgemm_mixed": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
+    "ozemu_dgemm_host_mixed": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
 }
 
 
@@ -273,6 +285,62 @@ def ozemu_dgemm_2limb(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
 
 def ozemu_dgemm_host_2limb(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
     return _call("ozemu_dgemm_host_2limb", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
+
+
+def ozemu_max_moduli_mixed():
+    return _call("ozemu_max_moduli_mixed")
+
+
+def ozemu_single_digit_moduli_mixed():
+    return _call("ozemu_single_digit_moduli_mixed")
+
+
+def ozemu_moduli_mixed(r):
+    buf = (ctypes.c_int32 * max(r, 1))()
+    st = _call("ozemu_moduli_mixed", r, ctypes.cast(buf, ctypes.c_void_p))
+    if st != OZEMU_OK:
+        raise OzemuError(st, "ozemu_moduli_mixed")
+    return [int(x) for x in buf[:r]]
+
+
+def ozemu_bit_budget_mixed(k, r):
+    pa, pb = ctypes.c_int(0), ctypes.c_int(0)
+    st = _call("ozemu_bit_budget_mixed", k, r, ctypes.byref(pa), ctypes.byref(pb))
+    if st != OZEMU_OK:
+        raise OzemuError(st, "ozemu_bit_budget_mixed")
+    return pa.value, pb.value
+
+
+def ozemu_plane_bytes_mixed(rows, k, r):
+    return _call("ozemu_plane_bytes_mixed", rows, k, r)
+
+
+def ozemu_products_mixed(r):
+    return _call("ozemu_products_mixed", r)
+
+
+def ozemu_split_rows_f64_mixed(rows, k, X, ldx, p, r, planes, shifts, stream):
+    return _call("ozemu_split_rows_f64_mixed", rows, k, X, ldx, p, r, planes, shifts, stream)
+
+
+def ozemu_split_cols_f64_mixed(k, cols, X, ldx, p, r, planes, shifts, stream):
+    return _call("ozemu_split_cols_f64_mixed", k, cols, X, ldx, p, r, planes, shifts, stream)
+
+
+def ozemu_residue_gemm_mixed(m, n, k, r, a_planes, b_planes, residues, stream):
+    return _call("ozemu_residue_gemm_mixed", m, n, k, r, a_planes, b_planes, residues, stream)
+
+
+def ozemu_crt_f64_mixed(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream):
+    return _call("ozemu_crt_f64_mixed", m, n, r, residues, shifts_a, shifts_b, C, ldc, stream)
+
+
+def ozemu_dgemm_mixed(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
+    return _call("ozemu_dgemm_mixed", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
+
+
+def ozemu_dgemm_host_mixed(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
+    return _call("ozemu_dgemm_host_mixed", m, n, k, A, lda, B, ldb, C, ldc, r, stream)
 
 
 # ------------------------------------------------------- torch marshalling
@@ -539,4 +607,76 @@ def crt_f64_2limb(m, n, r, residues, shifts_a, shifts_b, out=None, stream=None):
     C = torch.empty((m, n), dtype=torch.float64, device=residues.device) if out is None else out
     _check(ozemu_crt_f64_2limb(m, n, r, residues.data_ptr(), shifts_a.data_ptr(), shifts_b.data_ptr(),
                                C.data_ptr(), _ld(C), _stream(stream)), "ozemu_crt_f64_2limb")
+    return C
+
+
+# --------------------------------------------------- mixed-digit moduli
+
+def dgemm_mixed(A, B, r, out=None, stream=None):
+    """Emulated fp64 A @ B with r mixed-digit moduli (one FP4 product for
+    each single-digit modulus, four for each two-digit one)."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2:
+        raise ValueError("inner dimensions differ")
+    C = torch.empty((m, n), dtype=torch.float64, device=A.device) if out is None else out
+    _check(ozemu_dgemm_mixed(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
+                             _stream(stream)), "ozemu_dgemm_mixed")
+    return C
+
+
+def dgemm_host_mixed(A, B, r, out=None, stream=None):
+    """ozemu_dgemm_host_mixed of CPU float64 tensors (pinned for overlap);
+    returns the CPU result after synchronising the stream."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2 or A.device.type != "cpu" or B.device.type != "cpu":
+        raise ValueError("expected CPU matrices with matching inner dimension")
+    C = torch.empty((m, n), dtype=torch.float64, pin_memory=A.is_pinned()) if out is None else out
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(ozemu_dgemm_host_mixed(m, n, k, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C), r,
+                                  s.cuda_stream), "ozemu_dgemm_host_mixed")
+    s.synchronize()
+    return C
+
+
+def split_rows_f64_mixed(X, p, r, stream=None):
+    """(planes, shifts) of the rows of a cuda float64 matrix, mixed digits."""
+    torch = _torch()
+    rows, k = X.shape
+    planes = torch.empty(ozemu_plane_bytes_mixed(rows, k, r), dtype=torch.uint8, device=X.device)
+    shifts = torch.empty(rows, dtype=torch.int32, device=X.device)
+    _check(ozemu_split_rows_f64_mixed(rows, k, X.data_ptr(), _ld(X), p, r, planes.data_ptr(), shifts.data_ptr(),
+                                      _stream(stream)), "ozemu_split_rows_f64_mixed")
+    return planes, shifts
+
+
+def split_cols_f64_mixed(X, p, r, stream=None):
+    """(planes, shifts) of the columns of a cuda float64 matrix, mixed digits."""
+    torch = _torch()
+    k, cols = X.shape
+    planes = torch.empty(ozemu_plane_bytes_mixed(cols, k, r), dtype=torch.uint8, device=X.device)
+    shifts = torch.empty(cols, dtype=torch.int32, device=X.device)
+    _check(ozemu_split_cols_f64_mixed(k, cols, X.data_ptr(), _ld(X), p, r, planes.data_ptr(), shifts.data_ptr(),
+                                      _stream(stream)), "ozemu_split_cols_f64_mixed")
+    return planes, shifts
+
+
+def residue_gemm_mixed(m, n, k, r, a_planes, b_planes, out=None, stream=None):
+    """uint8 residues [r][m][round_up(n, 16)] of the mixed-digit product."""
+    torch = _torch()
+    ldr = (n + 15) // 16 * 16
+    res = torch.empty((r, m, ldr), dtype=torch.uint8, device=a_planes.device) if out is None else out
+    _check(ozemu_residue_gemm_mixed(m, n, k, r, a_planes.data_ptr(), b_planes.data_ptr(), res.data_ptr(),
+                                    _stream(stream)), "ozemu_residue_gemm_mixed")
+    return res
+
+
+def crt_f64_mixed(m, n, r, residues, shifts_a, shifts_b, out=None, stream=None):
+    torch = _torch()
+    C = torch.empty((m, n), dtype=torch.float64, device=residues.device) if out is None else out
+    _check(ozemu_crt_f64_mixed(m, n, r, residues.data_ptr(), shifts_a.data_ptr(), shifts_b.data_ptr(),
+                               C.data_ptr(), _ld(C), _stream(stream)), "ozemu_crt_f64_mixed")
     return C

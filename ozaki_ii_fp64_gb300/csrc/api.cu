@@ -16,30 +16,47 @@ typedef unsigned __int128 u128;
 
 // ------------------------------------------------------------------ moduli
 // Greedy pairwise-coprime integers counting down from the ceiling: 256 for
-// the 3-limb moduli, 113 for the two-limb moduli.
+// the 3-limb moduli, 113 for the two-limb moduli.  The mixed-digit list
+// starts from the given single-digit moduli and continues the greedy count
+// from 113 with integers coprime to every modulus taken.
+uint32_t gcd_u32(uint32_t a, uint32_t b) {
+  while (b) {
+    uint32_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
 struct ModuliTable {
-  uint32_t m[kMaxModuli];
-  explicit ModuliTable(uint32_t ceiling) {
-    int n = 0;
-    for (uint32_t c = ceiling; n < kMaxModuli && c >= 2; --c) {
+  uint32_t m[kMaxR] = {};
+  int count = 0;
+  ModuliTable(uint32_t ceiling, int max_r, const uint32_t* first = nullptr, int n_first = 0) {
+    for (int i = 0; i < n_first; ++i) m[count++] = first[i];
+    for (uint32_t c = ceiling; count < max_r && c >= 2; --c) {
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        uint32_t a = c, b = m[j];
-        while (b) {
-          uint32_t t = a % b;
-          a = b;
-          b = t;
-        }
-        ok = (a == 1);
-      }
-      if (ok) m[n++] = c;
+      for (int j = 0; j < count && ok; ++j) ok = gcd_u32(c, m[j]) == 1;
+      if (ok) m[count++] = c;
     }
   }
 };
+
+// The moduli m <= 13 whose every residue class holds a member of S (one FP4
+// digit per residue), as a pairwise-coprime set of largest product, the even
+// one first: their residue products take one FP4 product each.
+constexpr uint32_t kSingleDigitModuli[kMixSingle] = {8, 13, 11, 9, 7, 5};
+
+// limbs: 3 (three-limb list), 2 (two-limb list), 1 (mixed-digit list).
 const ModuliTable& moduli(int limbs = 3) {
-  static const ModuliTable t3(256), t2(113);
-  return limbs == 2 ? t2 : t3;
+  static const ModuliTable t3(256, kMaxModuli), t2(113, kMaxModuli),
+      t1(113, kMaxModuliMix, kSingleDigitModuli, kMixSingle);
+  return limbs == 1 ? t1 : (limbs == 2 ? t2 : t3);
 }
+
+int max_r(int limbs) { return limbs == 1 ? kMaxModuliMix : kMaxModuli; }
+
+// Single-digit moduli among the first r of the list (mixed-digit list only).
+int single_count(int r, int limbs) { return limbs == 1 ? (r < kMixSingle ? r : kMixSingle) : 0; }
 
 u128 modulus_product(int r, int limbs = 3) {
   u128 p = 1;
@@ -88,7 +105,8 @@ SplitModuli split_moduli(int r, int limbs = 3) {
   s.limbs = limbs;
   for (int l = 0; l < r; ++l) {
     s.m[l] = moduli(limbs).m[l];
-    if (s.m[l] != (limbs == 2 ? kModulusTable2[l] : kModulusTable[l])) s.r = 0;  // mismatch: the launch refuses
+    const uint32_t want = limbs == 1 ? kModulusTableMix[l] : (limbs == 2 ? kModulusTable2[l] : kModulusTable[l]);
+    if (s.m[l] != want) s.r = 0;  // mismatch: the launch refuses
   }
   return s;
 }
@@ -115,11 +133,12 @@ bool narrow_enabled() {
   return !(s && s[0] == '0');
 }
 
-EpiModuli epi_moduli(int r, int limbs = 3) {
+// Epilogue constants of moduli first .. first + r - 1 of the list.
+EpiModuli epi_moduli(int r, int limbs = 3, int first = 0) {
   EpiModuli e;
   std::memset(&e, 0, sizeof(e));
   for (int l = 0; l < r; ++l) {
-    const uint32_t m = moduli(limbs).m[l];
+    const uint32_t m = moduli(limbs).m[first + l];
     e.m[l] = static_cast<float>(m);
     e.inv_m[l] = 1.0f / static_cast<float>(m);
     const int w = static_cast<int>(169u % m);
@@ -161,7 +180,8 @@ CrtModuli crt_moduli(int r, int limbs = 3) {
   for (int t = 0; t < 9; ++t) c.m16[t] = t < 8 ? static_cast<uint32_t>((M >> (16 * t)) & 0xFFFF) : 0u;
   int bits = 0;
   while (bits < 128 && (M >> bits) != 0) ++bits;
-  if (bits != (limbs == 2 ? kCrtBits2[r] : kCrtBits[r])) c.r = 0;  // table mismatch: the launch refuses r = 0
+  const int want = limbs == 1 ? kCrtBitsMix[r] : (limbs == 2 ? kCrtBits2[r] : kCrtBits[r]);
+  if (bits != want) c.r = 0;  // table mismatch: the launch refuses r = 0
   const long double Md = static_cast<long double>(M);
   for (int t = 0; t < 9; ++t) c.gt[t] = static_cast<float>(std::ldexp(1.0L, 16 * t) / Md);
   return c;
@@ -251,8 +271,17 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Digit planes of the first r moduli: limbs per modulus for the three- and
+// two-limb lists; one per single-digit and two per two-digit modulus for the
+// mixed-digit list.
+long long digit_planes(int r, int limbs) {
+  if (limbs != 1) return static_cast<long long>(limbs) * r;
+  const int single = single_count(r, limbs);
+  return single + 2LL * (r - single);
+}
+
 size_t plane_bytes(long long rows, long long k, int r, int limbs = 3) {
-  return static_cast<size_t>(static_cast<long long>(limbs) * r * round_up(static_cast<int>(rows), kRowAlign)) *
+  return static_cast<size_t>(digit_planes(r, limbs) * round_up(static_cast<int>(rows), kRowAlign)) *
          static_cast<size_t>(round_up(static_cast<int>(k), kKAlign) / 2);
 }
 
@@ -280,6 +309,39 @@ int split_cols_f64(int k, int cols, const double* X, long long ldx, int p, int r
 
 int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* bp, uint8_t* res, DeviceState* d,
                  cudaStream_t st, int limbs = 3) {
+  if (limbs == 1) {
+    // Mixed-digit list: the single-digit moduli (one FP4 product each) and
+    // the two-digit moduli (four) are two launches over their own planes,
+    // writing consecutive moduli of the residue output.
+    const int single = single_count(r, limbs);
+    const size_t kp2 = static_cast<size_t>(round_up(k, kKAlign) / 2);
+    const size_t a_off = static_cast<size_t>(single) * round_up(m, kRowAlign) * kp2;
+    const size_t b_off = static_cast<size_t>(single) * round_up(n, kRowAlign) * kp2;
+    const size_t r_off = static_cast<size_t>(single) * m * round_up(n, 16);
+    for (int grp = 0; grp < 2; ++grp) {
+      const int rg = grp == 0 ? single : r - single;
+      if (rg == 0) continue;
+      LimbGemmCall c;
+      c.residue_mode = true;
+      c.m = m;
+      c.n = n;
+      c.k = k;
+      c.r = rg;
+      c.a_planes = grp == 0 ? ap : ap + a_off;
+      c.b_planes = grp == 0 ? bp : bp + b_off;
+      c.res_out = grp == 0 ? res : res + r_off;
+      c.ldr = round_up(n, 16);
+      c.c32 = nullptr;
+      c.ldc = 0;
+      c.kc_blocks = kchunk_blocks();
+      c.limbs = grp == 0 ? 1 : 2;
+      c.em = epi_moduli(rg, limbs, grp == 0 ? 0 : single);
+      c.flags = d->flags;
+      const int s = cuda_status(launch_limb_gemm(c, st));
+      if (s != OZEMU_OK) return s;
+    }
+    return OZEMU_OK;
+  }
   LimbGemmCall c;
   c.residue_mode = true;
   c.m = m;
@@ -627,7 +689,7 @@ size_t ozemu_plane_bytes(int rows, int k, int r) {
 }
 
 size_t ozemu_residue_bytes(int m, int n, int r) {
-  if (m < 0 || n < 0 || r < 1 || r > kMaxModuli) return 0;
+  if (m < 0 || n < 0 || r < 1 || r > kMaxR) return 0;
   return static_cast<size_t>(r) * static_cast<size_t>(m) * static_cast<size_t>(round_up(n, 16));
 }
 
@@ -645,7 +707,7 @@ int ozemu_split_rows_f64(int rows, int k, const double* X, int ldx, int p, int r
 
 static int split_cols_entry(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
                             int32_t* shifts, cudaStream_t stream, int limbs) {
-  if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+  if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1) || p < 0 || p > 62 || r < 1 || r > max_r(limbs))
     return OZEMU_ERR_INVALID_ARG;
   if (cols == 0) return OZEMU_OK;
   if ((k > 0 && !X) || !planes || !shifts || !aligned16(planes) || !rows_ok(cols, r)) return OZEMU_ERR_INVALID_ARG;
@@ -736,7 +798,7 @@ int ozemu_residue_gemm_i8(int m, int n, int k, int r, const int8_t* a_res8, cons
 
 static int residue_gemm_entry(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
                               uint8_t* residues, cudaStream_t stream, int limbs) {
-  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > max_r(limbs)) return OZEMU_ERR_INVALID_ARG;
   if (m == 0 || n == 0) return OZEMU_OK;
   if (!residues || !aligned16(residues) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
   if (k > 0 && (!a_planes || !b_planes || !aligned16(a_planes) || !aligned16(b_planes)))
@@ -789,7 +851,7 @@ int ozemu_residues_narrow_f64(int m, int n, int k, int r, const double* A, int l
 
 static int crt_entry(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a, const int32_t* shifts_b,
                      double* C, int ldc, cudaStream_t stream, int limbs) {
-  if (m < 0 || n < 0 || r < 1 || r > kMaxModuli || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m < 0 || n < 0 || r < 1 || r > max_r(limbs) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
   if (m == 0 || n == 0) return OZEMU_OK;
   if (!residues || !aligned16(residues) || !shifts_a || !shifts_b || !C) return OZEMU_ERR_INVALID_ARG;
   DeviceState* d = nullptr;
@@ -870,37 +932,99 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r), stream));
 }
 
-// ---------------------------------------------------------- two-limb moduli
-int ozemu_moduli_2limb(int r, int32_t* out) {
-  if (r < 1 || r > kMaxModuli || !out) return OZEMU_ERR_INVALID_ARG;
-  for (int l = 0; l < r; ++l) out[l] = static_cast<int32_t>(moduli(2).m[l]);
+// ------------------------------------------- two-limb and mixed-digit moduli
+// The entry points of the two families share these bodies; `limbs` names
+// the list (2: two-limb, 1: mixed-digit).
+static int family_moduli(int r, int32_t* out, int limbs) {
+  if (r < 1 || r > max_r(limbs) || !out) return OZEMU_ERR_INVALID_ARG;
+  for (int l = 0; l < r; ++l) out[l] = static_cast<int32_t>(moduli(limbs).m[l]);
   return OZEMU_OK;
 }
 
-int ozemu_bit_budget_2limb(int k, int r, int* p_a, int* p_b) {
-  if (k < 1 || r < 1 || r > kMaxModuli || !p_a || !p_b) return OZEMU_ERR_INVALID_ARG;
-  const int P = budget_P(k, r, 2);
+static int family_bit_budget(int k, int r, int* p_a, int* p_b, int limbs) {
+  if (k < 1 || r < 1 || r > max_r(limbs) || !p_a || !p_b) return OZEMU_ERR_INVALID_ARG;
+  const int P = budget_P(k, r, limbs);
   if (P < 0) return OZEMU_ERR_INVALID_ARG;
   *p_a = (P + 1) / 2;
   *p_b = P / 2;
   return OZEMU_OK;
 }
 
-size_t ozemu_plane_bytes_2limb(int rows, int k, int r) {
-  if (rows < 0 || k < 0 || r < 1 || r > kMaxModuli) return 0;
-  return plane_bytes(rows, k, r, 2);
+static size_t family_plane_bytes(int rows, int k, int r, int limbs) {
+  if (rows < 0 || k < 0 || r < 1 || r > max_r(limbs)) return 0;
+  return plane_bytes(rows, k, r, limbs);
 }
 
-int ozemu_split_rows_f64_2limb(int rows, int k, const double* X, int ldx, int p, int r, uint8_t* planes,
-                               int32_t* shifts, cudaStream_t stream) {
-  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1) || p < 0 || p > 62 || r < 1 || r > kMaxModuli)
+static int family_split_rows(int rows, int k, const double* X, int ldx, int p, int r, uint8_t* planes,
+                             int32_t* shifts, cudaStream_t stream, int limbs) {
+  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1) || p < 0 || p > 62 || r < 1 || r > max_r(limbs))
     return OZEMU_ERR_INVALID_ARG;
   if (rows == 0) return OZEMU_OK;
   if ((k > 0 && !X) || !planes || !shifts || !aligned16(planes) || !rows_ok(rows, r)) return OZEMU_ERR_INVALID_ARG;
   DeviceState* d = nullptr;
   int s = device_state(&d);
   if (s != OZEMU_OK) return s;
-  return split_rows_f64(rows, k, X, ldx, p, r, planes, shifts, d, stream, 2);
+  return split_rows_f64(rows, k, X, ldx, p, r, planes, shifts, d, stream, limbs);
+}
+
+static int family_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                        int r, cudaStream_t stream, int limbs, bool from_host) {
+  if (m < 0 || n < 0 || k < 0 || r < 1 || r > max_r(limbs)) return OZEMU_ERR_INVALID_ARG;
+  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
+  int pa_bits = 0, pb_bits = 0;
+  if (k > 0 && family_bit_budget(k, r, &pa_bits, &pb_bits, limbs) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (from_host) {
+    s = pipeline_state(d);
+    if (s != OZEMU_OK) return s;
+    if (k == 0) {
+      uint8_t* buf = nullptr;
+      s = workspace(d, align256(static_cast<size_t>(m) * n * 8), &buf);
+      if (s != OZEMU_OK) return s;
+      double* Cd = reinterpret_cast<double*>(buf);
+      if (launch_zero_f64(Cd, m, n, n, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
+      return cuda_status(cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 8, Cd, n * 8, static_cast<size_t>(n) * 8,
+                                           m, cudaMemcpyDeviceToHost, stream));
+    }
+    return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, true, d, stream, limbs);
+  }
+  if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
+  if (m >= 2048) return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, false, d, stream, limbs);
+  const size_t pa = align256(plane_bytes(m, k, r, limbs)), pb = align256(plane_bytes(n, k, r, limbs));
+  const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
+  const size_t rb = align256(ozemu_residue_bytes(m, n, r));
+  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  uint8_t* ws = nullptr;
+  s = workspace(d, pa + pb + sa + sb + rb + bt, &ws);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ap = ws;
+  uint8_t* bp = ap + pa;
+  int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
+  int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
+  uint8_t* res = bp + pb + sa + sb;
+  double* btr = reinterpret_cast<double*>(res + rb);
+  s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, d, stream, limbs);
+  if (s != OZEMU_OK) return s;
+  s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, d, stream, limbs);
+  if (s != OZEMU_OK) return s;
+  s = residue_gemm(m, n, k, r, ap, bp, res, d, stream, limbs);
+  if (s != OZEMU_OK) return s;
+  return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r, limbs), stream));
+}
+
+int ozemu_moduli_2limb(int r, int32_t* out) { return family_moduli(r, out, 2); }
+
+int ozemu_bit_budget_2limb(int k, int r, int* p_a, int* p_b) { return family_bit_budget(k, r, p_a, p_b, 2); }
+
+size_t ozemu_plane_bytes_2limb(int rows, int k, int r) { return family_plane_bytes(rows, k, r, 2); }
+
+int ozemu_split_rows_f64_2limb(int rows, int k, const double* X, int ldx, int p, int r, uint8_t* planes,
+                               int32_t* shifts, cudaStream_t stream) {
+  return family_split_rows(rows, k, X, ldx, p, r, planes, shifts, stream, 2);
 }
 
 int ozemu_split_cols_f64_2limb(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
@@ -920,62 +1044,58 @@ int ozemu_crt_f64_2limb(int m, int n, int r, const uint8_t* residues, const int3
 
 int ozemu_dgemm_host_2limb(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C,
                            int ldc, int r, cudaStream_t stream) {
-  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
-  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
-  if (m == 0 || n == 0) return OZEMU_OK;
-  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
-  int pa_bits = 0, pb_bits = 0;
-  if (k > 0 && ozemu_bit_budget_2limb(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
-  DeviceState* d = nullptr;
-  int s = device_state(&d);
-  if (s != OZEMU_OK) return s;
-  s = pipeline_state(d);
-  if (s != OZEMU_OK) return s;
-  if (k == 0) {
-    uint8_t* buf = nullptr;
-    s = workspace(d, align256(static_cast<size_t>(m) * n * 8), &buf);
-    if (s != OZEMU_OK) return s;
-    double* Cd = reinterpret_cast<double*>(buf);
-    if (launch_zero_f64(Cd, m, n, n, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
-    return cuda_status(cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 8, Cd, n * 8, static_cast<size_t>(n) * 8, m,
-                                         cudaMemcpyDeviceToHost, stream));
-  }
-  return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, true, d, stream, 2);
+  return family_dgemm(m, n, k, A, lda, B, ldb, C, ldc, r, stream, 2, true);
 }
 
 int ozemu_dgemm_2limb(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
                       int r, cudaStream_t stream) {
-  if (m < 0 || n < 0 || k < 0 || r < 1 || r > kMaxModuli) return OZEMU_ERR_INVALID_ARG;
-  if (lda < (k > 1 ? k : 1) || ldb < (n > 1 ? n : 1) || ldc < (n > 1 ? n : 1)) return OZEMU_ERR_INVALID_ARG;
-  if (m == 0 || n == 0) return OZEMU_OK;
-  if (!C || (k > 0 && (!A || !B)) || !rows_ok(m, r) || !rows_ok(n, r)) return OZEMU_ERR_INVALID_ARG;
-  int pa_bits = 0, pb_bits = 0;
-  if (k > 0 && ozemu_bit_budget_2limb(k, r, &pa_bits, &pb_bits) != OZEMU_OK) return OZEMU_ERR_INVALID_ARG;
-  DeviceState* d = nullptr;
-  int s = device_state(&d);
-  if (s != OZEMU_OK) return s;
-  if (k == 0) return cuda_status(launch_zero_f64(C, m, n, ldc, stream));
-  if (m >= 2048) return dgemm_chunked(m, n, k, A, lda, B, ldb, C, ldc, r, pa_bits, pb_bits, false, d, stream, 2);
-  const size_t pa = align256(plane_bytes(m, k, r, 2)), pb = align256(plane_bytes(n, k, r, 2));
-  const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
-  const size_t rb = align256(ozemu_residue_bytes(m, n, r));
-  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
-  uint8_t* ws = nullptr;
-  s = workspace(d, pa + pb + sa + sb + rb + bt, &ws);
-  if (s != OZEMU_OK) return s;
-  uint8_t* ap = ws;
-  uint8_t* bp = ap + pa;
-  int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
-  int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
-  uint8_t* res = bp + pb + sa + sb;
-  double* btr = reinterpret_cast<double*>(res + rb);
-  s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, d, stream, 2);
-  if (s != OZEMU_OK) return s;
-  s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, d, stream, 2);
-  if (s != OZEMU_OK) return s;
-  s = residue_gemm(m, n, k, r, ap, bp, res, d, stream, 2);
-  if (s != OZEMU_OK) return s;
-  return cuda_status(launch_crt_f64(m, n, res, round_up(n, 16), sap, sbp, C, ldc, crt_moduli(r, 2), stream));
+  return family_dgemm(m, n, k, A, lda, B, ldb, C, ldc, r, stream, 2, false);
+}
+
+int ozemu_max_moduli_mixed(void) { return kMaxModuliMix; }
+
+int ozemu_single_digit_moduli_mixed(void) { return kMixSingle; }
+
+int ozemu_moduli_mixed(int r, int32_t* out) { return family_moduli(r, out, 1); }
+
+int ozemu_bit_budget_mixed(int k, int r, int* p_a, int* p_b) { return family_bit_budget(k, r, p_a, p_b, 1); }
+
+size_t ozemu_plane_bytes_mixed(int rows, int k, int r) { return family_plane_bytes(rows, k, r, 1); }
+
+int ozemu_products_mixed(int r) {
+  if (r < 1 || r > kMaxModuliMix) return OZEMU_ERR_INVALID_ARG;
+  const int single = single_count(r, 1);
+  return single + 4 * (r - single);
+}
+
+int ozemu_split_rows_f64_mixed(int rows, int k, const double* X, int ldx, int p, int r, uint8_t* planes,
+                               int32_t* shifts, cudaStream_t stream) {
+  return family_split_rows(rows, k, X, ldx, p, r, planes, shifts, stream, 1);
+}
+
+int ozemu_split_cols_f64_mixed(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
+                               int32_t* shifts, cudaStream_t stream) {
+  return split_cols_entry(k, cols, X, ldx, p, r, planes, shifts, stream, 1);
+}
+
+int ozemu_residue_gemm_mixed(int m, int n, int k, int r, const uint8_t* a_planes, const uint8_t* b_planes,
+                             uint8_t* residues, cudaStream_t stream) {
+  return residue_gemm_entry(m, n, k, r, a_planes, b_planes, residues, stream, 1);
+}
+
+int ozemu_crt_f64_mixed(int m, int n, int r, const uint8_t* residues, const int32_t* shifts_a,
+                        const int32_t* shifts_b, double* C, int ldc, cudaStream_t stream) {
+  return crt_entry(m, n, r, residues, shifts_a, shifts_b, C, ldc, stream, 1);
+}
+
+int ozemu_dgemm_mixed(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                      int r, cudaStream_t stream) {
+  return family_dgemm(m, n, k, A, lda, B, ldb, C, ldc, r, stream, 1, false);
+}
+
+int ozemu_dgemm_host_mixed(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C,
+                           int ldc, int r, cudaStream_t stream) {
+  return family_dgemm(m, n, k, A, lda, B, ldb, C, ldc, r, stream, 1, true);
 }
 
 int ozemu_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,

@@ -11,7 +11,9 @@
 
 namespace ozemu {
 
-constexpr int kMaxModuli = 16;
+constexpr int kMaxModuli = 16;   // r limit of the three-limb and two-limb moduli
+constexpr int kMaxModuliMix = 20;  // r limit of the mixed-digit moduli
+constexpr int kMaxR = 20;        // size of the per-modulus constant arrays
 constexpr int kRowAlign = 128;   // plane rows padded to this (GEMM tile M)
 constexpr int kKAlign = 128;     // plane k padded to this (GEMM stage K)
 
@@ -35,13 +37,23 @@ constexpr uint32_t kModulusTable[kMaxModuli] = {256, 255, 253, 251, 247, 241, 23
 constexpr uint32_t kModulusTable2[kMaxModuli] = {113, 112, 111, 109, 107, 103, 101, 97,
                                                  95,  89,  83,  79,  73,  71,  67,  61};
 
+// The mixed-digit moduli.  The first kMixSingle are the moduli m for which
+// a single member of S lies in every residue class (m <= 13; the set with the
+// largest product, 8 13 11 9 7 5 = 360360, the even one first): their residue
+// product is ONE FP4 product.  The rest are the greedy pairwise-coprime
+// integers counting down from 113 that are coprime to those (all prime):
+// two base-13 digits each, 4 FP4 products, as the two-limb moduli.
+constexpr int kMixSingle = 6;
+constexpr uint32_t kModulusTableMix[kMaxModuliMix] = {8,   13,  11,  9,   7,  5,  113, 109, 107, 103,
+                                                      101, 97,  89,  83,  79, 73, 71,  67,  61,  59};
+
 // Moduli of a deconstruction launch: limbs 3 takes kModulusTable, limbs 2
-// kModulusTable2 (r = 0 if the host's moduli differ from the table; the
-// launch then refuses).
+// kModulusTable2, limbs 1 the mixed-digit kModulusTableMix (r = 0 if the
+// host's moduli differ from the table; the launch then refuses).
 struct SplitModuli {
   int r;
   int limbs;
-  uint32_t m[kMaxModuli];
+  uint32_t m[kMaxR];
 };
 
 // Per-modulus constants for the fused narrow-N path.
@@ -57,9 +69,9 @@ struct NarrowModuli {
 
 // Per-modulus constants for the GEMM epilogue.
 struct EpiModuli {
-  float m[kMaxModuli];
-  float inv_m[kMaxModuli];      // 1/m rounded to fp32
-  float w169[kMaxModuli];       // 169 mod m, balanced: |w| <= m/2
+  float m[kMaxR];
+  float inv_m[kMaxR];      // 1/m rounded to fp32
+  float w169[kMaxR];       // 169 mod m, balanced: |w| <= m/2
 };
 
 // Mixed-radix CRT constants.
@@ -68,17 +80,20 @@ struct EpiModuli {
 constexpr int kCrtBits[kMaxModuli + 1] = {0, 9, 16, 24, 32, 40, 48, 56, 64, 72, 80, 88, 95, 103, 111, 118, 126};
 // The same for the two-limb moduli (kModulusTable2).
 constexpr int kCrtBits2[kMaxModuli + 1] = {0, 7, 14, 21, 28, 34, 41, 48, 54, 61, 67, 74, 80, 86, 92, 99, 104};
+// The same for the mixed-digit moduli (kModulusTableMix).
+constexpr int kCrtBitsMix[kMaxModuliMix + 1] = {0,  4,  7,  11, 14, 17, 19, 26, 33, 39, 46,
+                                                53, 59, 66, 72, 78, 85, 91, 97, 103, 109};
 
 struct CrtModuli {
   int r;
-  int limbs;                              // 3: kModulusTable, 2: kModulusTable2
-  uint32_t m[kMaxModuli];
-  uint32_t magic[kMaxModuli];             // floor(2^32 / m)
-  uint32_t inv[kMaxModuli];               // (m_0 ... m_{l-1})^-1 mod m_l
-  uint32_t g[kMaxModuli][kMaxModuli];     // g[l][j] = (m_0...m_{j-1}) inv_l mod m_l, j < l
-  uint32_t prefix[kMaxModuli][4];         // m_0 ... m_{l-1} as 128-bit little-endian words
+  int limbs;                              // 3: kModulusTable, 2: kModulusTable2, 1: kModulusTableMix
+  uint32_t m[kMaxR];
+  uint32_t magic[kMaxR];                  // floor(2^32 / m)
+  uint32_t inv[kMaxR];                    // (m_0 ... m_{l-1})^-1 mod m_l
+  uint32_t g[kMaxR][kMaxR];               // g[l][j] = (m_0...m_{j-1}) inv_l mod m_l, j < l
+  uint32_t prefix[kMaxR][4];              // m_0 ... m_{l-1} as 128-bit little-endian words
   // Direct form: C' = sum_l c_l W_l - q M with W_l = (M/m_l) ((M/m_l)^-1 mod m_l).
-  uint32_t wb[4][16];                     // byte w of W_{4q+i} at byte i of wb[q][w]
+  uint32_t wb[5][16];                     // byte w of W_{4q+i} at byte i of wb[q][w]
   uint32_t wl16[8];                       // W_{r-1} in 16-bit limbs (a lone last modulus, r = 1 mod 4)
   uint32_t m16[9];                        // M in 16-bit limbs
   float gt[9];                            // 2^(16 t) / M

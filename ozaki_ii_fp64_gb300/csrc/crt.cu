@@ -36,7 +36,7 @@ __device__ __forceinline__ uint32_t dp4a_u8(uint32_t a, uint32_t b, uint32_t c) 
 // the estimate may be off by one: that output takes the mixed-radix digits
 // instead (crt_round), which are exact for any input.
 // NLimb = 2: the two-limb moduli (kModulusTable2), whose products have the
-// bit lengths kCrtBits2.
+// bit lengths kCrtBits2; NLimb = 1: the mixed-digit moduli (kCrtBitsMix).
 template <int R, int NLimb>
 __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const uint8_t* __restrict__ res,
                                                           long long ldr, const int32_t* __restrict__ sa,
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kCrtThreads) crt_kernel(int m, int n, const ui
                                                           long long ldc, const __grid_constant__ CrtModuli cm) {
   constexpr bool kLastByMad = (R % 4) == 1;   // a lone last modulus: multiply-adds, not dp4a
   constexpr int NQ = kLastByMad ? R / 4 : (R + 3) / 4;  // words of four residues through dp4a
-  constexpr int BM = NLimb == 2 ? kCrtBits2[R] : kCrtBits[R];  // bit length of M
+  constexpr int BM = NLimb == 1 ? kCrtBitsMix[R] : (NLimb == 2 ? kCrtBits2[R] : kCrtBits[R]);  // bit length of M
   constexpr int NL = (BM + 7) / 8;            // bytes of W_l
   constexpr int NT = (NL + 1) / 2;            // 16-bit positions of Y's partial sums
   constexpr int NX = (BM + 15) / 16;          // 16-bit limbs of C' (two's complement)
@@ -165,6 +165,20 @@ cudaError_t launch_crt_r(int m, int n, const uint8_t* residues, long long ldr, c
 
 cudaError_t launch_crt_f64(int m, int n, const uint8_t* residues, long long ldr, const int32_t* sa,
                            const int32_t* sb, double* C, long long ldc, const CrtModuli& cm, cudaStream_t stream) {
+  if (cm.limbs == 1) {  // mixed-digit moduli: r up to kMaxModuliMix
+    switch (cm.r) {
+#define OZEMU_CRT_MIX(R) \
+  case R:                \
+    return launch_crt_r<R, 1>(m, n, residues, ldr, sa, sb, C, ldc, cm, stream);
+      OZEMU_CRT_MIX(1) OZEMU_CRT_MIX(2) OZEMU_CRT_MIX(3) OZEMU_CRT_MIX(4) OZEMU_CRT_MIX(5) OZEMU_CRT_MIX(6)
+      OZEMU_CRT_MIX(7) OZEMU_CRT_MIX(8) OZEMU_CRT_MIX(9) OZEMU_CRT_MIX(10) OZEMU_CRT_MIX(11) OZEMU_CRT_MIX(12)
+      OZEMU_CRT_MIX(13) OZEMU_CRT_MIX(14) OZEMU_CRT_MIX(15) OZEMU_CRT_MIX(16) OZEMU_CRT_MIX(17)
+      OZEMU_CRT_MIX(18) OZEMU_CRT_MIX(19) OZEMU_CRT_MIX(20)
+#undef OZEMU_CRT_MIX
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   switch (cm.r) {
 #define OZEMU_CRT_CASE(R) \
   case R:                 \

@@ -6,8 +6,11 @@
 // [TME4] abstract: the per-output reconstruction term.
 //
 // Balanced digits v_l in [-floor(m_l/2), ceil(m_l/2) - 1] give
-// X = sum_l v_l (m_0 ... m_{l-1}) in [-M/2, M/2 - 1] (m_0 = 256 even, the
-// rest odd), which is the symmetric representative C' directly.  The digit
+// X = sum_l v_l (m_0 ... m_{l-1}) = C' (mod M).  When the one even modulus
+// comes first (256; 8 for the mixed-digit moduli; the other moduli odd), X
+// lies in [-M/2, M/2 - 1] and is the symmetric representative C' directly;
+// with the even modulus elsewhere (112, second of the two-limb moduli) X can
+// lie up to m_0/2 outside it, so X is brought into [-M/2, M/2) by +-M.  The digit
 // recurrence is v_l = c_l inv_l - sum_{j<l} v_j g_{l,j} (mod m_l), with
 // inv_l = (m_0...m_{l-1})^-1 and g_{l,j} = (m_0...m_{j-1}) inv_l mod m_l.
 // No fp64 arithmetic is used.
@@ -156,6 +159,11 @@ __device__ __noinline__ uint64_t crt_round(const uint32_t (&c)[R], int S, const 
     const int sh = 128 - 32 * L;
     X = (X << sh) >> sh;
   }
+  i128 M = 0;
+#pragma unroll
+  for (int t = 7; t >= 0; --t) M = (M << 16) | static_cast<i128>(cm.m16[t]);
+  if (2 * X >= M) X -= M;
+  else if (2 * X < -M) X += M;
   return round_scaled(X, S);
 }
 

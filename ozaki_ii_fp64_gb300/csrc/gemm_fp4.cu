@@ -306,12 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_fp4_fill(d2, a2, b0, idesc, s2, s2, 1u);       // 1 (in D2)
                 mma_fp4_lastuse(d2, a2, b1, idesc, s2, s26, 1u);   // 13 (in D2)
                 mma_fp4(d2, a2, b2, idesc, s26, s26, 1u);          // 169 (in D2)
-              } else {
+              } else if constexpr (NL == 2) {
                 // D1 = A0B0 + 13 (A0B1 + A1B0), D2 = A1B1 (weight 169 at the drain).
                 mma_fp4_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
                 mma_fp4_lastuse(d1, a0, b1, idesc, s2, s26, 1u);   // 13
                 mma_fp4_fill(d1, a1, b0, idesc, s2, s26, 1u);      // 13
                 mma_fp4_lastuse(d2, a1, b1, idesc, s2, s2, acc);   // 1 (in D2)
+              } else {
+                // Single-digit moduli: D1 = A0B0, the residue product itself.
+                (void)a1; (void)a2; (void)b1; (void)b2;
+                mma_fp4(d1, a0, b0, idesc, s2, s2, acc);           // 1
               }
               if (ks == 0)
                 known_full = mbar_test_wait(&full[(it + 1) % C::kStages], ((it + 1) / C::kStages) & 1);
@@ -348,7 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t v1[CW], v2[CW];
         tmem_ld_cols<CW>(tbase + lane_off + kColD1 + col0, v1);
-        tmem_ld_cols<CW>(tbase + lane_off + kColD2 + col0, v2);
+        if constexpr (NL == 1) {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) v2[i] = 0u;  // single-digit moduli: no D2 (0.0f)
+        } else {
+          tmem_ld_cols<CW>(tbase + lane_off + kColD2 + col0, v2);
+        }
         tmem_wait_ld();
         // Accumulators copied: the next chunk's MMAs may start.
         tc_fence_before();
@@ -461,9 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kBN2 = kPairTileCols;              // pair tile N (224)
 constexpr int kBHalf = kBN2 / 2;                 // B rows per CTA
 constexpr int kBTile2 = kBHalf * kBKBytes;       // 7168 B
-constexpr int kStage2 = 3 * kATile + 3 * kBTile2;
-constexpr int kStages2 = 4;
-constexpr int kSmem2 = 1024 + kStages2 * kStage2 + 256;
+// A stage holds one 128-wide K block: the NL A limb tiles, then the NL B
+// limb tiles; the ring keeps 180 KB of them in flight for every NL (4
+// stages of three limbs, 6 of two, 12 of one).
+template <int NL>
+struct PairCfg {
+  static constexpr int kStage = NL * (kATile + kBTile2);
+  static constexpr int kStages = (180 * 1024) / kStage;
+  static constexpr int kSmem = 1024 + kStages * kStage + 256;
+};
+constexpr int kSmem2 = PairCfg<3>::kSmem;
+static_assert(PairCfg<1>::kSmem == kSmem2 && PairCfg<2>::kSmem == kSmem2, "one shared-memory size for every NL");
 constexpr int kTmemCols2 = 512;
 constexpr uint32_t kColD1p = 0, kColD2p = 224, kColSf2p = 448, kColSf26p = 464;
 constexpr int kPairCols = kBN2 / 2;              // accumulator columns per epilogue thread (two per lane quarter)
@@ -507,6 +524,8 @@ template <bool kInt, int NL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     limb_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const PairArgs args) {
+  constexpr int kStage2 = PairCfg<NL>::kStage;
+  constexpr int kStages2 = PairCfg<NL>::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2);
@@ -524,9 +543,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   // Three-limb moduli: D1 and D2 fill 448 of the 512 TMEM columns, one tile
   // at a time.  Two-limb moduli: one accumulator D = D1 + 169 D2 per tile
-  // (exact for K chunks of 4096), so two tiles' accumulators alternate and
-  // the MMAs of one round run while the epilogue drains the other.
-  constexpr int kBufs = NL == 2 ? 2 : 1;
+  // (exact for K chunks of 4096); single-digit moduli: one accumulator
+  // D = A0 B0.  Then two tiles' accumulators alternate and the MMAs of one
+  // round run while the epilogue drains the other.
+  constexpr int kBufs = NL <= 2 ? 2 : 1;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStages2; ++s) {
@@ -601,7 +621,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(st + j * kATile, &tmA, full_leader, (NL * kb + j) * kBKBytes, a_row);
 #pragma unroll
           for (int j = 0; j < NL; ++j)
-            tma_load_2d_pair(st + 3 * kATile + j * kBTile2, &tmB, full_leader, (NL * kb + j) * kBKBytes, b_row);
+            tma_load_2d_pair(st + NL * kATile + j * kBTile2, &tmB, full_leader, (NL * kb + j) * kBKBytes, b_row);
         }
       }
       if (!ok) settle_after_abort();
@@ -646,11 +666,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
               const uint64_t a1 = smem_desc_sw64(st + 1 * kATile + ks * 32);
               const uint64_t a2 = smem_desc_sw64(st + 2 * kATile + ks * 32);
-              const uint64_t b0 = smem_desc_sw64(st + 3 * kATile + 0 * kBTile2 + ks * 32);
-              const uint64_t b1 = smem_desc_sw64(st + 3 * kATile + 1 * kBTile2 + ks * 32);
-              const uint64_t b2 = smem_desc_sw64(st + 3 * kATile + 2 * kBTile2 + ks * 32);
+              const uint64_t b0 = smem_desc_sw64(st + NL * kATile + 0 * kBTile2 + ks * 32);
+              const uint64_t b1 = smem_desc_sw64(st + NL * kATile + 1 * kBTile2 + ks * 32);
+              const uint64_t b2 = smem_desc_sw64(st + NL * kATile + 2 * kBTile2 + ks * 32);
               const uint32_t acc = (kb == kc0 && ks == 0) ? 0u : 1u;
-              if constexpr (NL == 3) {
+              if constexpr (NL == 1) {
+                // Single-digit moduli: D = A0 B0, the residue product itself.
+                (void)a1; (void)a2; (void)b1; (void)b2;
+                mma_fp4_pair(dacc, a0, b0, idesc, s2, s2, acc);            // 1
+              } else if constexpr (NL == 3) {
                 mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
                 mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
                 mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)
@@ -710,8 +734,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        if constexpr (NL == 2) {
-          // One accumulator, |D| < 3600 * 4096 < 2^24: one reduction modulo m.
+        if constexpr (NL <= 2) {
+          // One accumulator (|D| < 3600 * 4096 < 2^24 for two-limb moduli,
+          // 64 * 2^18 for single-digit ones): one reduction modulo m.
           const uint32_t dcol = tbase + lane_off + static_cast<uint32_t>(buf * kBN2) + col0;
           uint32_t v1[kSlice], n1[kSlice];
           tmem_ld_cols<kSlice>(dcol, n1);
@@ -907,7 +932,10 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   a.n = c.n;
   a.kb_total = k_p / 128;
   // Two-limb moduli: one accumulator, exact for chunks of 4096 (32 blocks).
+  // Single-digit moduli (|digit| <= 8): |D| grows by at most 64 per K
+  // element, so chunks of 2^18 (2048 blocks) are exact.
   a.kc_blocks = (NL == 2 && c.kc_blocks > 32) ? 32 : c.kc_blocks;
+  if (NL == 1) a.kc_blocks = a.kb_total < 2048 ? a.kb_total : 2048;
   a.rows_a_p = rows_a_p;
   a.rows_b_p = rows_b_p;
   a.tiles_m2 = (c.m + 255) / 256;
@@ -977,6 +1005,10 @@ cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream) {
   if (call.limbs == 2) {  // two-limb moduli: residue products only
     if (!call.residue_mode) return cudaErrorInvalidValue;
     return use_pair(call) ? launch_pair<false, 2>(call, stream) : launch_mode<true, 2>(call, stream);
+  }
+  if (call.limbs == 1) {  // single-digit moduli: residue products only
+    if (!call.residue_mode) return cudaErrorInvalidValue;
+    return use_pair(call) ? launch_pair<false, 1>(call, stream) : launch_mode<true, 1>(call, stream);
   }
   if (call.limbs != 3) return cudaErrorInvalidValue;
   if (use_pair(call))

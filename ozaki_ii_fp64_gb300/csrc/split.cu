@@ -105,16 +105,29 @@ struct ResidueStep {
   float inv_up;
 };
 
-// Modulus l of the 3-limb (nl = 3) or two-limb (nl = 2) list.
+// Modulus l of the 3-limb (nl = 3), two-limb (nl = 2) or mixed-digit
+// (nl = 1) list.
+__host__ __device__ constexpr uint32_t table_modulus(int l, int nl) {
+  return nl == 1 ? kModulusTableMix[l] : (nl == 2 ? kModulusTable2[l] : kModulusTable[l]);
+}
+
+// Table rows 0 .. 10 (residues b < -117, which no modulus of the mixed-digit
+// list reaches) hold, in the mixed-digit launch, the single digit of each
+// residue modulo 11: row w for b = w - 5, the member of S congruent to b
+// mod 11 of smallest magnitude (b = +-5 -> -+6).  Every other single-digit
+// modulus takes the low base-13 digit of the shared rows, which is b itself
+// for |b| <= 4 and the class digit mod 13 (b = +-5, +-6 -> -+8, 6, -6) for 13.
+constexpr uint32_t kMod11Row = 0u;
+
 __host__ __device__ constexpr ResidueStep residue_step(int l, int nl) {
-  const uint32_t m = nl == 2 ? kModulusTable2[l] : kModulusTable[l], h = m >> 1;
+  const uint32_t m = table_modulus(l, nl), h = m >> 1;
   ResidueStep st{m, 0u, 0u, 0u, 0u, 0.0f};
   for (int i = 0; i < 4; ++i) {
     st.clo |= pow2_mod(8 * i, m) << (8 * i);
     st.chi |= pow2_mod(32 + 8 * i, m) << (8 * i);
   }
   st.bias = (h + m - pow2_mod(63, m)) % m;
-  st.row = 128u - h;  // table row of b = -h
+  st.row = (nl == 1 && m == 11u) ? kMod11Row : 128u - h;  // table row of b = -h
   int lg = 0;
   while ((1u << lg) < m) ++lg;
   const int e = 23 + lg;  // ceil(2^e / m) lies in [2^23, 2^24): exact in fp32
@@ -139,7 +152,20 @@ __host__ __device__ constexpr ResidueStep residue_step_biased(int l, int nl) {
    residue_step_biased(15, NL)}
 __constant__ ResidueStep kSteps3[kMaxModuli] = OZEMU_STEPS(3);
 __constant__ ResidueStep kSteps2[kMaxModuli] = OZEMU_STEPS(2);
+__constant__ ResidueStep kSteps1[kMaxModuliMix] = {
+    residue_step_biased(0, 1),  residue_step_biased(1, 1),  residue_step_biased(2, 1),  residue_step_biased(3, 1),
+    residue_step_biased(4, 1),  residue_step_biased(5, 1),  residue_step_biased(6, 1),  residue_step_biased(7, 1),
+    residue_step_biased(8, 1),  residue_step_biased(9, 1),  residue_step_biased(10, 1), residue_step_biased(11, 1),
+    residue_step_biased(12, 1), residue_step_biased(13, 1), residue_step_biased(14, 1), residue_step_biased(15, 1),
+    residue_step_biased(16, 1), residue_step_biased(17, 1), residue_step_biased(18, 1), residue_step_biased(19, 1)};
 #undef OZEMU_STEPS
+
+// Digits per modulus: NL for the 3- and two-limb lists; in the mixed-digit
+// list (NL = 1) one for the first kMixSingle moduli and two for the rest.
+template <int L, int NL>
+__host__ __device__ constexpr int digits_of() {
+  return NL == 1 ? (L < kMixSingle ? 1 : 2) : NL;
+}
 
 // Byte offset of this lane's table word for the balanced residue of A'
 // modulo modulus L, relative to the table row of b = -h.  A table row is 128
@@ -152,7 +178,7 @@ __constant__ ResidueStep kSteps2[kMaxModuli] = OZEMU_STEPS(2);
 template <int L, int NL>
 __device__ __forceinline__ uint32_t residue_offset(uint32_t ulo, uint32_t uhi, uint32_t lane_hi) {
   constexpr ResidueStep st = residue_step(L, NL);
-  const ResidueStep& ks = NL == 2 ? kSteps2[L] : kSteps3[L];
+  const ResidueStep& ks = NL == 1 ? kSteps1[L] : (NL == 2 ? kSteps2[L] : kSteps3[L]);
   uint32_t w;
   if constexpr (st.m == 256u) {
     w = (ulo & 0xFFu) ^ 0x80u;  // 2^63 = 0 (mod 256): b is the low byte of A', signed
@@ -171,10 +197,14 @@ __device__ __forceinline__ uint32_t residue_offset(uint32_t ulo, uint32_t uhi, u
 }
 
 // Codes of 8 elements for modulus L, packed and stored.  Lane i reads bank i
-// only, so a warp's lookups never conflict.
+// only, so a warp's lookups never conflict.  o / modulus_words: this row's
+// word of modulus 0 and the stride between moduli; in the mixed-digit list
+// the single-digit moduli use (o, modulus_words) and the two-digit ones
+// (o2, modulus_words2), counted from the first two-digit modulus.
 template <int L, bool kRes8, int NL>
 __device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const uint32_t (&uhi)[8], const char* tb,
-                                              uint32_t lane_hi, uint32_t* o, long long modulus_words) {
+                                              uint32_t lane_hi, uint32_t* o, long long modulus_words, uint32_t* o2,
+                                              long long modulus_words2) {
   constexpr uint32_t kRow0 = residue_step(L, NL).row * kTableRowBytes;
   const char* t0 = tb + kRow0;
   uint32_t c[8];
@@ -191,26 +221,31 @@ __device__ __forceinline__ void modulus_codes(const uint32_t (&ulo)[8], const ui
     uint32_t w0, w1, w2;
     pack8(c, w0, w1, w2);
     // Limb j of a 128-element K block sits 64 j bytes after limb 0 (two-limb
-    // moduli: the third limb is 0 and not stored).
-    uint32_t* p = o + L * modulus_words;
+    // moduli: the third limb is 0 and not stored; single-digit moduli store
+    // the low digit only).
+    constexpr int D = digits_of<L, NL>();
+    uint32_t* p = (NL == 1 && L >= kMixSingle) ? o2 + (L - kMixSingle) * modulus_words2 : o + L * modulus_words;
     __stcs(p, w0);
-    __stcs(p + 16, w1);
-    if constexpr (NL == 3) __stcs(p + 32, w2);
+    if constexpr (D >= 2) __stcs(p + 16, w1);
+    if constexpr (D == 3) __stcs(p + 32, w2);
   }
 }
 
 template <bool kRes8, int NL, int... Ls>
 __device__ __forceinline__ void all_moduli(std::integer_sequence<int, Ls...>, const uint32_t (&ulo)[8],
                                            const uint32_t (&uhi)[8], const char* tb, uint32_t lane_hi, uint32_t* o,
-                                           long long modulus_words) {
-  (modulus_codes<Ls, kRes8, NL>(ulo, uhi, tb, lane_hi, o, modulus_words), ...);
+                                           long long modulus_words, uint32_t* o2, long long modulus_words2) {
+  (modulus_codes<Ls, kRes8, NL>(ulo, uhi, tb, lane_hi, o, modulus_words, o2, modulus_words2), ...);
 }
 
 // Pass 2 of the row split over the row's elements: integers, residues and
-// limb codes (or residue bytes), packed and stored.
+// limb codes (or residue bytes), packed and stored.  out_row2 /
+// modulus_words2: the row of the first two-digit modulus and the stride
+// between two-digit moduli (mixed-digit list only).
 template <int R, bool kRes8, int NL, bool kFast>
 __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, int vec_ok, int s, const char* tb,
-                                            uint32_t lane_hi, uint8_t* out_row, long long modulus_words) {
+                                            uint32_t lane_hi, uint8_t* out_row, long long modulus_words,
+                                            uint8_t* out_row2, long long modulus_words2) {
   // Backwards over the row: pass 1 read it forwards, so the most recently
   // read part (the likeliest still in L2) comes first.
   const int kfirst = threadIdx.x * kElemsPerThread;
@@ -226,8 +261,12 @@ __device__ __forceinline__ void split_pass2(const double* rowp, int k, int k_p, 
       ulo[e] = static_cast<uint32_t>(u);
       uhi[e] = static_cast<uint32_t>(u >> 32);
     }
-    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : (k0 >> 7) * (64 * NL) + (k0 & 127) / 2));
-    all_moduli<kRes8, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_words);
+    // Single-digit rows (mixed list) hold one 64-byte digit run per K block.
+    constexpr int kRun = NL == 1 ? 64 : 64 * NL;
+    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + (kRes8 ? k0 : (k0 >> 7) * kRun + (k0 & 127) / 2));
+    uint32_t* o2 = NL == 1 ? reinterpret_cast<uint32_t*>(out_row2 + (k0 >> 7) * 128 + (k0 & 127) / 2) : nullptr;
+    all_moduli<kRes8, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_words, o2,
+                          modulus_words2);
   }
 }
 
@@ -283,9 +322,18 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   return m;
 }
 
+// Single digit of a balanced residue b modulo 11 (|b| <= 5): b itself, or
+// -+6 for b = +-5 (the members of S congruent to b mod 11).
+__device__ uint32_t mod11_code(int b) {
+  const int d = b == 5 ? -6 : (b == -5 ? 6 : b);
+  return e2m1_nibble(d);
+}
+
 // kRes8 = false: FP4 limb planes [r][3][rows_p][k_p/2] (the FP4 path).
 // kRes8 = true: the balanced residues themselves as int8 [r][rows_p][k_p]
-// (input of the INT8 comparison GEMM).
+// (input of the INT8 comparison GEMM).  NL = 1: the mixed-digit list, whose
+// single-digit moduli come first ([l][rows_p][k_p/2] each) and whose
+// two-digit moduli follow ([l][rows_p][k_p] each, the two-limb layout).
 template <int R, bool kRes8, int NL>
 __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     split_rows_f64_kernel(const double* __restrict__ X, long long ldx, int rows, int k, int rows_p, int k_p, int p,
@@ -295,8 +343,12 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
   extern __shared__ __align__(16) uint32_t tbl[];
   __shared__ uint32_t red[kSplitThreads / 32];
   uint32_t* stage = tbl + kTableWords;
-  for (int i = threadIdx.x; i < 256; i += kSplitThreads)
-    stage[i] = kRes8 ? static_cast<uint32_t>(static_cast<uint8_t>(i - 128)) : limb_code(i - 128);
+  for (int i = threadIdx.x; i < 256; i += kSplitThreads) {
+    uint32_t code = kRes8 ? static_cast<uint32_t>(static_cast<uint8_t>(i - 128)) : limb_code(i - 128);
+    if (NL == 1 && i >= static_cast<int>(kMod11Row) && i < static_cast<int>(kMod11Row) + 11)
+      code = mod11_code(i - static_cast<int>(kMod11Row) - 5);
+    stage[i] = code;
+  }
   __syncthreads();
   for (int w = threadIdx.x; w < kTableWords; w += kSplitThreads)
     tbl[w] = stage[w >> (kTableRowShift - 2)];
@@ -305,19 +357,27 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
   const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);  // (4 lane) << 25
 
   // FP4 planes: a row holds the three limbs of each 128-element K block
-  // side by side (3 x 64 bytes); moduli follow one another.
+  // side by side (3 x 64 bytes); moduli follow one another.  Mixed-digit
+  // list: single-digit rows of k_p/2 bytes, then two-digit rows of k_p.
   const long long row_bytes = kRes8 ? k_p : static_cast<long long>(NL) * k_p / 2;
   const long long modulus_stride = static_cast<long long>(rows_p) * row_bytes;
+  constexpr int kSingle = NL == 1 ? (R < kMixSingle ? R : kMixSingle) : 0;  // mixed: single-digit moduli
+  const long long row_bytes2 = k_p;
+  const long long modulus_stride2 = static_cast<long long>(rows_p) * row_bytes2;
+  uint8_t* planes2 = planes + kSingle * modulus_stride;  // first two-digit modulus (mixed list)
   const int vec_ok = row_vector_width(X, ldx);
 
   for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
     uint8_t* out_row = planes + static_cast<long long>(row) * row_bytes;
+    uint8_t* out_row2 = planes2 + static_cast<long long>(row) * row_bytes2;
     if (row >= rows) {  // padding row: digit (or residue) 0 everywhere
-      for (int l = 0; l < R; ++l)
-        {
-          uint32_t* o = reinterpret_cast<uint32_t*>(out_row + l * modulus_stride);
-          for (int w = threadIdx.x; w < row_bytes / 4; w += kSplitThreads) o[w] = 0u;
-        }
+      for (int l = 0; l < R; ++l) {
+        const bool two = NL == 1 && l >= kSingle;
+        uint32_t* o = reinterpret_cast<uint32_t*>(two ? out_row2 + (l - kSingle) * modulus_stride2
+                                                      : out_row + l * modulus_stride);
+        const long long words = (two ? row_bytes2 : row_bytes) / 4;
+        for (int w = threadIdx.x; w < words; w += kSplitThreads) o[w] = 0u;
+      }
       continue;
     }
     const double* rowp = X + static_cast<long long>(row) * ldx;
@@ -354,9 +414,11 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitBlocksPerSM)
     // Pass 2: integers, residues, limbs.  Rows whose largest magnitude is
     // normal (with p <= 52) take the right-shift rounding.
     if (mh >= 0x00100000u && p <= 52)
-      split_pass2<R, kRes8, NL, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
+      split_pass2<R, kRes8, NL, true>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4, out_row2,
+                                      modulus_stride2 / 4);
     else
-      split_pass2<R, kRes8, NL, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4);
+      split_pass2<R, kRes8, NL, false>(rowp, k, k_p, vec_ok, s, tb, lane_hi, out_row, modulus_stride / 4, out_row2,
+                                       modulus_stride2 / 4);
   }
 }
 
@@ -503,6 +565,24 @@ cudaError_t launch_split_limbs(const double* X, long long ldx, int rows, int k, 
 template <bool kRes8>
 cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, int p, const SplitModuli& mods,
                               uint8_t* planes, int32_t* shifts, uint32_t* flags, cudaStream_t stream) {
+  if (mods.limbs == 1) {  // the mixed-digit list (FP4 planes only), r up to kMaxModuliMix
+    if constexpr (kRes8) {
+      return cudaErrorInvalidValue;
+    } else {
+      switch (mods.r) {
+#define OZEMU_SPLIT_MIX(R) \
+  case R:                  \
+    return launch_split_r<R, false, 1>(X, ldx, rows, k, p, planes, shifts, flags, stream);
+        OZEMU_SPLIT_MIX(1) OZEMU_SPLIT_MIX(2) OZEMU_SPLIT_MIX(3) OZEMU_SPLIT_MIX(4) OZEMU_SPLIT_MIX(5)
+        OZEMU_SPLIT_MIX(6) OZEMU_SPLIT_MIX(7) OZEMU_SPLIT_MIX(8) OZEMU_SPLIT_MIX(9) OZEMU_SPLIT_MIX(10)
+        OZEMU_SPLIT_MIX(11) OZEMU_SPLIT_MIX(12) OZEMU_SPLIT_MIX(13) OZEMU_SPLIT_MIX(14) OZEMU_SPLIT_MIX(15)
+        OZEMU_SPLIT_MIX(16) OZEMU_SPLIT_MIX(17) OZEMU_SPLIT_MIX(18) OZEMU_SPLIT_MIX(19) OZEMU_SPLIT_MIX(20)
+#undef OZEMU_SPLIT_MIX
+        default:
+          return cudaErrorInvalidValue;
+      }
+    }
+  }
   switch (mods.r) {
 #define OZEMU_SPLIT_CASE(R) \
   case R:                   \

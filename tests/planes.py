@@ -33,3 +33,24 @@ def limb_value(digits):
     if digits.shape[1] > 2:
         v = v + 169 * digits[:, 2]
     return v
+
+
+def decode_planes_mixed(planes, rows, k, r, single=6):
+    """Mixed-digit plane bytes -> digits (r, 2, rows_p, k_p): single-digit
+    moduli first ([rows_p][k_p/2] each, second digit reported as 0), then
+    two-digit moduli ([rows_p][k_p] each, the two-limb layout)."""
+    rows_p = (rows + 127) // 128 * 128
+    k_p = (k + 127) // 128 * 128
+    ns = min(r, single)
+    plane = rows_p * k_p // 2
+    b = np.asarray(planes, dtype=np.uint8)
+    d1, c1 = decode_planes(b[:ns * plane], rows, k, ns, limbs=1)
+    digits = np.zeros((r, 2, rows_p, k_p), dtype=np.int64)
+    codes = np.zeros((r, 2, rows_p, k_p), dtype=np.uint8)
+    digits[:ns, :1] = d1
+    codes[:ns, :1] = c1
+    if r > ns:
+        d2, c2 = decode_planes(b[ns * plane:], rows, k, r - ns, limbs=2)
+        digits[ns:] = d2
+        codes[ns:] = c2
+    return digits, codes

@@ -69,7 +69,8 @@ def test_layout_sizes(oz):
     assert oz.ozemu_plane_bytes(129, 300, 13) == 3 * 13 * 256 * 192
     assert oz.ozemu_residue_bytes(5, 17, 2) == 2 * 5 * 32
     assert oz.ozemu_plane_bytes(-1, 1, 1) == 0
-    assert oz.ozemu_residue_bytes(1, 1, 17) == 0
+    assert oz.ozemu_residue_bytes(1, 1, 20) == 20 * 16  # r up to 20: the mixed-digit list
+    assert oz.ozemu_residue_bytes(1, 1, 21) == 0
 
 
 def test_two_limb_moduli_match_oracle(oz):
@@ -86,6 +87,31 @@ def test_two_limb_bit_budget_matches_oracle(oz, k, r):
             oz.ozemu_bit_budget_2limb(k, r)
         return
     assert oz.ozemu_bit_budget_2limb(k, r) == (pa, pb)
+
+
+def test_mixed_moduli_products_and_budget_match_oracle(oz):
+    assert oz.ozemu_max_moduli_mixed() == 20 and oz.ozemu_single_digit_moduli_mixed() == 6
+    assert oz.ozemu_moduli_mixed(20) == oracle.moduli(20, oracle.MIXED)
+    for r in range(1, 21):
+        assert oz.ozemu_products_mixed(r) == sum(oracle.products_per_modulus(l, oracle.MIXED) for l in range(r))
+    assert oz.ozemu_products_mixed(0) == oz.OZEMU_ERR_INVALID_ARG
+    for k in (1, 2, 300, 8192, 65536, 131071):
+        for r in (1, 4, 6, 7, 13, 19, 20):
+            try:
+                _, pa, pb = oracle.bit_budget(k, r, oracle.MIXED)
+            except ValueError:
+                with pytest.raises(oz.OzemuError):
+                    oz.ozemu_bit_budget_mixed(k, r)
+                continue
+            assert oz.ozemu_bit_budget_mixed(k, r) == (pa, pb)
+
+
+def test_mixed_layout_sizes(oz):
+    # single-digit moduli: one plane each; two-digit moduli: two
+    assert oz.ozemu_plane_bytes_mixed(1, 1, 1) == 128 * 64
+    assert oz.ozemu_plane_bytes_mixed(129, 300, 6) == 6 * 256 * 192
+    assert oz.ozemu_plane_bytes_mixed(129, 300, 19) == (6 + 2 * 13) * 256 * 192
+    assert oz.ozemu_plane_bytes_mixed(1, 1, 21) == 0
 
 
 def test_two_limb_layout_sizes(oz):

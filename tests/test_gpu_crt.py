@@ -54,10 +54,18 @@ def chosen_integers(M, count, rng):
     return vals
 
 
-@pytest.mark.parametrize("r", [1, 2, 3, 5, 8, 11, 12, 13, 14, 16])
-def test_crt_stage_matches_oracle(oz, r):
-    rng = random.Random(1000 + r)
-    mods = oracle.moduli(r)
+@pytest.mark.parametrize("r,family", [(1, "three"), (2, "three"), (3, "three"), (5, "three"), (8, "three"),
+                                      (11, "three"), (12, "three"), (13, "three"), (14, "three"), (16, "three"),
+                                      (2, "two"), (3, "two"), (9, "two"), (16, "two"),
+                                      (1, "mixed"), (2, "mixed"), (5, "mixed"), (6, "mixed"), (7, "mixed"),
+                                      (13, "mixed"), (17, "mixed"), (19, "mixed"), (20, "mixed")])
+def test_crt_stage_matches_oracle(oz, r, family):
+    # The two-limb list has its even modulus (112) second, the others first:
+    # near +-M/2 the mixed-radix fallback must still return C' itself.
+    rng = random.Random(1000 + r + {"three": 0, "two": 50, "mixed": 100}[family])
+    ceil = {"three": oracle.MODULUS_CEILING, "two": oracle.MODULUS_CEILING_2LIMB, "mixed": oracle.MIXED}[family]
+    crt = {"three": oz.crt_f64, "two": oz.crt_f64_2limb, "mixed": oz.crt_f64_mixed}[family]
+    mods = oracle.moduli(r, ceil)
     M = 1
     for mm in mods:
         M *= mm
@@ -73,8 +81,7 @@ def test_crt_stage_matches_oracle(oz, r):
     sb = np.array([rng.randrange(-40, 40) for _ in range(n)], dtype=np.int32)
     sa[:8] = bits - 60  # ordinary results for the first rows
     expect = oracle.scale_back_array(Cp, sa, sb)
-    C = oz.crt_f64(m, n, r, torch.from_numpy(res).to(DEV), torch.from_numpy(sa).to(DEV),
-                   torch.from_numpy(sb).to(DEV))
+    C = crt(m, n, r, torch.from_numpy(res).to(DEV), torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV))
     assert oz.get_status() == oz.OZEMU_OK
     got = C.cpu().numpy()
     bad = np.argwhere(got.view(np.int64) != expect.view(np.int64))
