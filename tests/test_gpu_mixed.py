@@ -173,9 +173,11 @@ def test_dgemm_mixed_shapes(oz, m, n, k, r, dist):
         assert oracle.error_bound_ratio(A, B, C) <= 1.0
 
 
-@pytest.mark.parametrize("m,n,k,r", [(20, 30, 40, 1), (33, 70, 100, 2), (65, 17, 300, 3), (40, 90, 500, 5),
+@pytest.mark.parametrize("m,n,k,r", [(20, 30, 3, 1), (33, 70, 40, 2), (65, 17, 300, 3), (40, 90, 500, 5),
                                      (130, 80, 1000, 6), (50, 66, 700, 7), (70, 70, 200, 11)])
 def test_dgemm_mixed_few_moduli(oz, m, n, k, r):
+    # Few moduli leave few bits (r = 1: M = 8, so k <= 3); the CRT's word
+    # counts change with the bit length of M: every instance against the oracle.
     A, B = make_pair(m, n, k, seed=m + n + k + r + 1, dist="normal")
     check_dgemm(oz, A, B, r)
 
