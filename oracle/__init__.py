@@ -22,7 +22,8 @@ with no independent pin say "parity unpinned".
 """
 
 from .ozaki2 import (  # noqa: F401
-    S, BASE, LIMB_WEIGHTS, N_LIMBS, MODULUS_CEILING, MODULUS_CEILING_2LIMB, MIXED,
+    S, BASE, LIMB_WEIGHTS, N_LIMBS, MODULUS_CEILING, MODULUS_CEILING_2LIMB, MODULUS_CEILING_WIDE, MIXED,
+    accumulator_growth,
     single_digit_moduli, single_digit_set, single_digit, digits_of_modulus, products_per_modulus,
     moduli, modulus_product, bit_budget, frexp_exponent, row_shifts,
     scale_round_scalar, scale_round, balanced_residue, balanced_residue_array,

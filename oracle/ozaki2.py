@@ -57,6 +57,12 @@ MODULUS_CEILING = 256
 MODULUS_CEILING_2LIMB = 113
 
 
+# Wide-moduli reading (a derived variant; [AWE] abstract: base-13 limbs in S
+# with weights (1, 13, 169)): with the top limb allowed anywhere in S (up to
+# +-12), three limbs reach every integer of [-732, 732] (pinned), so moduli up
+# to 1465 fit three limbs: about 10.5 bits per 9 products instead of 8.
+MODULUS_CEILING_WIDE = 1465
+
 # Mixed-digit reading ([AWE] abstract: the formulation holds modulo m, and the
 # encodings may differ per input range).  A modulus m whose every residue
 # class holds a member of S needs ONE digit per residue, so its residue
@@ -271,13 +277,15 @@ def limb_table_int8():
     return np.array([limb_split(v) for v in range(-128, 128)], dtype=np.int64)
 
 
-def limb_digits(X):
-    """Limb digits of an int array with values in [-128, 127]: shape (3, ...)."""
+def limb_digits(X, lo=-128, hi=127):
+    """Limb digits of an int array with values in [lo, hi] (int8 range by
+    default; [-732, 732] for the wide moduli): shape (3, ...)."""
     X = np.asarray(X, dtype=np.int64)
-    if X.size and (X.min() < -128 or X.max() > 127):
-        raise ValueError("limb_digits expects int8-range values")
-    tab = limb_table_int8()
-    d = tab[X + 128]  # (..., 3)
+    if X.size and (X.min() < lo or X.max() > hi):
+        raise ValueError("limb_digits expects values in [%d, %d]" % (lo, hi))
+    tab = limb_table_int8() if (lo, hi) == (-128, 127) else \
+        np.array([limb_split(v) for v in range(lo, hi + 1)], dtype=np.int64)
+    d = tab[X - lo]  # (..., 3)
     return np.moveaxis(d, -1, 0)
 
 
@@ -416,6 +424,8 @@ def digits_of_modulus(res, m, l, ceiling=MODULUS_CEILING):
         table = np.array([single_digit(x, m) for x in range(-h, m - h)], dtype=np.int64)
         d = table[np.asarray(res, dtype=np.int64) + h]
         return np.stack([d, np.zeros_like(d), np.zeros_like(d)])
+    if ceiling == MODULUS_CEILING_WIDE:
+        return limb_digits(res, -732, 732)
     return limb_digits(res)
 
 
@@ -424,7 +434,29 @@ def products_per_modulus(l, ceiling=MODULUS_CEILING):
     1 (a single-digit modulus of the mixed list)."""
     if ceiling == MIXED:
         return 1 if l < len(single_digit_set()) else 4
-    return 4 if ceiling == MODULUS_CEILING_2LIMB else 9
+    return 4 if ceiling == MODULUS_CEILING_2LIMB else 9  # three limbs: 256 and the wide 1465
+
+
+def accumulator_growth(ceiling=MODULUS_CEILING, single_accumulator=False):
+    """Largest |increment| one K element adds to the FP32 accumulators of the
+    limb GEMM for residues of the given moduli list (brute force over every
+    pair of digit triples the split produces): with two accumulators
+    D1 = A0B0 + 13 (A0B1 + A1B0) and D2 = the rest (weights 1, 13, 169), or
+    one accumulator D = sum 13^(i+j) A_i B_j.  Returns (growth of D1, growth
+    of D2) or the single growth; an exact chunk holds (2^24 - 1) // growth
+    K elements."""
+    lo, hi = {MODULUS_CEILING: (-128, 127), MODULUS_CEILING_2LIMB: (-56, 56),
+              MODULUS_CEILING_WIDE: (-732, 732)}[ceiling]  # the balanced residues of each list
+    trip = np.array([limb_split(v) for v in range(lo, hi + 1)], dtype=np.int64)
+    g1 = g2 = gs = 0
+    for a in trip:
+        d1 = np.abs(a[0] * trip[:, 0] + 13 * (a[0] * trip[:, 1] + a[1] * trip[:, 0]))
+        d2 = np.abs(a[0] * trip[:, 2] + a[1] * trip[:, 1] + a[2] * trip[:, 0]
+                    + 13 * (a[1] * trip[:, 2] + a[2] * trip[:, 1]) + 169 * a[2] * trip[:, 2])
+        g1, g2 = max(g1, int(d1.max())), max(g2, int(d2.max()))
+        full = np.abs(sum(13 ** (i + j) * a[i] * trip[:, j] for i in range(3) for j in range(3)))
+        gs = max(gs, int(full.max()))
+    return gs if single_accumulator else (g1, g2)
 
 
 def deconstruct(X, p, r, ceiling=MODULUS_CEILING):
