@@ -72,6 +72,9 @@ def parse():
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--chunks", type=int, default=4,
                     help="row chunks of A in the timed step (1: the stages one after another)")
+    ap.add_argument("--schedule", default="pipelined", choices=["pipelined", "phased"],
+                    help="pipelined: each chunk's CRT beside the next chunk's GEMM, chunk splits beside the "
+                         "GEMMs; phased: all splits (A beside B), then the GEMMs, then the CRTs")
     return ap.parse_args()
 
 
@@ -557,6 +560,20 @@ def run_gpu(args):
             check(fam.split_rows(mc, k, A.data_ptr() + row0 * k * 8, k, pA, r, apc.data_ptr(), sac.data_ptr(),
                                  s_split.cuda_stream), "split A chunk")
             evA[c].record(s_split)
+        if args.schedule == "phased":
+            # Splits of A beside B's, then the GEMMs back to back, then the CRTs.
+            stream.wait_event(evA[nch - 1])
+            for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
+                if gev is not None:
+                    gev[c][0].record(stream)
+                check(fam.residue_gemm(mc, n, k, r, apc.data_ptr(), bp.data_ptr(), resc.data_ptr(), sh),
+                      "digit gemm chunk")
+                if gev is not None:
+                    gev[c][1].record(stream)
+            for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
+                check(fam.crt(mc, n, r, resc.data_ptr(), sac.data_ptr(), sb.data_ptr(), C.data_ptr() + row0 * n * 8,
+                              n, sh), "crt chunk")
+            return
         for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
             stream.wait_event(evA[c])
             if gev is not None:
@@ -662,6 +679,7 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": bench_config(args, spec, r, n_prod, pA + pB),
             "schedule": {"path": "narrow (fused)" if narrow else "digit planes", "row_chunks": nch,
+                         "order": args.schedule,
                          "three_limb_r": spec["r"], "three_limb_bit_budget": P3},
             "pct_fp4_roofline" if not narrow else "pct_io_roofline": round(pct_roof, 2), "roofline": roofline,
             "stage_ms": {kk: round(v, 3) for kk, v in stage_ms.items()},

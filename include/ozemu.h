@@ -154,7 +154,9 @@ int ozemu_split_rows_f64(int rows, int k, const double* X, int ldx, int p, int r
                          uint8_t* planes, int32_t* shifts, cudaStream_t stream);
 
 /* Same for the columns of X (k x cols, row-major, ldx >= cols): column j
- * becomes plane row j.  Uses the cached workspace for a transposed copy. */
+ * becomes plane row j.  Two passes over X, no transposed copy: the column
+ * maxima (the cached workspace holds them, 8 bytes per column), then the
+ * split of 128-row x 64-column blocks staged in shared memory. */
 int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r,
                          uint8_t* planes, int32_t* shifts, cudaStream_t stream);
 
@@ -294,7 +296,7 @@ int ozemu_probe_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
  * process exits.  The problem must fit: with rows_p(x) = round_up(x, 128),
  * k_p = round_up(k, 128) and 256-byte alignment of each part,
  *   3 r (rows_p(m) + rows_p(n)) k_p / 2 + 4 (m + n) + r m round_up(n, 16)
- *   + 8 k n + 256  <=  64 MiB,
+ *   + 8 n + 256  <=  64 MiB,
  * otherwise the call returns OZEMU_ERR_SCRATCH_TOO_SMALL before enqueueing
  * anything (for example m = n = k = 1024 with r = 13 fits; 2048^3 does not).
  * The first call on a device looks up the array's device address (once per

@@ -298,14 +298,16 @@ int split_rows_f64(int rows, int k, const double* X, long long ldx, int p, int r
       launch_split_rows_f64(X, ldx, rows, k, p, split_moduli(r, limbs), planes, shifts, d->flags, st));
 }
 
+// Columns of X (k x cols) into limb planes, without a transposed copy:
+// scratch holds the cols column maxima (8 bytes each).
 int split_cols_f64(int k, int cols, const double* X, long long ldx, int p, int r, uint8_t* planes,
-                   int32_t* shifts, double* scratch, DeviceState* d, cudaStream_t st, int limbs = 3) {
-  if (k > 0) {
-    cudaError_t e = launch_transpose_f64(X, ldx, k, cols, scratch, k, st);
-    if (e != cudaSuccess) return OZEMU_ERR_CUDA;
-  }
-  return split_rows_f64(cols, k, scratch, k > 0 ? k : 1, p, r, planes, shifts, d, st, limbs);
+                   int32_t* shifts, void* scratch, DeviceState* d, cudaStream_t st, int limbs = 3) {
+  return cuda_status(launch_split_cols_f64(X, ldx, k, cols, p, split_moduli(r, limbs), planes, shifts,
+                                           static_cast<unsigned long long*>(scratch), d->flags, st));
 }
+
+// Bytes of the column-maximum scratch of a column split of `cols` columns.
+size_t colmax_bytes(int cols) { return align256(static_cast<size_t>(cols > 0 ? cols : 1) * 8); }
 
 int residue_gemm(int m, int n, int k, int r, const uint8_t* ap, const uint8_t* bp, uint8_t* res, DeviceState* d,
                  cudaStream_t st, int limbs = 3) {
@@ -465,7 +467,7 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   const size_t szA = from_host ? align256(static_cast<size_t>(m) * k * 8) : 0;
   const size_t szB = from_host ? align256(static_cast<size_t>(k) * n * 8) : 0;
   const size_t szC = from_host ? align256(static_cast<size_t>(m) * n * 8) : 0;
-  const size_t szBt = align256(static_cast<size_t>(k) * bcols * 8);
+  const size_t szBt = colmax_bytes(bcols);
   const size_t szBp = align256(plane_bytes(bcols, k, r, limbs)), szSb = align256(static_cast<size_t>(bcols) * 4);
   const size_t szAp = align256(plane_bytes(chunk, k, r, limbs)), szSa = align256(static_cast<size_t>(chunk) * 4);
   const size_t szRes = align256(ozemu_residue_bytes(chunk, bcols, r));
@@ -477,7 +479,7 @@ int dgemm_chunked(int m, int n, int k, const double* A, int lda, const double* B
   const double* Bd = from_host ? reinterpret_cast<const double*>(buf + szA) : B;
   double* Cd = from_host ? reinterpret_cast<double*>(buf + szA + szB) : C;
   const long long ldad = from_host ? k : lda, ldbd = from_host ? n : ldb, ldcd = from_host ? n : ldc;
-  double* Bt = reinterpret_cast<double*>(buf + szA + szB + szC);
+  void* Bt = buf + szA + szB + szC;  // column maxima of B's split
   uint8_t* per_bblock = buf + szA + szB + szC + szBt;           // [nbc] planes + shifts of B's column blocks
   uint8_t* per_chunk = per_bblock + nbc * (szBp + szSb);       // [nch] planes + shifts of A's rows, residues
   cudaStream_t cs = d->copy_stream, xs = d->crt_stream;
@@ -715,9 +717,9 @@ static int split_cols_entry(int k, int cols, const double* X, int ldx, int p, in
   int s = device_state(&d);
   if (s != OZEMU_OK) return s;
   uint8_t* ws = nullptr;
-  s = workspace(d, align256(static_cast<size_t>(k > 0 ? k : 1) * cols * sizeof(double)), &ws);
+  s = workspace(d, colmax_bytes(cols), &ws);
   if (s != OZEMU_OK) return s;
-  return split_cols_f64(k, cols, X, ldx, p, r, planes, shifts, reinterpret_cast<double*>(ws), d, stream, limbs);
+  return split_cols_f64(k, cols, X, ldx, p, r, planes, shifts, ws, d, stream, limbs);
 }
 
 int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r, uint8_t* planes,
@@ -913,7 +915,7 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   const size_t pa = align256(plane_bytes(m, k, r)), pb = align256(plane_bytes(n, k, r));
   const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
   const size_t rb = align256(ozemu_residue_bytes(m, n, r));
-  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  const size_t bt = colmax_bytes(n);  // column maxima of B
   uint8_t* ws = nullptr;
   s = workspace(d, pa + pb + sa + sb + rb + bt, &ws);
   if (s != OZEMU_OK) return s;
@@ -922,7 +924,7 @@ int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, 
   int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
   int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
   uint8_t* res = bp + pb + sa + sb;
-  double* btr = reinterpret_cast<double*>(res + rb);
+  void* btr = res + rb;
   s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, d, stream);
   if (s != OZEMU_OK) return s;
   s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, d, stream);
@@ -997,7 +999,7 @@ static int family_dgemm(int m, int n, int k, const double* A, int lda, const dou
   const size_t pa = align256(plane_bytes(m, k, r, limbs)), pb = align256(plane_bytes(n, k, r, limbs));
   const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
   const size_t rb = align256(ozemu_residue_bytes(m, n, r));
-  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  const size_t bt = colmax_bytes(n);  // column maxima of B
   uint8_t* ws = nullptr;
   s = workspace(d, pa + pb + sa + sb + rb + bt, &ws);
   if (s != OZEMU_OK) return s;
@@ -1006,7 +1008,7 @@ static int family_dgemm(int m, int n, int k, const double* A, int lda, const dou
   int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
   int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
   uint8_t* res = bp + pb + sa + sb;
-  double* btr = reinterpret_cast<double*>(res + rb);
+  void* btr = res + rb;
   s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, d, stream, limbs);
   if (s != OZEMU_OK) return s;
   s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, d, stream, limbs);
@@ -1197,7 +1199,7 @@ int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const dou
   const size_t pa = align256(plane_bytes(m, k, r)), pb = align256(plane_bytes(n, k, r));
   const size_t sa = align256(static_cast<size_t>(m) * 4), sb = align256(static_cast<size_t>(n) * 4);
   const size_t rb = align256(ozemu_residue_bytes(m, n, r));
-  const size_t bt = align256(static_cast<size_t>(k) * n * sizeof(double));
+  const size_t bt = colmax_bytes(n);  // column maxima of B
   if (k > 0 && fl + pa + pb + sa + sb + rb + bt > kNoAllocBytes) return OZEMU_ERR_SCRATCH_TOO_SMALL;
   uint8_t* base = nullptr;
   int s = noalloc_scratch(&base);
@@ -1213,7 +1215,7 @@ int ozemu_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const dou
   int32_t* sap = reinterpret_cast<int32_t*>(bp + pb);
   int32_t* sbp = reinterpret_cast<int32_t*>(bp + pb + sa);
   uint8_t* res = bp + pb + sa + sb;
-  double* btr = reinterpret_cast<double*>(res + rb);
+  void* btr = res + rb;
   s = split_rows_f64(m, k, A, lda, pa_bits, r, ap, sap, &d, stream);
   if (s != OZEMU_OK) return s;
   s = split_cols_f64(k, n, B, ldb, pb_bits, r, bp, sbp, btr, &d, stream);

@@ -470,12 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kBN2 = kPairTileCols;              // pair tile N (224)
 constexpr int kBHalf = kBN2 / 2;                 // B rows per CTA
 constexpr int kBTile2 = kBHalf * kBKBytes;       // 7168 B
-// A stage holds one 128-wide K block: the NL A limb tiles, then the NL B
-// limb tiles; the ring keeps 180 KB of them in flight for every NL (4
-// stages of three limbs, 6 of two, 12 of one).
+// A stage holds kKpS 128-wide K blocks: the NL A limb tiles of each, then
+// the NL B limb tiles of each; the ring keeps 180 KB of them in flight for
+// every NL (4 stages of three limbs, 6 of two, 3 of four single-digit K
+// blocks).  Single-digit moduli take 4 K blocks per stage so that each stage
+// barrier serves 8 MMAs, as a two-limb stage does: with one K block (2 MMAs)
+// per barrier the issuing thread's wait and commit per stage left the tensor
+// pipe idle most of the time.
 template <int NL>
 struct PairCfg {
-  static constexpr int kStage = NL * (kATile + kBTile2);
+  static constexpr int kKpS = NL == 1 ? 4 : 1;  // K blocks per stage
+  static constexpr int kStage = kKpS * NL * (kATile + kBTile2);
   static constexpr int kStages = (180 * 1024) / kStage;
   static constexpr int kSmem = 1024 + kStages * kStage + 256;
 };
@@ -526,6 +531,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                           const PairArgs args) {
   constexpr int kStage2 = PairCfg<NL>::kStage;
   constexpr int kStages2 = PairCfg<NL>::kStages;
+  constexpr int kKpS = PairCfg<NL>::kKpS;
+  constexpr int kATiles = kKpS * NL;  // A tiles per stage (B tiles follow them)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2);
@@ -601,27 +608,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pair_tile_coords(t, args, l, tm2, tn);
         const int a_row = l * args.rows_a_p + tm2 * 256 + static_cast<int>(rank) * kBM;
         const int b_row = l * args.rows_b_p + tn * kBN2 + static_cast<int>(rank) * kBHalf;
-        for (int kb = 0; kb < kb_total; ++kb, ++it) {
-          const int s = it % kStages2;
-          const uint32_t ph = (it / kStages2) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1, abort_word, args.flags)) {
-            ok = false;
-            break;
+        for (int kc0 = 0; kc0 < kb_total && ok; kc0 += args.kc_blocks) {
+          const int kc1 = kc0 + args.kc_blocks < kb_total ? kc0 + args.kc_blocks : kb_total;
+          for (int kb = kc0; kb < kc1; kb += kKpS, ++it) {
+            const int nb = kc1 - kb < kKpS ? kc1 - kb : kKpS;  // K blocks in this stage
+            const int s = it % kStages2;
+            const uint32_t ph = (it / kStages2) & 1;
+            if (!mbar_wait(&empty[s], ph ^ 1, abort_word, args.flags)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = smem + s * kStage2;
+            const uint32_t full_leader = mapa_shared(&full[s], 0);
+            // Only the first CTA arms the barrier (with both CTAs' bytes): a
+            // remote release-arrive from the second CTA would wait for its
+            // earlier bulk copies and serialise the stages.  The phase cannot
+            // complete before it is armed, and the second CTA cannot fill a
+            // stage of the next phase before the pair's MMAs freed it.
+            if (leader) mbar_arrive_expect_tx(&full[s], 2 * nb * NL * (kATile + kBTile2));
+            for (int q = 0; q < nb; ++q) {
+#pragma unroll
+              for (int j = 0; j < NL; ++j)
+                tma_load_2d_pair(st + (q * NL + j) * kATile, &tmA, full_leader, (NL * (kb + q) + j) * kBKBytes,
+                                 a_row);
+#pragma unroll
+              for (int j = 0; j < NL; ++j)
+                tma_load_2d_pair(st + kATiles * kATile + (q * NL + j) * kBTile2, &tmB, full_leader,
+                                 (NL * (kb + q) + j) * kBKBytes, b_row);
+            }
           }
-          uint8_t* st = smem + s * kStage2;
-          const uint32_t full_leader = mapa_shared(&full[s], 0);
-          // Only the first CTA arms the barrier (with both CTAs' bytes): a
-          // remote release-arrive from the second CTA would wait for its
-          // earlier bulk copies and serialise the stages.  The phase cannot
-          // complete before it is armed, and the second CTA cannot fill a
-          // stage of the next phase before the pair's MMAs freed it.
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * NL * (kATile + kBTile2));
-#pragma unroll
-          for (int j = 0; j < NL; ++j)
-            tma_load_2d_pair(st + j * kATile, &tmA, full_leader, (NL * kb + j) * kBKBytes, a_row);
-#pragma unroll
-          for (int j = 0; j < NL; ++j)
-            tma_load_2d_pair(st + NL * kATile + j * kBTile2, &tmB, full_leader, (NL * kb + j) * kBKBytes, b_row);
         }
       }
       if (!ok) settle_after_abort();
@@ -651,7 +666,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t dacc = tbase + static_cast<uint32_t>(buf * kBN2);  // two-limb accumulator
           const int kc1 = kc0 + args.kc_blocks < kb_total ? kc0 + args.kc_blocks : kb_total;
-          for (int kb = kc0; kb < kc1; ++kb, ++it) {
+          for (int kb = kc0; kb < kc1; kb += kKpS, ++it) {
             const int s = it % kStages2;
             const uint32_t ph = (it / kStages2) & 1;
             if (!known_full && !mbar_wait(&full[s], ph, abort_word, args.flags)) {
@@ -661,6 +676,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             known_full = false;
             tc_fence_after();
             const uint32_t st = smem_u32(smem + s * kStage2);
+            if constexpr (NL == 1) {
+              // Single-digit moduli: D = A0 B0, the residue product itself,
+              // over the stage's nb K blocks.
+              const int nb = kc1 - kb < kKpS ? kc1 - kb : kKpS;
+              for (int q = 0; q < nb; ++q) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                  const uint64_t a0 = smem_desc_sw64(st + q * kATile + ks * 32);
+                  const uint64_t b0 = smem_desc_sw64(st + kATiles * kATile + q * kBTile2 + ks * 32);
+                  const uint32_t acc = (kb == kc0 && q == 0 && ks == 0) ? 0u : 1u;
+                  mma_fp4_pair(dacc, a0, b0, idesc, s2, s2, acc);  // 1
+                }
+              }
+              known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
+              tc_commit_pair_multicast(&empty[s], 0x3);
+              continue;
+            }
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
               const uint64_t a0 = smem_desc_sw64(st + 0 * kATile + ks * 32);
@@ -670,11 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t b1 = smem_desc_sw64(st + NL * kATile + 1 * kBTile2 + ks * 32);
               const uint64_t b2 = smem_desc_sw64(st + NL * kATile + 2 * kBTile2 + ks * 32);
               const uint32_t acc = (kb == kc0 && ks == 0) ? 0u : 1u;
-              if constexpr (NL == 1) {
-                // Single-digit moduli: D = A0 B0, the residue product itself.
-                (void)a1; (void)a2; (void)b1; (void)b2;
-                mma_fp4_pair(dacc, a0, b0, idesc, s2, s2, acc);            // 1
-              } else if constexpr (NL == 3) {
+              if constexpr (NL == 3) {
                 mma_fp4_pair_fill(d1, a0, b0, idesc, s2, s2, acc);      // 1
                 mma_fp4_pair_use(d1, a0, b1, idesc, s2, s26, 1u);       // 13
                 mma_fp4_pair_lastuse(d2, a0, b2, idesc, s2, s2, acc);   // 1 (in D2)

@@ -18,6 +18,12 @@ cudaError_t launch_split_rows_f64_res8(const double* X, long long ldx, int rows,
                                        cudaStream_t stream);
 cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k, uint8_t* planes,
                                  cudaStream_t stream);
+// Deconstruction of the columns of X (k x cols, row-major) into limb planes
+// (plane row j = column j) without a transposed copy: a column-maximum pass
+// into colmax (cols words of device scratch, zeroed here), then the split.
+cudaError_t launch_split_cols_f64(const double* X, long long ldx, int k, int cols, int p, const SplitModuli& mods,
+                                  uint8_t* planes, int32_t* shifts, unsigned long long* colmax, uint32_t* flags,
+                                  cudaStream_t stream);
 cudaError_t launch_transpose_f64(const double* in, long long ldin, int rows, int cols, double* out,
                                  long long ldout, cudaStream_t stream);
 // INT8 limb planes of the columns of X (k x cols, row-major, k >= 1): plane

@@ -527,6 +527,139 @@ __global__ void transpose_kernel(const T* __restrict__ in, long long ldin, int r
   }
 }
 
+// ------------------------------------------------------------- fp64 columns
+// Columns of X (k x cols, row-major) split without a transposed copy, in two
+// passes over X: the column maxima, then one CTA per (64 columns, 128-row K
+// block) that stages the block in shared memory as it lies in X (16-byte loads
+// along the rows) and forms, per thread, the digit words of 8 consecutive K
+// elements of one column for each of four groups, stored into the column's
+// plane row exactly as the row split stores a row.
+constexpr int kColStrip = 64;       // columns per CTA
+constexpr int kColPitchF64 = 65;    // doubles per staged K row (odd: at most 2-way bank conflicts)
+constexpr int kColMaxRows = 128;    // rows per CTA of the column-maximum pass
+
+// colmax[j] = max over column j of |x| as a 63-bit pattern (atomicMax into a
+// zeroed array): warp w of a CTA reads rows r0 + w, r0 + w + 8, ..., each
+// lane two adjacent columns of a 64-column strip.
+__global__ void __launch_bounds__(256) col_absmax_kernel(const double* __restrict__ X, long long ldx, int k,
+                                                         int cols, unsigned long long* __restrict__ colmax) {
+  __shared__ unsigned long long part[8][kColStrip];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * kColStrip;
+  const int r0 = blockIdx.y * kColMaxRows;
+  const int r1 = min(r0 + kColMaxRows, k);
+  const int col = c0 + 2 * lane;
+  const bool vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0) && (col + 1 < cols);
+  unsigned long long m0 = 0, m1 = 0;
+  for (int row = r0 + warp; row < r1; row += 8) {
+    const double* p = X + static_cast<long long>(row) * ldx + col;
+    unsigned long long b0 = 0, b1 = 0;
+    if (vec) {
+      const double2 v = *reinterpret_cast<const double2*>(p);
+      b0 = static_cast<unsigned long long>(__double_as_longlong(v.x));
+      b1 = static_cast<unsigned long long>(__double_as_longlong(v.y));
+    } else {
+      if (col < cols) b0 = static_cast<unsigned long long>(__double_as_longlong(p[0]));
+      if (col + 1 < cols) b1 = static_cast<unsigned long long>(__double_as_longlong(p[1]));
+    }
+    b0 &= 0x7FFFFFFFFFFFFFFFull;
+    b1 &= 0x7FFFFFFFFFFFFFFFull;
+    m0 = b0 > m0 ? b0 : m0;
+    m1 = b1 > m1 ? b1 : m1;
+  }
+  part[warp][2 * lane] = m0;
+  part[warp][2 * lane + 1] = m1;
+  __syncthreads();
+  if (threadIdx.x < kColStrip && c0 + static_cast<int>(threadIdx.x) < cols) {
+    unsigned long long m = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = part[w][threadIdx.x] > m ? part[w][threadIdx.x] : m;
+    if (m) atomicMax(colmax + c0 + threadIdx.x, m);
+  }
+}
+
+template <int R, int NL>
+__global__ void __launch_bounds__(256, 2)
+    split_cols_f64_kernel(const double* __restrict__ X, long long ldx, int k, int cols, int cols_p, int k_p, int p,
+                          const unsigned long long* __restrict__ colmax, uint8_t* __restrict__ planes,
+                          int32_t* __restrict__ shifts, uint32_t* flags) {
+  extern __shared__ __align__(16) uint32_t tbl[];
+  uint32_t* stage = tbl + kTableWords;
+  double* tile = reinterpret_cast<double*>(stage + 256);  // [128][kColPitchF64]
+  for (int i = threadIdx.x; i < 256; i += 256) {
+    uint32_t code = limb_code(i - 128);
+    if (NL == 1 && i >= static_cast<int>(kMod11Row) && i < static_cast<int>(kMod11Row) + 11)
+      code = mod11_code(i - static_cast<int>(kMod11Row) - 5);
+    stage[i] = code;
+  }
+  const int c0 = blockIdx.x * kColStrip, kb = blockIdx.y;
+  // Stage the K block: row i of the block, columns c0 .. c0 + 63 (zeros
+  // past k and cols), 32 threads per row with two columns each.
+  const bool vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0) && (c0 + kColStrip <= cols);
+  for (int w = threadIdx.x; w < 128 * 32; w += 256) {
+    const int i = w >> 5, q = w & 31;
+    const int row = kb * 128 + i, col = c0 + 2 * q;
+    double v0 = 0.0, v1 = 0.0;
+    if (row < k) {
+      const double* src = X + static_cast<long long>(row) * ldx + col;
+      if (vec) {
+        const double2 v = *reinterpret_cast<const double2*>(src);
+        v0 = v.x;
+        v1 = v.y;
+      } else {
+        if (col < cols) v0 = src[0];
+        if (col + 1 < cols) v1 = src[1];
+      }
+    }
+    tile[i * kColPitchF64 + 2 * q] = v0;
+    tile[i * kColPitchF64 + 2 * q + 1] = v1;
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < kTableWords; w += 256) tbl[w] = stage[w >> (kTableRowShift - 2)];
+  __syncthreads();
+  const char* tb = reinterpret_cast<const char*>(tbl);
+  const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);
+
+  const int col = threadIdx.x >> 2, q = threadIdx.x & 3;  // column of the strip; quarter of the word index
+  const int gcol = c0 + col;
+  const unsigned long long mx = gcol < cols ? colmax[gcol] : 0ull;
+  const int s = mx ? p - frexp_exp_bits(mx) : 0;
+  if (kb == 0 && q == 0 && gcol < cols) {
+    shifts[gcol] = s;
+    if (mx >= 0x7FF0000000000000ull) atomicOr(flags, kFlagNonFinite);
+  }
+  // The fast rounding needs the column's largest magnitude normal (p <= 52).
+  const bool fast = (mx >> 52) != 0 && p <= 52;
+
+  // Plane rows as the row split writes them (single-digit rows of the mixed
+  // list first, then its two-digit rows).
+  const long long row_bytes = static_cast<long long>(NL) * k_p / 2;
+  const long long modulus_stride = static_cast<long long>(cols_p) * row_bytes;
+  constexpr int kSingle = NL == 1 ? (R < kMixSingle ? R : kMixSingle) : 0;
+  const long long row_bytes2 = k_p;
+  const long long modulus_stride2 = static_cast<long long>(cols_p) * row_bytes2;
+  uint8_t* out_row = planes + static_cast<long long>(gcol) * row_bytes;
+  uint8_t* out_row2 = planes + kSingle * modulus_stride + static_cast<long long>(gcol) * row_bytes2;
+  constexpr int kRun = NL == 1 ? 64 : 64 * NL;
+#pragma unroll 1
+  for (int g = 0; g < 4; ++g) {
+    const int r0 = g * 32 + q * 8;  // the 8 elements of K-block word 4g + q
+    uint32_t ulo[8], uhi[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(tile[(r0 + e) * kColPitchF64 + col]));
+      const uint64_t u = fast ? offset_integer_fast(bits, 1075 - s, 1ull << 63) : scaled_offset(bits, s) + (1ull << 62);
+      ulo[e] = static_cast<uint32_t>(u);
+      uhi[e] = static_cast<uint32_t>(u >> 32);
+    }
+    const int word = 4 * g + q;
+    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + kb * kRun) + word;
+    uint32_t* o2 = NL == 1 ? reinterpret_cast<uint32_t*>(out_row2 + kb * 128) + word : nullptr;
+    all_moduli<false, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_stride / 4, o2,
+                          modulus_stride2 / 4);
+  }
+}
+
 int split_grid(int rows_p) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -592,6 +725,64 @@ cudaError_t launch_split_mode(const double* X, long long ldx, int rows, int k, i
     OZEMU_SPLIT_CASE(11) OZEMU_SPLIT_CASE(12) OZEMU_SPLIT_CASE(13) OZEMU_SPLIT_CASE(14) OZEMU_SPLIT_CASE(15)
     OZEMU_SPLIT_CASE(16)
 #undef OZEMU_SPLIT_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+template <int R, int NL>
+cudaError_t launch_split_cols_r(const double* X, long long ldx, int k, int cols, int p, uint8_t* planes,
+                                int32_t* shifts, unsigned long long* colmax, uint32_t* flags, cudaStream_t stream) {
+  const int cols_p = round_up(cols, kRowAlign), k_p = round_up(k, kKAlign);
+  if (k_p / 128 > 65535) return cudaErrorInvalidValue;  // grid.y limit
+  cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(cols) * sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  if (k > 0) {
+    dim3 g1((cols + kColStrip - 1) / kColStrip, (k + kColMaxRows - 1) / kColMaxRows);
+    if (g1.y > 65535) return cudaErrorInvalidValue;
+    col_absmax_kernel<<<g1, 256, 0, stream>>>(X, ldx, k, cols, colmax);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const size_t smem = static_cast<size_t>(kTableWords + 256) * sizeof(uint32_t) +
+                      static_cast<size_t>(128) * kColPitchF64 * sizeof(double);
+  e = cudaFuncSetAttribute(split_cols_f64_kernel<R, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 g2(cols_p / kColStrip, k_p / 128);
+  split_cols_f64_kernel<R, NL><<<g2, 256, smem, stream>>>(X, ldx, k, cols, cols_p, k_p, p, colmax, planes, shifts,
+                                                           flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_cols_f64(const double* X, long long ldx, int k, int cols, int p, const SplitModuli& mods,
+                                  uint8_t* planes, int32_t* shifts, unsigned long long* colmax, uint32_t* flags,
+                                  cudaStream_t stream) {
+  if (mods.limbs == 1) {
+    switch (mods.r) {
+#define OZEMU_COLS_MIX(R) \
+  case R:                 \
+    return launch_split_cols_r<R, 1>(X, ldx, k, cols, p, planes, shifts, colmax, flags, stream);
+      OZEMU_COLS_MIX(1) OZEMU_COLS_MIX(2) OZEMU_COLS_MIX(3) OZEMU_COLS_MIX(4) OZEMU_COLS_MIX(5)
+      OZEMU_COLS_MIX(6) OZEMU_COLS_MIX(7) OZEMU_COLS_MIX(8) OZEMU_COLS_MIX(9) OZEMU_COLS_MIX(10)
+      OZEMU_COLS_MIX(11) OZEMU_COLS_MIX(12) OZEMU_COLS_MIX(13) OZEMU_COLS_MIX(14) OZEMU_COLS_MIX(15)
+      OZEMU_COLS_MIX(16) OZEMU_COLS_MIX(17) OZEMU_COLS_MIX(18) OZEMU_COLS_MIX(19) OZEMU_COLS_MIX(20)
+#undef OZEMU_COLS_MIX
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
+  switch (mods.r) {
+#define OZEMU_COLS_CASE(R)                                                                                     \
+  case R:                                                                                                      \
+    if (mods.limbs == 3) return launch_split_cols_r<R, 3>(X, ldx, k, cols, p, planes, shifts, colmax, flags, stream); \
+    if (mods.limbs == 2) return launch_split_cols_r<R, 2>(X, ldx, k, cols, p, planes, shifts, colmax, flags, stream); \
+    return cudaErrorInvalidValue;
+    OZEMU_COLS_CASE(1) OZEMU_COLS_CASE(2) OZEMU_COLS_CASE(3) OZEMU_COLS_CASE(4) OZEMU_COLS_CASE(5)
+    OZEMU_COLS_CASE(6) OZEMU_COLS_CASE(7) OZEMU_COLS_CASE(8) OZEMU_COLS_CASE(9) OZEMU_COLS_CASE(10)
+    OZEMU_COLS_CASE(11) OZEMU_COLS_CASE(12) OZEMU_COLS_CASE(13) OZEMU_COLS_CASE(14) OZEMU_COLS_CASE(15)
+    OZEMU_COLS_CASE(16)
+#undef OZEMU_COLS_CASE
     default:
       return cudaErrorInvalidValue;
   }
