@@ -592,44 +592,10 @@ __global__ void __launch_bounds__(256, 2)
       code = mod11_code(i - static_cast<int>(kMod11Row) - 5);
     stage[i] = code;
   }
-  const int c0 = blockIdx.x * kColStrip, kb = blockIdx.y;
-  // Stage the K block: row i of the block, columns c0 .. c0 + 63 (zeros
-  // past k and cols), 32 threads per row with two columns each.
-  const bool vec = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0) && (c0 + kColStrip <= cols);
-  for (int w = threadIdx.x; w < 128 * 32; w += 256) {
-    const int i = w >> 5, q = w & 31;
-    const int row = kb * 128 + i, col = c0 + 2 * q;
-    double v0 = 0.0, v1 = 0.0;
-    if (row < k) {
-      const double* src = X + static_cast<long long>(row) * ldx + col;
-      if (vec) {
-        const double2 v = *reinterpret_cast<const double2*>(src);
-        v0 = v.x;
-        v1 = v.y;
-      } else {
-        if (col < cols) v0 = src[0];
-        if (col + 1 < cols) v1 = src[1];
-      }
-    }
-    tile[i * kColPitchF64 + 2 * q] = v0;
-    tile[i * kColPitchF64 + 2 * q + 1] = v1;
-  }
   __syncthreads();
   for (int w = threadIdx.x; w < kTableWords; w += 256) tbl[w] = stage[w >> (kTableRowShift - 2)];
-  __syncthreads();
   const char* tb = reinterpret_cast<const char*>(tbl);
   const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);
-
-  const int col = threadIdx.x >> 2, q = threadIdx.x & 3;  // column of the strip; quarter of the word index
-  const int gcol = c0 + col;
-  const unsigned long long mx = gcol < cols ? colmax[gcol] : 0ull;
-  const int s = mx ? p - frexp_exp_bits(mx) : 0;
-  if (kb == 0 && q == 0 && gcol < cols) {
-    shifts[gcol] = s;
-    if (mx >= 0x7FF0000000000000ull) atomicOr(flags, kFlagNonFinite);
-  }
-  // The fast rounding needs the column's largest magnitude normal (p <= 52).
-  const bool fast = (mx >> 52) != 0 && p <= 52;
 
   // Plane rows as the row split writes them (single-digit rows of the mixed
   // list first, then its two-digit rows).
@@ -638,25 +604,66 @@ __global__ void __launch_bounds__(256, 2)
   constexpr int kSingle = NL == 1 ? (R < kMixSingle ? R : kMixSingle) : 0;
   const long long row_bytes2 = k_p;
   const long long modulus_stride2 = static_cast<long long>(cols_p) * row_bytes2;
-  uint8_t* out_row = planes + static_cast<long long>(gcol) * row_bytes;
-  uint8_t* out_row2 = planes + kSingle * modulus_stride + static_cast<long long>(gcol) * row_bytes2;
   constexpr int kRun = NL == 1 ? 64 : 64 * NL;
-#pragma unroll 1
-  for (int g = 0; g < 4; ++g) {
-    const int r0 = g * 32 + q * 8;  // the 8 elements of K-block word 4g + q
-    uint32_t ulo[8], uhi[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(tile[(r0 + e) * kColPitchF64 + col]));
-      const uint64_t u = fast ? offset_integer_fast(bits, 1075 - s, 1ull << 63) : scaled_offset(bits, s) + (1ull << 62);
-      ulo[e] = static_cast<uint32_t>(u);
-      uhi[e] = static_cast<uint32_t>(u >> 32);
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0);
+  const int col = threadIdx.x >> 2, q = threadIdx.x & 3;  // column of the strip; quarter of the word index
+  const int nstrips = cols_p / kColStrip;
+  const int total = nstrips * (k_p / 128);
+
+  // Persistent: work item w is (64-column strip w % nstrips, K block
+  // w / nstrips), so neighbouring CTAs read neighbouring parts of the same rows.
+  for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    const int c0 = (w % nstrips) * kColStrip, kb = w / nstrips;
+    const bool vec = vec_ok && (c0 + kColStrip <= cols);
+    __syncthreads();  // the previous block is consumed (and the table is built)
+    for (int i2 = threadIdx.x; i2 < 128 * 32; i2 += 256) {
+      const int i = i2 >> 5, h = i2 & 31;
+      const int row = kb * 128 + i, cc = c0 + 2 * h;
+      double v0 = 0.0, v1 = 0.0;
+      if (row < k) {
+        const double* src = X + static_cast<long long>(row) * ldx + cc;
+        if (vec) {
+          const double2 v = *reinterpret_cast<const double2*>(src);
+          v0 = v.x;
+          v1 = v.y;
+        } else {
+          if (cc < cols) v0 = src[0];
+          if (cc + 1 < cols) v1 = src[1];
+        }
+      }
+      tile[i * kColPitchF64 + 2 * h] = v0;
+      tile[i * kColPitchF64 + 2 * h + 1] = v1;
     }
-    const int word = 4 * g + q;
-    uint32_t* o = reinterpret_cast<uint32_t*>(out_row + kb * kRun) + word;
-    uint32_t* o2 = NL == 1 ? reinterpret_cast<uint32_t*>(out_row2 + kb * 128) + word : nullptr;
-    all_moduli<false, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_stride / 4, o2,
-                          modulus_stride2 / 4);
+    __syncthreads();
+    const int gcol = c0 + col;
+    const unsigned long long mx = gcol < cols ? colmax[gcol] : 0ull;
+    const int s = mx ? p - frexp_exp_bits(mx) : 0;
+    if (kb == 0 && q == 0 && gcol < cols) {
+      shifts[gcol] = s;
+      if (mx >= 0x7FF0000000000000ull) atomicOr(flags, kFlagNonFinite);
+    }
+    // The fast rounding needs the column's largest magnitude normal (p <= 52).
+    const bool fast = (mx >> 52) != 0 && p <= 52;
+    uint8_t* out_row = planes + static_cast<long long>(gcol) * row_bytes + kb * kRun;
+    uint8_t* out_row2 = planes + kSingle * modulus_stride + static_cast<long long>(gcol) * row_bytes2 + kb * 128;
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      const int r0 = g * 32 + q * 8;  // the 8 elements of K-block word 4g + q
+      uint32_t ulo[8], uhi[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(tile[(r0 + e) * kColPitchF64 + col]));
+        const uint64_t u =
+            fast ? offset_integer_fast(bits, 1075 - s, 1ull << 63) : scaled_offset(bits, s) + (1ull << 62);
+        ulo[e] = static_cast<uint32_t>(u);
+        uhi[e] = static_cast<uint32_t>(u >> 32);
+      }
+      const int word = 4 * g + q;
+      uint32_t* o = reinterpret_cast<uint32_t*>(out_row) + word;
+      uint32_t* o2 = NL == 1 ? reinterpret_cast<uint32_t*>(out_row2) + word : nullptr;
+      all_moduli<false, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_stride / 4, o2,
+                            modulus_stride2 / 4);
+    }
   }
 }
 
@@ -734,7 +741,6 @@ template <int R, int NL>
 cudaError_t launch_split_cols_r(const double* X, long long ldx, int k, int cols, int p, uint8_t* planes,
                                 int32_t* shifts, unsigned long long* colmax, uint32_t* flags, cudaStream_t stream) {
   const int cols_p = round_up(cols, kRowAlign), k_p = round_up(k, kKAlign);
-  if (k_p / 128 > 65535) return cudaErrorInvalidValue;  // grid.y limit
   cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(cols) * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
   if (k > 0) {
@@ -749,9 +755,10 @@ cudaError_t launch_split_cols_r(const double* X, long long ldx, int k, int cols,
   e = cudaFuncSetAttribute(split_cols_f64_kernel<R, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 g2(cols_p / kColStrip, k_p / 128);
-  split_cols_f64_kernel<R, NL><<<g2, 256, smem, stream>>>(X, ldx, k, cols, cols_p, k_p, p, colmax, planes, shifts,
-                                                           flags);
+  const long long items = static_cast<long long>(cols_p / kColStrip) * (k_p / 128);
+  const int grid = static_cast<int>(items < split_grid(1 << 30) ? items : split_grid(1 << 30));  // 2 CTAs per SM
+  split_cols_f64_kernel<R, NL><<<grid, 256, smem, stream>>>(X, ldx, k, cols, cols_p, k_p, p, colmax, planes, shifts,
+                                                             flags);
   return cudaGetLastError();
 }
 
