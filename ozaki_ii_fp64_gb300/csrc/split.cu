@@ -529,14 +529,16 @@ __global__ void transpose_kernel(const T* __restrict__ in, long long ldin, int r
 
 // ------------------------------------------------------------- fp64 columns
 // Columns of X (k x cols, row-major) split without a transposed copy, in two
-// passes over X: the column maxima, then one CTA per (64 columns, 128-row K
-// block) that stages the block in shared memory as it lies in X (16-byte loads
-// along the rows) and forms, per thread, the digit words of 8 consecutive K
-// elements of one column for each of four groups, stored into the column's
-// plane row exactly as the row split stores a row.
-constexpr int kColStrip = 64;       // columns per CTA
-constexpr int kColPitchF64 = 65;    // doubles per staged K row (odd: at most 2-way bank conflicts)
+// passes over X: the column maxima, then persistent CTAs that each take
+// (64 columns, 128-row K block) items: the block is staged in shared memory
+// column by column (each warp loads 32 consecutive elements of a row), and
+// 16 threads of a column form the digit words of its 16 runs of 8 K elements,
+// so a warp's stores are two 64-byte runs of plane rows, as the row split's
+// stores are 128-byte runs.
+constexpr int kColStrip = 64;       // columns per work item
+constexpr int kColPitchF64 = 129;   // doubles per staged column (odd: loads/stores at most 2 wavefronts per 256 B)
 constexpr int kColMaxRows = 128;    // rows per CTA of the column-maximum pass
+constexpr int kColThreads = 512;
 
 // colmax[j] = max over column j of |x| as a 63-bit pattern (atomicMax into a
 // zeroed array): warp w of a CTA reads rows r0 + w, r0 + w + 8, ..., each
@@ -578,22 +580,38 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const double* __restric
   }
 }
 
+// The digit words of 8 K elements (staged column pointer src) of one column
+// for every modulus: the fast rounding or the general one.
+template <int R, int NL, bool kFast>
+__device__ __forceinline__ void col_words(const double* src, int s, const char* tb, uint32_t lane_hi, uint32_t* o,
+                                          long long mw, uint32_t* o2, long long mw2) {
+  uint32_t ulo[8], uhi[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(src[e]));
+    const uint64_t u = kFast ? offset_integer_fast(bits, 1075 - s, 1ull << 63) : scaled_offset(bits, s) + (1ull << 62);
+    ulo[e] = static_cast<uint32_t>(u);
+    uhi[e] = static_cast<uint32_t>(u >> 32);
+  }
+  all_moduli<false, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, mw, o2, mw2);
+}
+
 template <int R, int NL>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(kColThreads, 2)
     split_cols_f64_kernel(const double* __restrict__ X, long long ldx, int k, int cols, int cols_p, int k_p, int p,
                           const unsigned long long* __restrict__ colmax, uint8_t* __restrict__ planes,
                           int32_t* __restrict__ shifts, uint32_t* flags) {
   extern __shared__ __align__(16) uint32_t tbl[];
   uint32_t* stage = tbl + kTableWords;
-  double* tile = reinterpret_cast<double*>(stage + 256);  // [128][kColPitchF64]
-  for (int i = threadIdx.x; i < 256; i += 256) {
+  double* tile = reinterpret_cast<double*>(stage + 256);  // [kColStrip][kColPitchF64]: column c at tile + c * pitch
+  for (int i = threadIdx.x; i < 256; i += kColThreads) {
     uint32_t code = limb_code(i - 128);
     if (NL == 1 && i >= static_cast<int>(kMod11Row) && i < static_cast<int>(kMod11Row) + 11)
       code = mod11_code(i - static_cast<int>(kMod11Row) - 5);
     stage[i] = code;
   }
   __syncthreads();
-  for (int w = threadIdx.x; w < kTableWords; w += 256) tbl[w] = stage[w >> (kTableRowShift - 2)];
+  for (int w = threadIdx.x; w < kTableWords; w += kColThreads) tbl[w] = stage[w >> (kTableRowShift - 2)];
   const char* tb = reinterpret_cast<const char*>(tbl);
   const uint32_t lane_hi = (threadIdx.x & 31u) << (34 - kTableRowShift);
 
@@ -605,64 +623,45 @@ __global__ void __launch_bounds__(256, 2)
   const long long row_bytes2 = k_p;
   const long long modulus_stride2 = static_cast<long long>(cols_p) * row_bytes2;
   constexpr int kRun = NL == 1 ? 64 : 64 * NL;
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) && ((ldx & 1) == 0);
-  const int col = threadIdx.x >> 2, q = threadIdx.x & 3;  // column of the strip; quarter of the word index
+  const int wd = threadIdx.x & 15;    // word of the 64-byte digit run: K elements 8 wd .. 8 wd + 7
+  const int cl = threadIdx.x >> 4;    // column within a 32-column half of the strip
   const int nstrips = cols_p / kColStrip;
   const int total = nstrips * (k_p / 128);
 
-  // Persistent: work item w is (64-column strip w % nstrips, K block
-  // w / nstrips), so neighbouring CTAs read neighbouring parts of the same rows.
+  // Work item w: (64-column strip w % nstrips, K block w / nstrips), so
+  // neighbouring CTAs read neighbouring parts of the same rows.
   for (int w = blockIdx.x; w < total; w += gridDim.x) {
     const int c0 = (w % nstrips) * kColStrip, kb = w / nstrips;
-    const bool vec = vec_ok && (c0 + kColStrip <= cols);
     __syncthreads();  // the previous block is consumed (and the table is built)
-    for (int i2 = threadIdx.x; i2 < 128 * 32; i2 += 256) {
-      const int i = i2 >> 5, h = i2 & 31;
-      const int row = kb * 128 + i, cc = c0 + 2 * h;
-      double v0 = 0.0, v1 = 0.0;
-      if (row < k) {
-        const double* src = X + static_cast<long long>(row) * ldx + cc;
-        if (vec) {
-          const double2 v = *reinterpret_cast<const double2*>(src);
-          v0 = v.x;
-          v1 = v.y;
-        } else {
-          if (cc < cols) v0 = src[0];
-          if (cc + 1 < cols) v1 = src[1];
-        }
-      }
-      tile[i * kColPitchF64 + 2 * h] = v0;
-      tile[i * kColPitchF64 + 2 * h + 1] = v1;
+    for (int i2 = threadIdx.x; i2 < 128 * kColStrip; i2 += kColThreads) {
+      const int i = i2 / kColStrip, c = i2 % kColStrip;
+      const int row = kb * 128 + i, cc = c0 + c;
+      tile[c * kColPitchF64 + i] = (row < k && cc < cols) ? X[static_cast<long long>(row) * ldx + cc] : 0.0;
     }
     __syncthreads();
-    const int gcol = c0 + col;
-    const unsigned long long mx = gcol < cols ? colmax[gcol] : 0ull;
-    const int s = mx ? p - frexp_exp_bits(mx) : 0;
-    if (kb == 0 && q == 0 && gcol < cols) {
-      shifts[gcol] = s;
-      if (mx >= 0x7FF0000000000000ull) atomicOr(flags, kFlagNonFinite);
-    }
-    // The fast rounding needs the column's largest magnitude normal (p <= 52).
-    const bool fast = (mx >> 52) != 0 && p <= 52;
-    uint8_t* out_row = planes + static_cast<long long>(gcol) * row_bytes + kb * kRun;
-    uint8_t* out_row2 = planes + kSingle * modulus_stride + static_cast<long long>(gcol) * row_bytes2 + kb * 128;
 #pragma unroll 1
-    for (int g = 0; g < 4; ++g) {
-      const int r0 = g * 32 + q * 8;  // the 8 elements of K-block word 4g + q
-      uint32_t ulo[8], uhi[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(tile[(r0 + e) * kColPitchF64 + col]));
-        const uint64_t u =
-            fast ? offset_integer_fast(bits, 1075 - s, 1ull << 63) : scaled_offset(bits, s) + (1ull << 62);
-        ulo[e] = static_cast<uint32_t>(u);
-        uhi[e] = static_cast<uint32_t>(u >> 32);
+    for (int half = 0; half < 2; ++half) {
+      const int c = half * 32 + cl;
+      const int gcol = c0 + c;
+      const unsigned long long mx = gcol < cols ? colmax[gcol] : 0ull;
+      const int s = mx ? p - frexp_exp_bits(mx) : 0;
+      if (kb == 0 && wd == 0 && gcol < cols) {
+        shifts[gcol] = s;
+        if (mx >= 0x7FF0000000000000ull) atomicOr(flags, kFlagNonFinite);
       }
-      const int word = 4 * g + q;
-      uint32_t* o = reinterpret_cast<uint32_t*>(out_row) + word;
-      uint32_t* o2 = NL == 1 ? reinterpret_cast<uint32_t*>(out_row2) + word : nullptr;
-      all_moduli<false, NL>(std::make_integer_sequence<int, R>{}, ulo, uhi, tb, lane_hi, o, modulus_stride / 4, o2,
-                            modulus_stride2 / 4);
+      uint32_t* o = reinterpret_cast<uint32_t*>(planes + static_cast<long long>(gcol) * row_bytes + kb * kRun) + wd;
+      uint32_t* o2 = NL == 1 ? reinterpret_cast<uint32_t*>(planes + kSingle * modulus_stride +
+                                                           static_cast<long long>(gcol) * row_bytes2 + kb * 128) +
+                                   wd
+                             : nullptr;
+      const double* src = tile + c * kColPitchF64 + 8 * wd;
+      // The fast rounding needs the column's largest magnitude normal
+      // (p <= 52); taken when every column of the warp allows it.
+      const bool fast = (mx >> 52) != 0 && p <= 52;
+      if (__all_sync(0xFFFFFFFFu, fast))
+        col_words<R, NL, true>(src, s, tb, lane_hi, o, modulus_stride / 4, o2, modulus_stride2 / 4);
+      else
+        col_words<R, NL, false>(src, s, tb, lane_hi, o, modulus_stride / 4, o2, modulus_stride2 / 4);
     }
   }
 }
@@ -751,14 +750,14 @@ cudaError_t launch_split_cols_r(const double* X, long long ldx, int k, int cols,
     if (e != cudaSuccess) return e;
   }
   const size_t smem = static_cast<size_t>(kTableWords + 256) * sizeof(uint32_t) +
-                      static_cast<size_t>(128) * kColPitchF64 * sizeof(double);
+                      static_cast<size_t>(kColStrip) * kColPitchF64 * sizeof(double);
   e = cudaFuncSetAttribute(split_cols_f64_kernel<R, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(cols_p / kColStrip) * (k_p / 128);
   const int grid = static_cast<int>(items < split_grid(1 << 30) ? items : split_grid(1 << 30));  // 2 CTAs per SM
-  split_cols_f64_kernel<R, NL><<<grid, 256, smem, stream>>>(X, ldx, k, cols, cols_p, k_p, p, colmax, planes, shifts,
-                                                             flags);
+  split_cols_f64_kernel<R, NL><<<grid, kColThreads, smem, stream>>>(X, ldx, k, cols, cols_p, k_p, p, colmax, planes,
+                                                                     shifts, flags);
   return cudaGetLastError();
 }
 
