@@ -583,12 +583,12 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const double* __restric
 // The digit words of 8 K elements (staged column pointer src) of one column
 // for every modulus: the fast rounding or the general one.
 template <int R, int NL, bool kFast>
-__device__ __forceinline__ void col_words(const double* src, int s, const char* tb, uint32_t lane_hi, uint32_t* o,
-                                          long long mw, uint32_t* o2, long long mw2) {
+__device__ __forceinline__ void col_words(const double* src, int rot, int s, const char* tb, uint32_t lane_hi,
+                                          uint32_t* o, long long mw, uint32_t* o2, long long mw2) {
   uint32_t ulo[8], uhi[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(src[e]));
+    const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(src[(e + rot) & 7]));
     const uint64_t u = kFast ? offset_integer_fast(bits, 1075 - s, 1ull << 63) : scaled_offset(bits, s) + (1ull << 62);
     ulo[e] = static_cast<uint32_t>(u);
     uhi[e] = static_cast<uint32_t>(u >> 32);
@@ -636,7 +636,12 @@ __global__ void __launch_bounds__(kColThreads, 2)
     for (int i2 = threadIdx.x; i2 < 128 * kColStrip; i2 += kColThreads) {
       const int i = i2 / kColStrip, c = i2 % kColStrip;
       const int row = kb * 128 + i, cc = c0 + c;
-      tile[c * kColPitchF64 + i] = (row < k && cc < cols) ? X[static_cast<long long>(row) * ldx + cc] : 0.0;
+      // Element e of the column's 8-element group g sits at slot (e + g/2) mod 8
+      // of the group, so that the 16 threads of a column, reading element e
+      // of their groups at once, hit 16 distinct bank pairs.
+      const int g = i >> 3, e = i & 7;
+      tile[c * kColPitchF64 + (g << 3) + ((e + (g >> 1)) & 7)] =
+          (row < k && cc < cols) ? X[static_cast<long long>(row) * ldx + cc] : 0.0;
     }
     __syncthreads();
 #pragma unroll 1
@@ -659,9 +664,9 @@ __global__ void __launch_bounds__(kColThreads, 2)
       // (p <= 52); taken when every column of the warp allows it.
       const bool fast = (mx >> 52) != 0 && p <= 52;
       if (__all_sync(0xFFFFFFFFu, fast))
-        col_words<R, NL, true>(src, s, tb, lane_hi, o, modulus_stride / 4, o2, modulus_stride2 / 4);
+        col_words<R, NL, true>(src, wd >> 1, s, tb, lane_hi, o, modulus_stride / 4, o2, modulus_stride2 / 4);
       else
-        col_words<R, NL, false>(src, s, tb, lane_hi, o, modulus_stride / 4, o2, modulus_stride2 / 4);
+        col_words<R, NL, false>(src, wd >> 1, s, tb, lane_hi, o, modulus_stride / 4, o2, modulus_stride2 / 4);
     }
   }
 }
