@@ -164,7 +164,6 @@ CrtModuli crt_moduli(int r, int limbs = 3) {
       c.g[l][j] = static_cast<uint32_t>((static_cast<uint64_t>(pj % m) * inv) % m);
       pj *= moduli(limbs).m[j];
     }
-    for (int w = 0; w < 4; ++w) c.prefix[l][w] = static_cast<uint32_t>(pref >> (32 * w));
     pref *= m;
   }
   // Direct form.  pref is now M (< 2^126).
@@ -173,7 +172,8 @@ CrtModuli crt_moduli(int r, int limbs = 3) {
     const uint32_t m = moduli(limbs).m[l];
     const u128 Ml = M / m;
     const u128 W = Ml * inv_mod(static_cast<uint32_t>(Ml % m), m);  // < M
-    for (int w = 0; w < 16; ++w) c.wb[l / 4][w] |= static_cast<uint32_t>((W >> (8 * w)) & 0xFF) << (8 * (l % 4));
+    for (int t = 0; t < 8; ++t)
+      c.w16[l / 4][t][(l % 4) / 2] |= static_cast<uint32_t>((W >> (16 * t)) & 0xFFFF) << (16 * (l % 2));
     if (l == r - 1)
       for (int t = 0; t < 8; ++t) c.wl16[t] = static_cast<uint32_t>((W >> (16 * t)) & 0xFFFF);
   }

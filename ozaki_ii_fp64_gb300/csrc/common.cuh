@@ -91,9 +91,10 @@ struct CrtModuli {
   uint32_t magic[kMaxR];                  // floor(2^32 / m)
   uint32_t inv[kMaxR];                    // (m_0 ... m_{l-1})^-1 mod m_l
   uint32_t g[kMaxR][kMaxR];               // g[l][j] = (m_0...m_{j-1}) inv_l mod m_l, j < l
-  uint32_t prefix[kMaxR][4];              // m_0 ... m_{l-1} as 128-bit little-endian words
   // Direct form: C' = sum_l c_l W_l - q M with W_l = (M/m_l) ((M/m_l)^-1 mod m_l).
-  uint32_t wb[5][16];                     // byte w of W_{4q+i} at byte i of wb[q][w]
+  // w16[q][t][h]: 16-bit limb t of W_{4q+2h} (low half) and of W_{4q+2h+1}
+  // (high half), the operands of the two-way dot products.
+  uint32_t w16[5][8][2];
   uint32_t wl16[8];                       // W_{r-1} in 16-bit limbs (a lone last modulus, r = 1 mod 4)
   uint32_t m16[9];                        // M in 16-bit limbs
   float gt[9];                            // 2^(16 t) / M

@@ -68,10 +68,11 @@ __device__ __noinline__ uint64_t round_scaled(i128 X, int S) {
   return neg ? (bits | 0x8000000000000000ull) : bits;
 }
 
-// round_scaled for the common case, on the words of X: a normal (or
-// overflowing) result takes the top 64 bits of |X| and a sticky bit; a
-// result in the subnormal range goes through round_scaled.
-__device__ __forceinline__ uint64_t round_scaled_fast(i128 X, int S) {
+// round_scaled for a normal (or overflowing) result, on the words of X: the
+// top 64 bits of |X| and a sticky bit.  A result in the subnormal range sets
+// sub and returns an unspecified value (round_scaled takes it).
+__device__ __forceinline__ uint64_t round_scaled_normal(i128 X, int S, bool& sub) {
+  sub = false;
   if (X == 0) return 0ull;
   const bool neg = X < 0;
   const u128 mag = neg ? static_cast<u128>(-X) : static_cast<u128>(X);
@@ -91,7 +92,7 @@ __device__ __forceinline__ uint64_t round_scaled_fast(i128 X, int S) {
     e = 63 - lz;
   }
   int b = e - S;  // exponent of the result's leading bit
-  if (b < -1022) return round_scaled(X, S);
+  sub = b < -1022;
   uint64_t q = M >> 11;
   const uint64_t rb = (M >> 10) & 1ull;
   const bool st = sticky || (M & 0x3FFull) != 0;
