@@ -663,6 +663,7 @@ def run_gpu(args):
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
                     "traffic": (int(tr["bytes_per_launch"]) if tr else None),
+                    "traffic_per": (tr.get("unit_of_launch", "launch") if tr else None),
                     "kernel": "limb_gemm_pair_kernel (CTA pair, 256x224 tiles), %d launch(es) per chunk"
                               % fam.gemm_launches(r),
                     "peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (pk_kind, FP4_OVER_BF16),
