@@ -36,3 +36,4 @@ from .ozaki2 import (  # noqa: F401
     error_bound_ratio_sliced, error_bound_ratio_pairs, residues_one_modulus, residues_of_moduli,
 )
 from .cost_model import oi_star, tme_time, deconstruction_time  # noqa: F401
+from . import int4_int8  # noqa: F401  (INT4 x INT8 in four FP4 products)
