@@ -54,9 +54,10 @@ def a_table(t=T):
 
 
 def b_table(t=T, g=G):
-    """v(b) for b in [-128, 127]: v_1, v_2, v_3 run over S (in S's order),
-    v_4 is fixed by the relation sum_k t_k g_k v_k = 0 and must lie in S;
-    the first v found for each b = sum_k g_k v_k is kept."""
+    """v(b) for b in [-128, 127]: among the v in S^4 with the relation
+    sum_k t_k g_k v_k = 0 and b = sum_k g_k v_k, the one with the smallest
+    sum_k |v_k|, ties going to the lexicographically smallest tuple (a rule
+    that does not depend on the order S is listed in)."""
     out = {}
     c4 = t[3] * g[3]
     for v1 in S:
@@ -67,7 +68,10 @@ def b_table(t=T, g=G):
                     continue
                 v = (v1, v2, v3, int(v4))
                 b = sum(gk * vk for gk, vk in zip(g, v))
-                if B_RANGE[0] <= b <= B_RANGE[1] and b not in out:
+                if not B_RANGE[0] <= b <= B_RANGE[1]:
+                    continue
+                key = (sum(abs(x) for x in v), v)
+                if b not in out or key < (sum(abs(x) for x in out[b]), out[b]):
                     out[b] = v
     missing = [b for b in range(B_RANGE[0], B_RANGE[1] + 1) if b not in out]
     if missing:
