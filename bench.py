@@ -1072,6 +1072,30 @@ def other_workloads(torch, oz, fams, stream, sh, check, dev, args, pk, fp4_peak,
     out["igemm_s8_4096"] = leg
     del Ai, Bi, Ci
 
+    # The exact INT4 x INT8 -> INT32 product in four FP4 products (the
+    # encoding a b = sum_k g_k u_k(a) v_k(b)) at 4096^3, beside the INT8 x
+    # INT8 product's nine on the same shape.
+    A4_h, B4_h = make_pair(4096, 4096, 4096, 6, "int4_int8")
+    A4 = torch.from_numpy(A4_h).to(dev)
+    B4 = torch.from_numpy(B4_h).to(dev)
+    C4 = torch.empty((4096, 4096), dtype=torch.int32, device=dev)
+    s4_ms = time_ms(torch, stream, lambda: check(oz.ozemu_igemm_s4s8(4096, 4096, 4096, A4.data_ptr(), B4.data_ptr(),
+                                                                     C4.data_ptr(), sh), "igemm_s4s8"), reps=5)
+    leg4 = {"ms": round(s4_ms, 3), "tops": round(iflop / (s4_ms / 1e3) / 1e12, 1), "fp4_products": 4,
+            "roofline": {"bound": "tensor", "achieved": round(4 * iflop / (s4_ms / 1e3) / 1e12, 1),
+                         "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(4 * iflop / (s4_ms / 1e3) / 1e12 / fp4_peak, 4)},
+            "vs_int8_x_int8_9_products": round(ig_ms / s4_ms, 3),
+            "launches": "split A rows (4 planes), split B columns (4 planes), plane GEMM (int32 epilogue)",
+            "inputs": "A uniform in [-8, 7], B uniform int8, seed 6"}
+    # Exactness on a sample of rows: float64 products of these integers are exact.
+    rows = np.arange(0, 4096, 257)
+    ref = A4_h[rows].astype(np.float64) @ B4_h.astype(np.float64)
+    leg4["exact_on_sampled_rows"] = bool(np.array_equal(C4[torch.from_numpy(rows).to(dev)].cpu().numpy(),
+                                                        ref.astype(np.int64)))
+    out["igemm_s4s8_4096"] = leg4
+    del A4, B4, C4
+
     # OI* of [TME4] abstract on this GPU: c_q r P_fp64 / (8 P_int), with c_q
     # the split kernel's thread instructions per input element and modulus
     # (ncu, r = 13), P_int the issue rate of the SMs (4 schedulers x 32 lanes

@@ -76,7 +76,8 @@ typedef enum {
   OZEMU_ERR_NONFINITE = -5,   /* an input held Inf or NaN (output unspecified) */
   OZEMU_ERR_TIMEOUT = -6,     /* a kernel pipeline wait hit its time limit  */
   OZEMU_ERR_UNSUPPORTED = -7, /* current device is not sm_103 (GB300)       */
-  OZEMU_ERR_SCRATCH_TOO_SMALL = -8 /* problem needs more than the fixed scratch */
+  OZEMU_ERR_SCRATCH_TOO_SMALL = -8, /* problem needs more than the fixed scratch */
+  OZEMU_ERR_RANGE = -9        /* an INT4 operand held a value outside [-8, 7] */
 } ozemu_status;
 
 /* ------------------------------------------------------------------------ */
@@ -90,6 +91,21 @@ typedef enum {
  * m, n or k = 0 is a no-op (k = 0 zeroes C32).  Uses the cached workspace. */
 int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B,
                    int32_t* C32, cudaStream_t stream);
+
+/* Exact C32 = A B for INT4 A (m x k, values in [-8, 7] stored one per int8,
+ * row-major, lda = k) and int8 B (k x n, row-major, ldb = n); C32 int32
+ * m x n row-major (ldc = n).  [AWE] abstract: an INT4 x INT8 product in four
+ * FP4 products.  Encoding: a b = sum_k g_k u_k(a) v_k(b) with g = (3, 2, 6,
+ * 12) and every plane value in S = {0, +-1, +-2, +-3, +-4, +-6, +-8, +-12};
+ * the B planes lie on the relation sum_k t_k g_k v_k = 0, t = (-12, -9, -6,
+ * 3/2), and u_k(a) = a + t_k z(a).  The four plane products go into one fp32
+ * accumulator per tile (the weights carried by the block scales), exact over
+ * K chunks of 8192 (|running value| <= 1024 per K element), summed in int32.
+ * An element of A outside [-8, 7] counts as 0 and makes the next
+ * ozemu_get_status() return OZEMU_ERR_RANGE.  k > 2097151 ->
+ * OZEMU_ERR_K_OVERFLOW; m, n or k = 0 is a no-op (k = 0 zeroes C32).  Uses
+ * the cached workspace.  device pointers; stream-ordered. */
+int ozemu_igemm_s4s8(int m, int n, int k, const int8_t* A, const int8_t* B, int32_t* C32, cudaStream_t stream);
 
 /* Emulated fp64 C = A B with r moduli: deconstruction of A's rows and B's
  * columns ([TME4] abstract), 9 FP4 limb GEMMs per modulus with modular
@@ -159,6 +175,23 @@ int ozemu_split_rows_f64(int rows, int k, const double* X, int ldx, int p, int r
  * split of 128-row x 64-column blocks staged in shared memory. */
 int ozemu_split_cols_f64(int k, int cols, const double* X, int ldx, int p, int r,
                          uint8_t* planes, int32_t* shifts, cudaStream_t stream);
+
+/* Four-plane layout of the INT4 x INT8 product: uint8
+ * [rows_p][k_p/128][4][64], for each 128-element K block the 64 bytes of
+ * each of the four planes (two FP4 e2m1 codes of digit / 2 per byte, low
+ * nibble = even k); rows_p = rows rounded up to 128, k_p = k rounded up to
+ * 128, padding digit 0.  Bytes for rows x k; 0 on negative sizes. */
+size_t ozemu_four_plane_bytes(int rows, int k);
+
+/* The four planes u_k of the rows of an INT4 matrix X (rows x k, values in
+ * [-8, 7] one per int8, leading dimension ldx >= k), for
+ * ozemu_igemm_s4s8's encoding; out-of-range values as there.  planes: device,
+ * 16-byte aligned, ozemu_four_plane_bytes(rows, k) bytes. */
+int ozemu_split_rows_s4(int rows, int k, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream);
+
+/* The four planes v_k of the columns of an int8 matrix X (k x cols,
+ * row-major, leading dimension ldx >= cols): plane row j holds column j. */
+int ozemu_split_cols_s8_four(int k, int cols, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream);
 
 /* INT8 limb planes of the rows of X (rows x k, ldx >= k): 3 planes. */
 int ozemu_split_rows_s8(int rows, int k, const int8_t* X, int ldx,

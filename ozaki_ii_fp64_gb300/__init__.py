@@ -22,11 +22,12 @@ OZEMU_ERR_NONFINITE = -5
 OZEMU_ERR_TIMEOUT = -6
 OZEMU_ERR_UNSUPPORTED = -7
 OZEMU_ERR_SCRATCH_TOO_SMALL = -8
+OZEMU_ERR_RANGE = -9
 
 _STATUS_NAMES = {
     0: "OZEMU_OK", -1: "OZEMU_ERR_INVALID_ARG", -2: "OZEMU_ERR_K_OVERFLOW", -3: "OZEMU_ERR_ALLOC",
     -4: "OZEMU_ERR_CUDA", -5: "OZEMU_ERR_NONFINITE", -6: "OZEMU_ERR_TIMEOUT", -7: "OZEMU_ERR_UNSUPPORTED",
-    -8: "OZEMU_ERR_SCRATCH_TOO_SMALL",
+    -8: "OZEMU_ERR_SCRATCH_TOO_SMALL", -9: "OZEMU_ERR_RANGE",
 }
 
 
@@ -44,6 +45,10 @@ _S = ctypes.c_size_t
 
 _SIGNATURES = {
     "ozemu_igemm_s8": (_I, [_I, _I, _I, _P, _P, _P, _P]),
+    "ozemu_igemm_s4s8": (_I, [_I, _I, _I, _P, _P, _P, _P]),
+    "ozemu_four_plane_bytes": (_S, [_I, _I]),
+    "ozemu_split_rows_s4": (_I, [_I, _I, _P, _I, _P, _P]),
+    "ozemu_split_cols_s8_four": (_I, [_I, _I, _P, _I, _P, _P]),
     "ozemu_dgemm": (_I, [_I, _I, _I, _P, _I, _P, _I, _P, _I, _I, _P]),
     "ozemu_max_moduli": (_I, []),
     "ozemu_moduli": (_I, [_I, _P]),
@@ -125,6 +130,22 @@ def _call(name, *args):
 
 def ozemu_igemm_s8(m, n, k, A, B, C32, stream):
     return _call("ozemu_igemm_s8", m, n, k, A, B, C32, stream)
+
+
+def ozemu_igemm_s4s8(m, n, k, A, B, C32, stream):
+    return _call("ozemu_igemm_s4s8", m, n, k, A, B, C32, stream)
+
+
+def ozemu_four_plane_bytes(rows, k):
+    return _call("ozemu_four_plane_bytes", rows, k)
+
+
+def ozemu_split_rows_s4(rows, k, X, ldx, planes, stream):
+    return _call("ozemu_split_rows_s4", rows, k, X, ldx, planes, stream)
+
+
+def ozemu_split_cols_s8_four(k, cols, X, ldx, planes, stream):
+    return _call("ozemu_split_cols_s8_four", k, cols, X, ldx, planes, stream)
 
 
 def ozemu_dgemm(m, n, k, A, lda, B, ldb, C, ldc, r, stream):
@@ -415,6 +436,20 @@ def igemm_s8(A, B, out=None, stream=None):
         raise ValueError("expected contiguous int8 matrices with matching inner dimension")
     C = torch.empty((m, n), dtype=torch.int32, device=A.device) if out is None else out
     _check(ozemu_igemm_s8(m, n, k, A.data_ptr(), B.data_ptr(), C.data_ptr(), _stream(stream)), "ozemu_igemm_s8")
+    return C
+
+
+def igemm_s4s8(A, B, out=None, stream=None):
+    """Exact int32 A @ B of a contiguous int8 cuda tensor A holding INT4 values
+    ([-8, 7]) and a contiguous int8 cuda tensor B (four FP4 products)."""
+    torch = _torch()
+    m, k = A.shape
+    k2, n = B.shape
+    if k != k2 or not A.is_contiguous() or not B.is_contiguous():
+        raise ValueError("expected contiguous int8 matrices with matching inner dimension")
+    C = torch.empty((m, n), dtype=torch.int32, device=A.device) if out is None else out
+    _check(ozemu_igemm_s4s8(m, n, k, A.data_ptr(), B.data_ptr(), C.data_ptr(), _stream(stream)),
+           "ozemu_igemm_s4s8")
     return C
 
 

@@ -1,9 +1,13 @@
 // C ABI of libozemu.so: argument checks, per-call constants, the cached
 // per-device workspace and status flags, and the staging of the kernels.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <numeric>
+#include <utility>
+#include <vector>
 
 #include "../../include/ozemu.h"
 #include "common.cuh"
@@ -609,6 +613,116 @@ int limb_gemm_s32(int m, int n, int k, const uint8_t* ap, const uint8_t* bp, int
 
 constexpr int kMaxKInt32 = 131071;
 
+// ------------------------------------------------ INT4 x INT8, four planes
+// [AWE] abstract: an INT4 x INT8 product in four FP4 products.  The encoding
+// a b = sum_k g_k u_k(a) v_k(b) (weights and relation in common.cuh): the A
+// planes u_k(a) = a + t_k z(a) with the smallest |z| (then the smaller z) of
+// the form n/d, d in {1, 2, 3, 4, 6}, that puts every u_k in S; the B planes
+// the v in S^4 on the relation with b = sum_k g_k v_k of smallest digit sum,
+// then lexicographically smallest.  Built once on the host.
+constexpr int kMaxKS4 = 2097151;  // |C| <= 1024 k stays below 2^31
+constexpr int kDigitsS[15] = {0, 1, -1, 2, -2, 3, -3, 4, -4, 6, -6, 8, -8, 12, -12};
+
+bool digit_in_s(int d) {
+  for (int x : kDigitsS)
+    if (x == d) return true;
+  return false;
+}
+
+uint32_t e2m1_code_host(int d) {  // the e2m1 nibble of d / 2 for d in S
+  const int a = d < 0 ? -d : d;
+  const uint32_t mag = a <= 4 ? static_cast<uint32_t>(a) : (a == 6 ? 5u : (a == 8 ? 6u : 7u));
+  return (d < 0 ? 8u : 0u) | mag;
+}
+
+struct FourTables {
+  FourCodes a, b;
+  bool ok = false;
+};
+
+FourTables build_four_tables() {
+  FourTables t;
+  for (int i = 0; i < 256; ++i) t.a.code[i] = t.b.code[i] = 0xFFFFFFFFu;
+  // Candidates z = n / d in lowest terms, by |z| then z.
+  std::vector<std::pair<int, int>> zs;
+  for (int d : {1, 2, 3, 4, 6})
+    for (int n = -48; n <= 48; ++n) {
+      int g = std::gcd(n < 0 ? -n : n, d);
+      if (g == 0) g = d;
+      const std::pair<int, int> z(n / g, d / g);
+      if (std::find(zs.begin(), zs.end(), z) == zs.end()) zs.push_back(z);
+    }
+  std::sort(zs.begin(), zs.end(), [](const std::pair<int, int>& x, const std::pair<int, int>& y) {
+    const long long ax = static_cast<long long>(std::abs(x.first)) * y.second;
+    const long long ay = static_cast<long long>(std::abs(y.first)) * x.second;
+    if (ax != ay) return ax < ay;
+    return static_cast<long long>(x.first) * y.second < static_cast<long long>(y.first) * x.second;
+  });
+  for (int a = -8; a <= 7; ++a) {
+    bool found = false;
+    for (const auto& z : zs) {
+      uint32_t code = 0;
+      bool ok = true;
+      for (int k = 0; k < 4 && ok; ++k) {
+        const int num = kFourRelation2[k] * z.first, den = 2 * z.second;  // t_k z = num / den
+        if (num % den != 0) {
+          ok = false;
+          break;
+        }
+        const int u = a + num / den;
+        if (!digit_in_s(u)) ok = false;
+        code |= e2m1_code_host(u) << (8 * k);
+      }
+      if (ok) {
+        t.a.code[a + 128] = code;
+        found = true;
+        break;
+      }
+    }
+    if (!found) return t;
+  }
+  int best_sum[256];
+  int best_v[256][4];
+  for (int i = 0; i < 256; ++i) best_sum[i] = -1;
+  for (int v0 : kDigitsS)
+    for (int v1 : kDigitsS)
+      for (int v2 : kDigitsS)
+        for (int v3 : kDigitsS) {
+          const int v[4] = {v0, v1, v2, v3};
+          int rel = 0, b = 0, sum = 0;
+          for (int k = 0; k < 4; ++k) {
+            rel += kFourRelation2[k] * kFourWeights[k] * v[k];
+            b += kFourWeights[k] * v[k];
+            sum += std::abs(v[k]);
+          }
+          if (rel != 0 || b < -128 || b > 127) continue;
+          const int i = b + 128;
+          const bool better = best_sum[i] < 0 || sum < best_sum[i] ||
+                              (sum == best_sum[i] && std::lexicographical_compare(v, v + 4, best_v[i], best_v[i] + 4));
+          if (better) {
+            best_sum[i] = sum;
+            for (int k = 0; k < 4; ++k) best_v[i][k] = v[k];
+          }
+        }
+  for (int i = 0; i < 256; ++i) {
+    if (best_sum[i] < 0) return t;
+    uint32_t code = 0;
+    for (int k = 0; k < 4; ++k) code |= e2m1_code_host(best_v[i][k]) << (8 * k);
+    t.b.code[i] = code;
+  }
+  t.ok = true;
+  return t;
+}
+
+const FourTables& four_tables() {
+  static const FourTables t = build_four_tables();
+  return t;
+}
+
+size_t four_plane_bytes(int rows, int k) {
+  return static_cast<size_t>(round_up(rows, kRowAlign)) * 2 * static_cast<size_t>(round_up(k, kKAlign));
+}
+
 // Scratch of the allocation-free entry point: one fixed static device array
 // (its device address is looked up per device, never allocated by us).
 constexpr size_t kNoAllocBytes = size_t(64) << 20;
@@ -895,6 +1009,72 @@ int ozemu_igemm_s8(int m, int n, int k, const int8_t* A, const int8_t* B, int32_
   if (launch_split_cols_s8(B, n, k, n, bp, stream) != cudaSuccess) return OZEMU_ERR_CUDA;
   if (cudaStreamWaitEvent(stream, d->ev[1], 0) != cudaSuccess) return OZEMU_ERR_CUDA;
   return limb_gemm_s32(m, n, k, ap, bp, C32, n, d, stream);
+}
+
+size_t ozemu_four_plane_bytes(int rows, int k) {
+  if (rows < 0 || k < 0) return 0;
+  return four_plane_bytes(rows, k);
+}
+
+int ozemu_split_rows_s4(int rows, int k, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream) {
+  if (rows < 0 || k < 0 || ldx < (k > 1 ? k : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (rows == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !aligned16(planes) || !rows_ok(rows, 2)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (!four_tables().ok) return OZEMU_ERR_UNSUPPORTED;
+  return cuda_status(launch_split_rows_four(X, ldx, rows, k, four_tables().a, planes, d->flags, stream));
+}
+
+int ozemu_split_cols_s8_four(int k, int cols, const int8_t* X, int ldx, uint8_t* planes, cudaStream_t stream) {
+  if (k < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1)) return OZEMU_ERR_INVALID_ARG;
+  if (cols == 0) return OZEMU_OK;
+  if ((k > 0 && !X) || !planes || !aligned16(planes) || !rows_ok(cols, 2)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (!four_tables().ok) return OZEMU_ERR_UNSUPPORTED;
+  if (k == 0) return OZEMU_OK;
+  return cuda_status(launch_split_cols_four(X, ldx, k, cols, four_tables().b, planes, d->flags, stream));
+}
+
+int ozemu_igemm_s4s8(int m, int n, int k, const int8_t* A, const int8_t* B, int32_t* C32, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0) return OZEMU_ERR_INVALID_ARG;
+  if (k > kMaxKS4) return OZEMU_ERR_K_OVERFLOW;
+  if (m == 0 || n == 0) return OZEMU_OK;
+  if (!C32 || (k > 0 && (!A || !B)) || !rows_ok(m, 2) || !rows_ok(n, 2)) return OZEMU_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int s = device_state(&d);
+  if (s != OZEMU_OK) return s;
+  if (k == 0) return cuda_status(launch_zero_s32(C32, m, n, n, stream));
+  if (!four_tables().ok) return OZEMU_ERR_UNSUPPORTED;
+  const size_t pa = align256(four_plane_bytes(m, k)), pb = align256(four_plane_bytes(n, k));
+  uint8_t* ws = nullptr;
+  s = workspace(d, pa + pb, &ws);
+  if (s != OZEMU_OK) return s;
+  uint8_t* ap = ws;
+  uint8_t* bp = ws + pa;
+  if (launch_split_rows_four(A, k, m, k, four_tables().a, ap, d->flags, stream) != cudaSuccess ||
+      launch_split_cols_four(B, n, k, n, four_tables().b, bp, d->flags, stream) != cudaSuccess)
+    return OZEMU_ERR_CUDA;
+  LimbGemmCall c;
+  c.residue_mode = false;
+  c.m = m;
+  c.n = n;
+  c.k = k;
+  c.r = 1;
+  c.a_planes = ap;
+  c.b_planes = bp;
+  c.res_out = nullptr;
+  c.ldr = 0;
+  c.c32 = C32;
+  c.ldc = n;
+  c.kc_blocks = 64;  // exact chunks of 8192: |running sum| <= 1024 per K element
+  c.limbs = 4;
+  c.em = epi_moduli(1);
+  c.flags = d->flags;
+  return cuda_status(launch_limb_gemm(c, stream));
 }
 
 int ozemu_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
@@ -1184,6 +1364,7 @@ int ozemu_get_status(cudaStream_t stream) {
   if (cudaMemset(d->flags, 0, sizeof(f)) != cudaSuccess) return OZEMU_ERR_CUDA;
   if (f & kFlagTimeout) return OZEMU_ERR_TIMEOUT;
   if (f & kFlagNonFinite) return OZEMU_ERR_NONFINITE;
+  if (f & kFlagRange) return OZEMU_ERR_RANGE;
   return OZEMU_OK;
 }
 

@@ -20,6 +20,7 @@ constexpr int kKAlign = 128;     // plane k padded to this (GEMM stage K)
 // Device flag bits (per-device word, reported by ozemu_get_status).
 constexpr uint32_t kFlagNonFinite = 1u;
 constexpr uint32_t kFlagTimeout = 2u;
+constexpr uint32_t kFlagRange = 4u;  // an INT4 operand held a value outside [-8, 7]
 
 // Time limit of one pipeline wait before the kernel gives up (ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -65,6 +66,18 @@ struct NarrowModuli {
   uint32_t off62[kMaxModuli];  // 2^62 mod m
   uint32_t offA[kMaxModuli];   // 2^(p_A) mod m
   uint32_t w16[kMaxModuli][4]; // 2^(16 c) mod m
+};
+
+// INT4 x INT8 in four FP4 products ([AWE] abstract): a b = sum_k g_k u_k(a)
+// v_k(b) with u, v in S, the B planes on the relation sum_k t_k g_k v_k = 0
+// (t = (-12, -9, -6, 3/2), kept doubled to stay integral) and
+// u_k(a) = a + t_k z(a).  The codes of value i - 128: the e2m1 nibble of
+// plane j's digit / 2 in byte j; 0xFFFFFFFF marks a value outside the
+// operand's range.
+constexpr int kFourWeights[4] = {3, 2, 6, 12};
+constexpr int kFourRelation2[4] = {-24, -18, -12, 3};
+struct FourCodes {
+  uint32_t code[256];
 };
 
 // Per-modulus constants for the GEMM epilogue.

@@ -488,6 +488,11 @@ constexpr int kSmem2 = PairCfg<3>::kSmem;
 static_assert(PairCfg<1>::kSmem == kSmem2 && PairCfg<2>::kSmem == kSmem2, "one shared-memory size for every NL");
 constexpr int kTmemCols2 = 512;
 constexpr uint32_t kColD1p = 0, kColD2p = 224, kColSf2p = 448, kColSf26p = 464;
+// INT4 x INT8 (four planes, NL = 4): the slot at kColSf26p holds 12 instead
+// of 26, and two more slots hold 4 and 6, so that each plane product k gets
+// scales whose product is 4 g_k (FP4 holds half the digit): (2, 6), (2, 4),
+// (4, 6), (4, 12) for g = (3, 2, 6, 12).
+constexpr uint32_t kColSf4p = 480, kColSf6p = 496;
 constexpr int kPairCols = kBN2 / 2;              // accumulator columns per epilogue thread (two per lane quarter)
 constexpr int kGroupM2 = 16;                     // pair-tile rows per raster group
 
@@ -553,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // (exact for K chunks of 4096); single-digit moduli: one accumulator
   // D = A0 B0.  Then two tiles' accumulators alternate and the MMAs of one
   // round run while the epilogue drains the other.
-  constexpr int kBufs = NL <= 2 ? 2 : 1;
+  constexpr int kBufs = (NL <= 2 || NL == 4) ? 2 : 1;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStages2; ++s) {
@@ -585,8 +590,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 16; ++i) v[i] = 0x40404040u;
     tmem_st16(tbase + lane_off + kColSf2p, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0x5D5D5D5Du;
+    for (int i = 0; i < 16; ++i) v[i] = NL == 4 ? 0x54545454u : 0x5D5D5D5Du;  // 12 or 26
     tmem_st16(tbase + lane_off + kColSf26p, v);
+    if constexpr (NL == 4) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0x48484848u;  // 4
+      tmem_st16(tbase + lane_off + kColSf4p, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0x4C4C4C4Cu;  // 6
+      tmem_st16(tbase + lane_off + kColSf6p, v);
+    }
     tmem_wait_st();
   }
   // Both CTAs' barriers initialised and scales written before any remote
@@ -676,6 +689,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             known_full = false;
             tc_fence_after();
             const uint32_t st = smem_u32(smem + s * kStage2);
+            if constexpr (NL == 4) {
+              // INT4 x INT8: D = sum_k g_k A_k B_k over the four planes, the
+              // weights carried by the scale pairs.
+              const uint32_t s4 = tbase + kColSf4p, s6 = tbase + kColSf6p, s12 = tbase + kColSf26p;
+#pragma unroll
+              for (int ks = 0; ks < 2; ++ks) {
+                uint64_t a[4], b[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  a[j] = smem_desc_sw64(st + j * kATile + ks * 32);
+                  b[j] = smem_desc_sw64(st + 4 * kATile + j * kBTile2 + ks * 32);
+                }
+                const uint32_t acc = (kb == kc0 && ks == 0) ? 0u : 1u;
+                mma_fp4_pair(dacc, a[0], b[0], idesc, s2, s6, acc);  // 3
+                mma_fp4_pair(dacc, a[1], b[1], idesc, s2, s4, 1u);   // 2
+                mma_fp4_pair(dacc, a[2], b[2], idesc, s4, s6, 1u);   // 6
+                mma_fp4_pair(dacc, a[3], b[3], idesc, s4, s12, 1u);  // 12
+                if (ks == 0)
+                  known_full = mbar_test_wait(&full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1);
+              }
+              tc_commit_pair_multicast(&empty[s], 0x3);
+              continue;
+            }
             if constexpr (NL == 1) {
               // Single-digit moduli: D = A0 B0, the residue product itself,
               // over the stage's nb K blocks.
@@ -762,6 +798,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if constexpr (NL == 4) {
+          // INT4 x INT8: one accumulator, exact below 2^24 for K chunks of
+          // 8192 (|a b| <= 1024); the int32 sums of the chunks add up in C32.
+          const uint32_t dcol = tbase + lane_off + static_cast<uint32_t>(buf * kBN2) + col0;
+          uint32_t v1[kSlice], n1[kSlice];
+          tmem_ld_cols<kSlice>(dcol, n1);
+#pragma unroll
+          for (int c = 0; c < CW; c += kSlice) {
+            tmem_wait_ld_regs(n1);
+#pragma unroll
+            for (int i = 0; i < kSlice; ++i) v1[i] = n1[i];
+            if (c + kSlice < CW) tmem_ld_cols<kSlice>(dcol + c + kSlice, n1);
+            if (grow < args.m) {
+              int32_t* crow = args.c32 + static_cast<long long>(grow) * args.ldc;
+              const int col = tn * kBN2 + static_cast<int>(col0) + c;
+#pragma unroll
+              for (int i = 0; i < kSlice; ++i) {
+                if (col + i < args.n) {
+                  const int v = __float2int_rn(__uint_as_float(v1[i]));
+                  crow[col + i] = first ? v : crow[col + i] + v;
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+          continue;
+        }
         if constexpr (NL <= 2) {
           // One accumulator (|D| < 3600 * 4096 < 2^24 for two-limb moduli,
           // 64 * 2^18 for single-digit ones): one reduction modulo m.
@@ -964,6 +1029,7 @@ cudaError_t launch_pair(const LimbGemmCall& c, cudaStream_t stream) {
   // element, so chunks of 2^18 (2048 blocks) are exact.
   a.kc_blocks = (NL == 2 && c.kc_blocks > 32) ? 32 : c.kc_blocks;
   if (NL == 1) a.kc_blocks = a.kb_total < 2048 ? a.kb_total : 2048;
+  if (NL == 4 && a.kc_blocks > 64) a.kc_blocks = 64;
   a.rows_a_p = rows_a_p;
   a.rows_b_p = rows_b_p;
   a.tiles_m2 = (c.m + 255) / 256;
@@ -1033,6 +1099,10 @@ cudaError_t launch_limb_gemm(const LimbGemmCall& call, cudaStream_t stream) {
   if (call.limbs == 2) {  // two-limb moduli: residue products only
     if (!call.residue_mode) return cudaErrorInvalidValue;
     return use_pair(call) ? launch_pair<false, 2>(call, stream) : launch_mode<true, 2>(call, stream);
+  }
+  if (call.limbs == 4) {  // INT4 x INT8 planes: int32 products only, any n
+    if (call.residue_mode || call.kc_blocks < 1) return cudaErrorInvalidValue;
+    return launch_pair<true, 4>(call, stream);
   }
   if (call.limbs == 1) {  // single-digit moduli: residue products only
     if (!call.residue_mode) return cudaErrorInvalidValue;

@@ -24,6 +24,13 @@ cudaError_t launch_split_rows_s8(const int8_t* X, long long ldx, int rows, int k
 cudaError_t launch_split_cols_f64(const double* X, long long ldx, int k, int cols, int p, const SplitModuli& mods,
                                   uint8_t* planes, int32_t* shifts, unsigned long long* colmax, uint32_t* flags,
                                   cudaStream_t stream);
+// The four planes of INT8-stored operands for the INT4 x INT8 product
+// (rows of A; columns of B, k >= 1), layout [rows_p][k_p/128][4][64];
+// values the code table marks out of range raise kFlagRange.
+cudaError_t launch_split_rows_four(const int8_t* X, long long ldx, int rows, int k, const FourCodes& codes,
+                                   uint8_t* planes, uint32_t* flags, cudaStream_t stream);
+cudaError_t launch_split_cols_four(const int8_t* X, long long ldx, int k, int cols, const FourCodes& codes,
+                                   uint8_t* planes, uint32_t* flags, cudaStream_t stream);
 cudaError_t launch_transpose_f64(const double* in, long long ldin, int rows, int cols, double* out,
                                  long long ldout, cudaStream_t stream);
 // INT8 limb planes of the columns of X (k x cols, row-major, k >= 1): plane

@@ -510,6 +510,120 @@ __global__ void __launch_bounds__(256) split_cols_s8_kernel(const int8_t* __rest
     *reinterpret_cast<uint4*>(o + l * 64) = make_uint4(w[l][0], w[l][1], w[l][2], w[l][3]);
 }
 
+// ------------------------------------------------- INT4 x INT8, four planes
+// Packs 8 four-plane codes (nibble of plane j in byte j) into the four plane
+// words: word j holds plane j of elements 0..7, element e in nibble e.
+__device__ __forceinline__ void pack8_four(const uint32_t (&c)[8], uint32_t (&w)[4]) {
+  const uint32_t p01 = c[0] + (c[1] << 4), p23 = c[2] + (c[3] << 4);
+  const uint32_t p45 = c[4] + (c[5] << 4), p67 = c[6] + (c[7] << 4);
+  const uint32_t lo = __byte_perm(p01, p23, 0x5140), hi = __byte_perm(p45, p67, 0x5140);
+  const uint32_t lo2 = __byte_perm(p01, p23, 0x7362), hi2 = __byte_perm(p45, p67, 0x7362);
+  w[0] = __byte_perm(lo, hi, 0x5410);
+  w[1] = __byte_perm(lo, hi, 0x7632);
+  w[2] = __byte_perm(lo2, hi2, 0x5410);
+  w[3] = __byte_perm(lo2, hi2, 0x7632);
+}
+
+// Code of an int8 value from the four-plane table; a value the table marks
+// out of range (0xFFFFFFFF) raises kFlagRange and takes digit 0.
+__device__ __forceinline__ uint32_t four_code(const uint32_t* lut, int v, bool& bad) {
+  const uint32_t c = lut[v + 128];
+  bad |= (c == 0xFFFFFFFFu);
+  return c == 0xFFFFFFFFu ? 0u : c;
+}
+
+// Four planes of the rows of X (rows x k, int8, row-major): row i of the
+// planes holds, per 128-element K block, the 64 bytes of each of the four
+// planes side by side; padding rows and K elements get code 0.
+__global__ void __launch_bounds__(kSplitThreads) split_rows_four_kernel(const int8_t* __restrict__ X, long long ldx,
+                                                                       int rows, int k, int rows_p, int k_p,
+                                                                       uint8_t* __restrict__ planes,
+                                                                       const __grid_constant__ FourCodes codes,
+                                                                       uint32_t* flags) {
+  __shared__ uint32_t lut[256];
+  for (int i = threadIdx.x; i < 256; i += kSplitThreads) lut[i] = codes.code[i];
+  __syncthreads();
+  const long long row_bytes = 2LL * k_p;
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(X) & 7u) == 0) && ((ldx & 7) == 0);
+  bool bad = false;
+  for (int row = blockIdx.x; row < rows_p; row += gridDim.x) {
+    uint32_t* o_row = reinterpret_cast<uint32_t*>(planes + static_cast<long long>(row) * row_bytes);
+    const int8_t* rowp = X + static_cast<long long>(row) * ldx;
+    for (int k0 = threadIdx.x * kElemsPerThread; k0 < k_p; k0 += kChunk) {
+      int8_t v[8];
+      if (row < rows && vec_ok && k0 + 8 <= k) {
+        uint2 w = __ldcs(reinterpret_cast<const uint2*>(rowp + k0));
+        const int8_t* pv = reinterpret_cast<const int8_t*>(&w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = pv[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (row < rows && k0 + e < k) ? rowp[k0 + e] : static_cast<int8_t>(0);
+      }
+      uint32_t c[8], w[4];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = four_code(lut, v[e], bad);
+      pack8_four(c, w);
+      uint32_t* o = o_row + (k0 >> 7) * 64 + (k0 & 127) / 8;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[16 * j] = w[j];
+    }
+  }
+  if (bad) atomicOr(flags, kFlagRange);
+}
+
+// Four planes of the columns of X (k x cols, int8, row-major): plane row j
+// holds column j.  One CTA per (128-element K block, 64 columns), staged in
+// shared memory as in split_cols_s8_kernel.
+__global__ void __launch_bounds__(256) split_cols_four_kernel(const int8_t* __restrict__ X, long long ldx, int k,
+                                                              int cols, int k_p, uint8_t* __restrict__ planes,
+                                                              const __grid_constant__ FourCodes codes,
+                                                              uint32_t* flags) {
+  __shared__ uint32_t lut[256];
+  __shared__ __align__(16) uint8_t tile[128 * (64 + 4)];
+  constexpr int kPitch = 64 + 4;
+  lut[threadIdx.x] = codes.code[threadIdx.x];
+  const int c0 = blockIdx.x * 64;
+  const int kb = blockIdx.y;
+  const bool vec = ((reinterpret_cast<uintptr_t>(X) & 3u) == 0) && ((ldx & 3) == 0) && (c0 + 64 <= cols);
+  for (int w = threadIdx.x; w < 128 * 16; w += 256) {
+    const int i = w / 16, q = w % 16;
+    const int kr = kb * 128 + i;
+    uint32_t v = 0;
+    if (kr < k) {
+      const int8_t* src = X + static_cast<long long>(kr) * ldx + c0 + 4 * q;
+      if (vec) {
+        v = __ldg(reinterpret_cast<const unsigned int*>(src));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c0 + 4 * q + e < cols) v |= static_cast<uint32_t>(static_cast<uint8_t>(src[e])) << (8 * e);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(tile + i * kPitch + 4 * q) = v;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int col = (threadIdx.x >> 5) * 8 + (lane >> 2);  // column within the tile, 0..63
+  const int q = lane & 3;                                // K elements 32 q .. 32 q + 31 of the block
+  bool bad = false;
+  uint32_t w[4][4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint32_t c[8], wg[4];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      c[e] = four_code(lut, static_cast<int>(static_cast<int8_t>(tile[(q * 32 + g * 8 + e) * kPitch + col])), bad);
+    pack8_four(c, wg);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j][g] = wg[j];
+  }
+  uint8_t* o = planes + static_cast<long long>(c0 + col) * (2LL * k_p) + kb * 256 + q * 16;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(o + j * 64) = make_uint4(w[j][0], w[j][1], w[j][2], w[j][3]);
+  if (bad) atomicOr(flags, kFlagRange);
+}
+
 // out[c][r] = in[r][c] for a rows x cols block of 32 x 32 tiles.
 template <typename T>
 __global__ void transpose_kernel(const T* __restrict__ in, long long ldin, int rows, int cols, T* __restrict__ out,
@@ -823,6 +937,23 @@ cudaError_t launch_split_cols_s8(const int8_t* X, long long ldx, int k, int cols
   if (k_p / 128 > 65535) return cudaErrorInvalidValue;  // grid.y limit
   dim3 grid(cols_p / kColTile, k_p / 128);
   split_cols_s8_kernel<<<grid, 256, 0, stream>>>(X, ldx, k, cols, k_p, planes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_rows_four(const int8_t* X, long long ldx, int rows, int k, const FourCodes& codes,
+                                   uint8_t* planes, uint32_t* flags, cudaStream_t stream) {
+  const int rows_p = round_up(rows, kRowAlign), k_p = round_up(k, kKAlign);
+  split_rows_four_kernel<<<split_grid(rows_p), kSplitThreads, 0, stream>>>(X, ldx, rows, k, rows_p, k_p, planes,
+                                                                           codes, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_cols_four(const int8_t* X, long long ldx, int k, int cols, const FourCodes& codes,
+                                   uint8_t* planes, uint32_t* flags, cudaStream_t stream) {
+  const int cols_p = round_up(cols, kRowAlign), k_p = round_up(k, kKAlign);
+  if (k_p / 128 > 65535) return cudaErrorInvalidValue;  // grid.y limit
+  dim3 grid(cols_p / 64, k_p / 128);
+  split_cols_four_kernel<<<grid, 256, 0, stream>>>(X, ldx, k, cols, k_p, planes, codes, flags);
   return cudaGetLastError();
 }
 

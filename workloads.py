@@ -12,6 +12,10 @@ cases; all data synthetic, seeded with numpy's default_rng):
                       integer in [-10, 10] per entry, seed 3
 * dgemv_16384_n{1,8}  A 16384 x 16384 ~ N(0, 1), B 16384 x n, seed 4
 * dgemm_4096_k65536   M=N=4096, K=65536, A, B ~ N(0, 1), seed 5
+
+and the INT4 x INT8 product of the four-product encoding (a sub-record of
+the measurement, not a metric workload): igemm_s4s8_4096, M=N=K=4096, A
+uniform in [-8, 7] (one value per int8), B uniform int8, seed 6.
 """
 
 import numpy as np
@@ -42,8 +46,13 @@ def draw(rng, shape, dist):
 
 
 def make_pair(m, n, k, seed, dist):
-    """(A, B) with A m x k and B k x n, row-major, drawn from one generator."""
+    """(A, B) with A m x k and B k x n, row-major, drawn from one generator
+    (dist "int4_int8": A in [-8, 7] and B in [-128, 127], both int8)."""
     rng = np.random.default_rng(seed)
+    if dist == "int4_int8":
+        A = rng.integers(-8, 8, size=(m, k), dtype=np.int8)
+        B = rng.integers(-128, 128, size=(k, n), dtype=np.int8)
+        return A, B
     A = np.ascontiguousarray(draw(rng, (m, k), dist))
     B = np.ascontiguousarray(draw(rng, (k, n), dist))
     return A, B
