@@ -462,6 +462,23 @@ def run_gpu(args):
     for key in ("m", "n", "k"):
         if getattr(args, key):
             spec[key] = getattr(args, key)
+    if spec["kind"] == "igemm":
+        # The exact integer products alone (their own line; not the metric's workload).
+        stream = torch.cuda.current_stream(dev)
+
+        def check_int(st, what):
+            if st != 0:
+                raise oz.OzemuError(st, what)
+
+        pk, pk_kind = peaks()
+        legs = int_products(torch, oz, stream, stream.cuda_stream, check_int, dev, pk["bf16_tflops"] * FP4_OVER_BF16)
+        if rank == 0:
+            print(json.dumps({"metric": "exact INT8 x INT8 GEMM TOP/s (2MNK/t) at 4096^3", "unit": "TOP/s",
+                              "value": legs["igemm_s8_4096"]["tops"], "higher_is_better": True, "n_gpus": ws,
+                              "dtype": "int8", "data": "synthetic", "config": {"workload": args.workload},
+                              "peak_source": "%s bf16 burst x %.0f" % (pk_kind, FP4_OVER_BF16),
+                              "int_products": legs}))
+        return
     if spec["kind"] != "dgemm":
         raise SystemExit("bench.py times the emulated DGEMM workloads")
     A_h, B_h = make_pair(spec["m"], spec["n"], spec["k"], spec["seed"], spec["dist"])
@@ -947,6 +964,59 @@ def fp4_mma_rate(torch, oz, stream, sh, check, dev, clk, fp4_peak):
     return out
 
 
+def int_products(torch, oz, stream, sh, check, dev, fp4_peak):
+    """The exact integer products at 4096^3: INT8 x INT8 (nine FP4 limb
+    products) beside cuBLASLt's INT8 GEMM, and INT4 x INT8 (four plane
+    products)."""
+    out = {}
+    # The exact INT8 x INT8 -> INT32 product (9 FP4 limb GEMMs) on the 4096^3
+    # int8 workload, beside cuBLASLt's INT8 GEMM on the same matrices.
+    Ai_h, Bi_h = make_pair(4096, 4096, 4096, WORKLOADS["igemm_s8_4096"]["seed"], "int8")
+    Ai = torch.from_numpy(Ai_h).to(dev)
+    Bi = torch.from_numpy(Bi_h).to(dev)
+    Ci = torch.empty((4096, 4096), dtype=torch.int32, device=dev)
+    ig_ms = time_ms(torch, stream, lambda: check(oz.ozemu_igemm_s8(4096, 4096, 4096, Ai.data_ptr(), Bi.data_ptr(),
+                                                                   Ci.data_ptr(), sh), "igemm"), reps=5)
+    iflop = 2.0 * 4096 ** 3
+    leg = {"ms": round(ig_ms, 3), "tops": round(iflop / (ig_ms / 1e3) / 1e12, 1),
+           "roofline": {"bound": "tensor", "achieved": round(9 * iflop / (ig_ms / 1e3) / 1e12, 1),
+                        "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                        "frac": round(9 * iflop / (ig_ms / 1e3) / 1e12 / fp4_peak, 4)},
+           "launches": "split A rows, split B columns, limb GEMM (int32 epilogue)"}
+    if hasattr(torch, "_int_mm"):
+        ref = torch._int_mm(Ai, Bi)
+        lt_ms = time_ms(torch, stream, lambda: torch._int_mm(Ai, Bi), reps=3)
+        leg["exact_vs_cublaslt"] = bool(torch.equal(ref, Ci))
+        leg["cublaslt_int8_ms"] = round(lt_ms, 3)
+    out["igemm_s8_4096"] = leg
+    del Ai, Bi, Ci
+
+    # The exact INT4 x INT8 -> INT32 product in four FP4 products (the
+    # encoding a b = sum_k g_k u_k(a) v_k(b)) at 4096^3, beside the INT8 x
+    # INT8 product's nine on the same shape.
+    A4_h, B4_h = make_pair(4096, 4096, 4096, 6, "int4_int8")
+    A4 = torch.from_numpy(A4_h).to(dev)
+    B4 = torch.from_numpy(B4_h).to(dev)
+    C4 = torch.empty((4096, 4096), dtype=torch.int32, device=dev)
+    s4_ms = time_ms(torch, stream, lambda: check(oz.ozemu_igemm_s4s8(4096, 4096, 4096, A4.data_ptr(), B4.data_ptr(),
+                                                                     C4.data_ptr(), sh), "igemm_s4s8"), reps=5)
+    leg4 = {"ms": round(s4_ms, 3), "tops": round(iflop / (s4_ms / 1e3) / 1e12, 1), "fp4_products": 4,
+            "roofline": {"bound": "tensor", "achieved": round(4 * iflop / (s4_ms / 1e3) / 1e12, 1),
+                         "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(4 * iflop / (s4_ms / 1e3) / 1e12 / fp4_peak, 4)},
+            "vs_int8_x_int8_9_products": round(ig_ms / s4_ms, 3),
+            "launches": "split A rows (4 planes), split B columns (4 planes), plane GEMM (int32 epilogue)",
+            "inputs": "A uniform in [-8, 7], B uniform int8, seed 6"}
+    # Exactness on a sample of rows: float64 products of these integers are exact.
+    rows = np.arange(0, 4096, 257)
+    ref = A4_h[rows].astype(np.float64) @ B4_h.astype(np.float64)
+    leg4["exact_on_sampled_rows"] = bool(np.array_equal(C4[torch.from_numpy(rows).to(dev)].cpu().numpy(),
+                                                        ref.astype(np.int64)))
+    out["igemm_s4s8_4096"] = leg4
+    del A4, B4, C4
+    return out
+
+
 def other_workloads(torch, oz, fams, stream, sh, check, dev, args, pk, fp4_peak, head_native, clk):
     """Sub-records of the other workloads: each product through the
     library's call for the shape (three-limb with the fused narrow path for
@@ -1050,51 +1120,7 @@ def other_workloads(torch, oz, fams, stream, sh, check, dev, args, pk, fp4_peak,
         out[name] = rec
         del A, B, C
         torch.cuda.empty_cache()
-    # The exact INT8 x INT8 -> INT32 product (9 FP4 limb GEMMs) on the 4096^3
-    # int8 workload, beside cuBLASLt's INT8 GEMM on the same matrices.
-    Ai_h, Bi_h = make_pair(4096, 4096, 4096, WORKLOADS["igemm_s8_4096"]["seed"], "int8")
-    Ai = torch.from_numpy(Ai_h).to(dev)
-    Bi = torch.from_numpy(Bi_h).to(dev)
-    Ci = torch.empty((4096, 4096), dtype=torch.int32, device=dev)
-    ig_ms = time_ms(torch, stream, lambda: check(oz.ozemu_igemm_s8(4096, 4096, 4096, Ai.data_ptr(), Bi.data_ptr(),
-                                                                   Ci.data_ptr(), sh), "igemm"), reps=5)
-    iflop = 2.0 * 4096 ** 3
-    leg = {"ms": round(ig_ms, 3), "tops": round(iflop / (ig_ms / 1e3) / 1e12, 1),
-           "roofline": {"bound": "tensor", "achieved": round(9 * iflop / (ig_ms / 1e3) / 1e12, 1),
-                        "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                        "frac": round(9 * iflop / (ig_ms / 1e3) / 1e12 / fp4_peak, 4)},
-           "launches": "split A rows, split B columns, limb GEMM (int32 epilogue)"}
-    if hasattr(torch, "_int_mm"):
-        ref = torch._int_mm(Ai, Bi)
-        lt_ms = time_ms(torch, stream, lambda: torch._int_mm(Ai, Bi), reps=3)
-        leg["exact_vs_cublaslt"] = bool(torch.equal(ref, Ci))
-        leg["cublaslt_int8_ms"] = round(lt_ms, 3)
-    out["igemm_s8_4096"] = leg
-    del Ai, Bi, Ci
-
-    # The exact INT4 x INT8 -> INT32 product in four FP4 products (the
-    # encoding a b = sum_k g_k u_k(a) v_k(b)) at 4096^3, beside the INT8 x
-    # INT8 product's nine on the same shape.
-    A4_h, B4_h = make_pair(4096, 4096, 4096, 6, "int4_int8")
-    A4 = torch.from_numpy(A4_h).to(dev)
-    B4 = torch.from_numpy(B4_h).to(dev)
-    C4 = torch.empty((4096, 4096), dtype=torch.int32, device=dev)
-    s4_ms = time_ms(torch, stream, lambda: check(oz.ozemu_igemm_s4s8(4096, 4096, 4096, A4.data_ptr(), B4.data_ptr(),
-                                                                     C4.data_ptr(), sh), "igemm_s4s8"), reps=5)
-    leg4 = {"ms": round(s4_ms, 3), "tops": round(iflop / (s4_ms / 1e3) / 1e12, 1), "fp4_products": 4,
-            "roofline": {"bound": "tensor", "achieved": round(4 * iflop / (s4_ms / 1e3) / 1e12, 1),
-                         "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                         "frac": round(4 * iflop / (s4_ms / 1e3) / 1e12 / fp4_peak, 4)},
-            "vs_int8_x_int8_9_products": round(ig_ms / s4_ms, 3),
-            "launches": "split A rows (4 planes), split B columns (4 planes), plane GEMM (int32 epilogue)",
-            "inputs": "A uniform in [-8, 7], B uniform int8, seed 6"}
-    # Exactness on a sample of rows: float64 products of these integers are exact.
-    rows = np.arange(0, 4096, 257)
-    ref = A4_h[rows].astype(np.float64) @ B4_h.astype(np.float64)
-    leg4["exact_on_sampled_rows"] = bool(np.array_equal(C4[torch.from_numpy(rows).to(dev)].cpu().numpy(),
-                                                        ref.astype(np.int64)))
-    out["igemm_s4s8_4096"] = leg4
-    del A4, B4, C4
+    out.update(int_products(torch, oz, stream, sh, check, dev, fp4_peak))
 
     # OI* of [TME4] abstract on this GPU: c_q r P_fp64 / (8 P_int), with c_q
     # the split kernel's thread instructions per input element and modulus

@@ -747,15 +747,28 @@ __global__ void __launch_bounds__(kColThreads, 2)
   for (int w = blockIdx.x; w < total; w += gridDim.x) {
     const int c0 = (w % nstrips) * kColStrip, kb = w / nstrips;
     __syncthreads();  // the previous block is consumed (and the table is built)
-    for (int i2 = threadIdx.x; i2 < 128 * kColStrip; i2 += kColThreads) {
-      const int i = i2 / kColStrip, c = i2 % kColStrip;
-      const int row = kb * 128 + i, cc = c0 + c;
-      // Element e of the column's 8-element group g sits at slot (e + g/2) mod 8
-      // of the group, so that the 16 threads of a column, reading element e
-      // of their groups at once, hit 16 distinct bank pairs.
-      const int g = i >> 3, e = i & 7;
-      tile[c * kColPitchF64 + (g << 3) + ((e + (g >> 1)) & 7)] =
-          (row < k && cc < cols) ? X[static_cast<long long>(row) * ldx + cc] : 0.0;
+    {
+      // Thread t stages column c = t % 64, rows i0 + 8 j (i0 = t / 64): each
+      // warp loads 32 consecutive elements of a row.  Element e of the
+      // column's 8-element group g sits at slot (e + g/2) mod 8 of the group,
+      // so that the 16 threads of a column, reading element e of their
+      // groups at once, hit 16 distinct bank pairs.
+      static_assert(kColThreads == 8 * kColStrip, "eight rows of the strip per pass");
+      const int c = threadIdx.x % kColStrip, i0 = threadIdx.x / kColStrip;
+      const int cc = c0 + c, row0 = kb * 128 + i0;
+      const double* src = X + static_cast<long long>(row0) * ldx + cc;
+      const long long step = 8 * ldx;
+      double* dst = tile + c * kColPitchF64;
+      double v[16];
+      if (cc < cols && kb * 128 + 128 <= k) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = src[j * step];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = (cc < cols && row0 + 8 * j < k) ? src[j * step] : 0.0;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dst[(j << 3) + ((i0 + (j >> 1)) & 7)] = v[j];
     }
     __syncthreads();
 #pragma unroll 1
