@@ -45,15 +45,15 @@ NARROW_MAX_K = 1 << 24       # k limit of the fused narrow path
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CPU_SAMPLE = 128        # sampled rows and columns of C per oracle step
 CPU_MIN_SECONDS = 10.0  # bounded CPU baseline: repeat the sample at least this long
-SPLIT_INSTR_PER_ELEMENT = 173.0  # split kernel, r = 13: thread instructions per input element (ncu, profiles/)
-SPLIT_INSTR_R = 13
+SPLIT_INSTR_PER_ELEMENT = 222.0  # row split, mixed-digit r = 19: thread instructions per input element (ncu)
+SPLIT_INSTR_R = 19
 FAMILIES = ("mixed", "two", "three")
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ozemu", choices=["ozemu", "reference"])
     ap.add_argument("--workload", default="dgemm_8192_wide", choices=sorted(WORKLOADS))
@@ -267,6 +267,17 @@ class ClockSampler:
                  "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: wait (up to 3 s) for its first
+        # sample, so that the samples fall inside the region that follows.
+        t0 = time.time()
+        while time.time() - t0 < 3.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+        self._skip = 0
+        with open(self.path) as f:
+            self._skip = sum(1 for _ in f)  # samples taken before the region
 
     def stop(self):
         if self.proc is None:
@@ -276,12 +287,14 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
+        rows, before = [], []
         with open(self.path) as f:
-            for line in f:
+            for i, line in enumerate(f):
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
-                    rows.append(parts)
+                    (rows if i >= getattr(self, "_skip", 0) else before).append(parts)
+        if not rows:  # a region shorter than the sampling interval: the last sample before it
+            rows = before[-1:]
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
@@ -733,7 +746,7 @@ def run_gpu(args):
         pe = fam.plane_bytes(128, 128, r) / (128 * 128)  # plane bytes per input element
         line["memory_stages"] = {
             "deconstruct_A": mem_entry("split_rows_f64_kernel", split_a, (8.0 + pe) * m * k),
-            "deconstruct_B": mem_entry("transpose + split_rows_f64_kernel", split_b, (8.0 + pe) * k * n),
+            "deconstruct_B": mem_entry("col_absmax_kernel + split_cols_f64_kernel", split_b, (8.0 + pe) * k * n),
             "reconstruct": mem_entry("crt_kernel", crt, (r + 8.0) * m * n)}
         del flush
 
@@ -1142,7 +1155,7 @@ def other_workloads(torch, oz, fams, stream, sh, check, dev, args, pk, fp4_peak,
                             out[name]["operational_intensity"],
                             "below_oi_star": out[name]["operational_intensity"] < oi_star}
         out["oi_star"] = {"c_q": round(c_q, 2), "c_q_source": "split kernel, %g thread instructions per element at "
-                          "r = %d (ncu, profiles/split_rows_dgemm_8192_wide.md)" % (SPLIT_INSTR_PER_ELEMENT,
+                          "r = %d (ncu, profiles/split_crt_dgemm_4096_mixed.md)" % (SPLIT_INSTR_PER_ELEMENT,
                                                                                      SPLIT_INSTR_R),
                           "P_fp64_tflops": round(nat, 3), "P_int_per_s": P_int,
                           "P_int_source": "%d SMs x 4 schedulers x 32 lanes x %.0f MHz" % (sms, mhz),
