@@ -51,7 +51,10 @@ struct LimbGemmCall {
   int32_t* c32;
   long long ldc;
   int kc_blocks;
-  int limbs = 3;  // limbs per modulus: 3, or 2 for the two-limb moduli (residue mode only)
+  // Digit planes per modulus: 3 (three-limb moduli, or the INT8 product), 2
+  // (two-limb moduli) or 1 (single-digit moduli), residue mode; 4: the four
+  // planes of the INT4 x INT8 product (int mode, r = 1, any K).
+  int limbs = 3;
   EpiModuli em;
   uint32_t* flags;
 };
