@@ -585,11 +585,13 @@ def run_gpu(args):
         ev_start.record(stream)
         s_split.wait_event(ev_start)
         s_crt.wait_event(ev_start)
-        split_b()
+        # As the library enqueues them: the chunks' splits on the split
+        # stream first, then B's split on the main stream.
         for c, (row0, mc, apc, sac, resc) in enumerate(chunk_bufs):
             check(fam.split_rows(mc, k, A.data_ptr() + row0 * k * 8, k, pA, r, apc.data_ptr(), sac.data_ptr(),
                                  s_split.cuda_stream), "split A chunk")
             evA[c].record(s_split)
+        split_b()
         if args.schedule == "phased":
             # Splits of A beside B's, then the GEMMs back to back, then the CRTs.
             stream.wait_event(evA[nch - 1])
