@@ -15,8 +15,8 @@
  *   [AWE]  arXiv 2609.24519 (Adaptive Weight Encoding for FP4 tensor cores),
  *          English abstract -- digits in S = {0,+-1,+-2,+-3,+-4,+-6,+-8,+-12}
  *          (FP4 e2m1 values times two), base-13 limbs with weights
- *          (1, 13, 169), 9 exact FP4 GEMMs per INT8 x INT8 product, the same
- *          formulation modulo m.
+ *          (1, 13, 169), 9 exact FP4 GEMMs per INT8 x INT8 product, 4 per
+ *          INT4 x INT8 product, the same formulation modulo m.
  *
  * Conventions
  *   - Matrices are row-major.  A is m x k (leading dimension lda >= k),
@@ -52,8 +52,8 @@
  *
  * Errors: calls return an ozemu_status.  Argument checks happen on the host
  * before anything is enqueued.  Device-side conditions (non-finite input,
- * a pipeline wait that hit its time limit) set a per-device flag that
- * ozemu_get_status reports and clears.
+ * an INT4 value outside [-8, 7], a pipeline wait that hit its time limit)
+ * set a per-device flag that ozemu_get_status reports and clears.
  */
 #ifndef OZEMU_H
 #define OZEMU_H
@@ -279,8 +279,8 @@ int ozemu_crt_f64(int m, int n, int r, const uint8_t* residues, const int32_t* s
 /* ------------------------------------------------------------------------ */
 
 /* Synchronises `stream`, then returns and clears the current device's flags:
- * OZEMU_ERR_NONFINITE, OZEMU_ERR_TIMEOUT, OZEMU_ERR_CUDA (a sticky CUDA error)
- * or OZEMU_OK.  The flags of ozemu_dgemm_noalloc are separate: see
+ * OZEMU_ERR_TIMEOUT, OZEMU_ERR_NONFINITE, OZEMU_ERR_RANGE (in that order of
+ * precedence), OZEMU_ERR_CUDA (a sticky CUDA error) or OZEMU_OK.  The flags of ozemu_dgemm_noalloc are separate: see
  * ozemu_get_status_noalloc. */
 int ozemu_get_status(cudaStream_t stream);
 
