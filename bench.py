@@ -582,7 +582,7 @@ def run_gpu(args):
     if narrow:
         launches_per_step = 3  # B's column residues, fused pass over A, CRT
     else:
-        launches_per_step = 2 + nch * (2 + fam.gemm_launches(r))  # B: transpose + split; chunk: split, GEMMs, CRT
+        launches_per_step = 2 + nch * (2 + fam.gemm_launches(r))  # B: column maxima + split; chunk: split, GEMMs, CRT
     n_dominant = 1 if narrow else nch
 
     def step(gev=None):
