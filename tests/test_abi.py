@@ -165,6 +165,13 @@ FAKE = 0x10000  # a non-null, 16-byte aligned value; never dereferenced
     lambda oz: oz.ozemu_crt_f64_2limb(4, 4, 0, FAKE, FAKE, FAKE, FAKE, 4, NULL),  # r < 1
     lambda oz: oz.ozemu_dgemm_host_2limb(4, 4, 60, FAKE, 60, FAKE, 4, FAKE, 4, 1, NULL),  # 2k >= 113
     lambda oz: oz.ozemu_dgemm_host_2limb(4, 4, 4, FAKE, 4, FAKE, 4, NULL, 4, 16, NULL),  # null C
+    lambda oz: oz.ozemu_igemm_s4s8(-1, 4, 4, FAKE, FAKE, FAKE, NULL),
+    lambda oz: oz.ozemu_igemm_s4s8(4, 4, 4, FAKE, FAKE, NULL, NULL),                # null C32
+    lambda oz: oz.ozemu_igemm_s4s8(4, 4, 4, NULL, FAKE, FAKE, NULL),                # null A
+    lambda oz: oz.ozemu_split_rows_s4(4, 4, FAKE, 3, FAKE, NULL),                   # ldx < k
+    lambda oz: oz.ozemu_split_rows_s4(4, 4, FAKE, 4, FAKE + 8, NULL),               # unaligned planes
+    lambda oz: oz.ozemu_split_cols_s8_four(4, 4, FAKE, 3, FAKE, NULL),              # ldx < cols
+    lambda oz: oz.ozemu_split_cols_s8_four(4, 4, NULL, 4, FAKE, NULL),              # null X
 ])
 def test_invalid_arguments_rejected_on_host(oz, call):
     assert call(oz) == oz.OZEMU_ERR_INVALID_ARG
@@ -173,6 +180,16 @@ def test_invalid_arguments_rejected_on_host(oz, call):
 def test_k_overflow_rejected_on_host(oz):
     assert oz.ozemu_igemm_s8(4, 4, 131072, FAKE, FAKE, FAKE, NULL) == oz.OZEMU_ERR_K_OVERFLOW
     assert oz.ozemu_limb_gemm_s32(4, 4, 131072, FAKE, FAKE, FAKE, 4, NULL) == oz.OZEMU_ERR_K_OVERFLOW
+    # INT4 x INT8: |C| <= 1024 k must stay below 2^31.
+    assert oz.ozemu_igemm_s4s8(4, 4, 2097152, FAKE, FAKE, FAKE, NULL) == oz.OZEMU_ERR_K_OVERFLOW
+
+
+def test_four_plane_layout_size(oz):
+    # [rows_p][k_p/128][4][64]: 2 k_p bytes per padded row.
+    assert oz.ozemu_four_plane_bytes(1, 1) == 128 * 2 * 128
+    assert oz.ozemu_four_plane_bytes(129, 129) == 256 * 2 * 256
+    assert oz.ozemu_four_plane_bytes(-1, 4) == 0
+    assert oz.OZEMU_ERR_RANGE == -9
 
 
 def test_narrow_limit(oz):
@@ -186,6 +203,8 @@ def test_empty_problems_are_noops(oz):
     assert oz.ozemu_igemm_s8(0, 0, 7, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
     assert oz.ozemu_split_rows_f64(0, 9, NULL, 9, 30, 13, NULL, NULL, NULL) == oz.OZEMU_OK
     assert oz.ozemu_residue_gemm(0, 3, 3, 13, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_igemm_s4s8(0, 3, 3, NULL, NULL, NULL, NULL) == oz.OZEMU_OK
+    assert oz.ozemu_split_rows_s4(0, 9, NULL, 9, NULL, NULL) == oz.OZEMU_OK
 
 
 def test_product_path_has_no_fallback():
