@@ -117,3 +117,30 @@ def test_s4s8_4096(oz):
     C = oz.igemm_s4s8(to_dev(A), to_dev(B)).cpu().numpy().astype(np.int64)
     assert oz.get_status() == oz.OZEMU_OK
     np.testing.assert_array_equal(C, exact_product(A, B))
+
+
+def test_s4s8_degenerate_k(oz):
+    B = np.ones((1, 70), dtype=np.int8) * -128
+    A = np.full((33, 1), 7, dtype=np.int8)
+    C = oz.igemm_s4s8(to_dev(A), to_dev(B)).cpu().numpy()
+    assert oz.get_status() == oz.OZEMU_OK
+    assert (C == -896).all()
+    # k = 0 zeroes C.
+    Cd = torch.full((5, 6), 123, dtype=torch.int32, device=DEV)
+    st = oz.ozemu_igemm_s4s8(5, 6, 0, 0, 0, Cd.data_ptr(), oz._stream())
+    assert st == oz.OZEMU_OK and (Cd.cpu().numpy() == 0).all()
+
+
+def test_split_rows_s4_padded_leading_dimension(oz):
+    rng = np.random.default_rng(5)
+    k, ldx = 200, 256
+    X = rng.integers(-8, 8, (140, ldx), dtype=np.int8)
+    planes = torch.zeros(oz.ozemu_four_plane_bytes(140, k), dtype=torch.uint8, device=DEV)
+    st = oz.ozemu_split_rows_s4(140, k, to_dev(X).data_ptr(), ldx, planes.data_ptr(), oz._stream())
+    assert st == oz.OZEMU_OK and oz.get_status() == oz.OZEMU_OK
+    digits, _ = decode_planes(planes.cpu().numpy(), 140, k, 1, limbs=4)
+    table = q.a_table()
+    lut = np.array([table[v] for v in range(-8, 8)])  # (16, 4)
+    want = lut[X[:, :k].astype(np.int64) + 8]          # (140, k, 4)
+    np.testing.assert_array_equal(np.moveaxis(digits[0, :, :140, :k], 0, -1), want)
+    assert (digits[0, :, :, k:] == 0).all() and (digits[0, :, 140:, :] == 0).all()
